@@ -1,0 +1,205 @@
+"""CPU oracle for the affine-4-bit dequantising GEMV -- TEST INFRASTRUCTURE.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package. The product path (the CUDA library and
+its Python binding) never loads it and never falls back to it.
+
+The arithmetic lives in ``q4a_oracle.c`` (plain single-threaded C, IEEE double
+precision, no code shared with the CUDA path). This module compiles it with
+gcc on first use (or through ``build()``) and wraps it with ctypes for numpy
+arrays.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4a_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_q4a.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle_q4a.so`` (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11",
+                               "-fno-fast-math", "-ffp-contract=off", "-fvisibility=hidden",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int64
+        D = ctypes.c_double
+        sig = {
+            "q4o_half_value": (D, [ctypes.c_uint16]),
+            "q4o_bf16_value": (D, [ctypes.c_uint16]),
+            "q4o_half_round": (ctypes.c_uint16, [D]),
+            "q4o_pack": (None, [P, P, I, I]),
+            "q4o_unpack": (None, [P, P, I, I]),
+            "q4o_dequant": (None, [P, P, P, P, I, I]),
+            "q4o_xsum": (None, [P, P, I, I]),
+            "q4o_gemv": (None, [P, P, P, P, P, P, I, I, I]),
+            "q4o_gemv_factored": (None, [P, P, P, P, P, I, I, I]),
+            "q4o_gemv_entries": (None, [P, P, P, P, I, P, P, P, P, I]),
+            "q4o_gemv_experts": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
+            "q4o_rmsnorm_f16": (None, [P, P, P, P, D, D, I, I]),
+            "q4o_silu_mul_f16": (None, [P, P, I, I]),
+            "q4o_route_topk": (None, [P, P, P, I, I, I]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0) if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+# ---- scalar format helpers ----------------------------------------------------
+
+def half_value(bits: int) -> float:
+    return _load().q4o_half_value(int(bits))
+
+
+def bf16_value(bits: int) -> float:
+    return _load().q4o_bf16_value(int(bits))
+
+
+def half_round(v: float) -> int:
+    return int(_load().q4o_half_round(float(v)))
+
+
+# ---- array functions -------------------------------------------------------------
+
+def pack(codes: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    rows, in_dim = codes.shape
+    out = np.empty((rows, in_dim // 2), np.uint8)
+    _load().q4o_pack(_p(out), _p(codes), rows, in_dim)
+    return out
+
+
+def unpack(packed: np.ndarray, in_dim: int) -> np.ndarray:
+    packed = _c(packed, np.uint8)
+    rows = packed.shape[0]
+    out = np.empty((rows, in_dim), np.uint8)
+    _load().q4o_unpack(_p(out), _p(packed), rows, in_dim)
+    return out
+
+
+def dequant(packed, s, b, in_dim: int) -> np.ndarray:
+    packed, s, b = _c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16)
+    rows = packed.shape[0]
+    out = np.empty((rows, in_dim), np.float64)
+    _load().q4o_dequant(_p(out), _p(packed), _p(s), _p(b), rows, in_dim)
+    return out
+
+
+def xsum(x_bits: np.ndarray) -> np.ndarray:
+    x_bits = _c(x_bits, np.uint16)
+    nb, in_dim = x_bits.shape
+    out = np.empty((nb, in_dim // 64), np.float64)
+    _load().q4o_xsum(_p(out), _p(x_bits), nb, in_dim)
+    return out
+
+
+def gemv(packed, s, b, x_bits, out_dim: int | None = None):
+    """Returns (y [nb][out], bound [nb][out]) in float64."""
+    packed, s, b, x_bits = (_c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16),
+                            _c(x_bits, np.uint16))
+    nb, in_dim = x_bits.shape
+    out_dim = packed.shape[0] if out_dim is None else out_dim
+    y = np.empty((nb, out_dim), np.float64)
+    bound = np.empty((nb, out_dim), np.float64)
+    _load().q4o_gemv(_p(y), _p(bound), _p(packed), _p(s), _p(b), _p(x_bits), nb, out_dim, in_dim)
+    return y, bound
+
+
+def gemv_factored(packed, s, b, x_bits) -> np.ndarray:
+    packed, s, b, x_bits = (_c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16),
+                            _c(x_bits, np.uint16))
+    nb, in_dim = x_bits.shape
+    out_dim = packed.shape[0]
+    y = np.empty((nb, out_dim), np.float64)
+    _load().q4o_gemv_factored(_p(y), _p(packed), _p(s), _p(b), _p(x_bits), nb, out_dim, in_dim)
+    return y
+
+
+def gemv_entries(packed, s, b, x_bits, r_idx, o_idx):
+    """y[k] = (W x)[r_idx[k]][o_idx[k]] and its bound, one dot product each."""
+    packed, s, b, x_bits = (_c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16),
+                            _c(x_bits, np.uint16))
+    r_idx, o_idx = _c(r_idx, np.int64), _c(o_idx, np.int64)
+    n = r_idx.shape[0]
+    in_dim = x_bits.shape[1]
+    y = np.empty(n, np.float64)
+    bound = np.empty(n, np.float64)
+    _load().q4o_gemv_entries(_p(y), _p(bound), _p(r_idx), _p(o_idx), n, _p(packed), _p(s),
+                             _p(b), _p(x_bits), in_dim)
+    return y, bound
+
+
+def gemv_experts(w_bank, s_bank, b_bank, x_bits, x_rows, expert_ids, token_offsets,
+                 n_experts: int, out_dim: int):
+    w_bank, s_bank, b_bank = _c(w_bank, np.uint8), _c(s_bank, np.uint16), _c(b_bank, np.uint16)
+    x_bits = _c(x_bits, np.uint16)
+    expert_ids = _c(expert_ids, np.int32)
+    token_offsets = _c(token_offsets, np.int32)
+    xr = None if x_rows is None else _c(x_rows, np.int32)
+    in_dim = x_bits.shape[1]
+    n_active = expert_ids.shape[0]
+    n_rows = int(token_offsets[-1])
+    y = np.empty((n_rows, out_dim), np.float64)
+    bound = np.empty((n_rows, out_dim), np.float64)
+    _load().q4o_gemv_experts(_p(y), _p(bound), _p(w_bank), _p(s_bank), _p(b_bank), _p(x_bits),
+                             _p(xr), _p(expert_ids), _p(token_offsets), n_active, n_experts,
+                             out_dim, in_dim)
+    return y, bound
+
+
+def rmsnorm_f16(x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0):
+    """Returns (xn fp16 bits [nb][n], inv_rms [nb])."""
+    x_raw, norm_w = _c(x_raw, np.float32), _c(norm_w, np.uint16)
+    nb, n = x_raw.shape
+    xn = np.empty((nb, n), np.uint16)
+    inv = np.empty(nb, np.float64)
+    _load().q4o_rmsnorm_f16(_p(xn), _p(inv), _p(x_raw), _p(norm_w), float(eps), float(shift), nb, n)
+    return xn, inv
+
+
+def silu_mul_f16(gate_up) -> np.ndarray:
+    gate_up = _c(gate_up, np.float32)
+    rows, two_inter = gate_up.shape
+    inter = two_inter // 2
+    h = np.empty((rows, inter), np.uint16)
+    _load().q4o_silu_mul_f16(_p(h), _p(gate_up), rows, inter)
+    return h
+
+
+def route_topk(logits, top_k: int):
+    """Returns (idx int32 [n_tok][k], weights float64 [n_tok][k])."""
+    logits = _c(logits, np.float32)
+    n_tok, n_exp = logits.shape
+    idx = np.empty((n_tok, top_k), np.int32)
+    wts = np.empty((n_tok, top_k), np.float64)
+    _load().q4o_route_topk(_p(idx), _p(wts), _p(logits), n_tok, n_exp, top_k)
+    return idx, wts

@@ -1,0 +1,394 @@
+/*
+ * q4a_oracle.c -- CPU oracle for the row-batched affine-4-bit dequantising
+ * matrix-vector product.
+ *
+ * TEST INFRASTRUCTURE, NOT THE PRODUCT. Only the test-suite, the smoke check
+ * and the benchmark's CPU-baseline leg load this file's library. It is plain,
+ * single-threaded C computing in IEEE double precision. It shares no code,
+ * header, table, constant generator or helper with the CUDA library: its own
+ * binary16 / bfloat16 decoders, its own nibble extraction, its own loops.
+ *
+ * Sources (web pages; cited by page and section):
+ *   [BATCH_MSL]  "BATCH_MSL" constant page (cherenkov kernels), a Metal kernel
+ *                library. Sections used: quantized_rows.metal (fn_q4_rows_h,
+ *                fn_q4_2rows_h: the affine-Q4 row dot products),
+ *                hyperconnection.metal (fn_group_norm_b, fn_norm_prep_b,
+ *                fn_qmv_silu_b), experts.metal (fn_topk_softmax_b,
+ *                fn_moe_gate_up_b, fn_moe_act_b, fn_moe_down_b),
+ *                expert_gemm.metal (fn_expert_qmm) and the prefill helper
+ *                fn_qmv_small_b (explicit nibble order and affine form).
+ *   [MEMRA]      memra-engine qwen4exp_gpu.rs source page: host reference math
+ *                (host_route_softmax_topk with its denominator floor,
+ *                f32_to_bf16_rne).
+ *
+ * What the method computes (spec contract, restated):
+ *   W is [out][in] with 4-bit codes q in 0..15; byte k of a packed row holds
+ *   element 2k in its low nibble and element 2k+1 in its high nibble. Every
+ *   run of 64 inputs (a group g) has a bfloat16 scale s[o][g] and bias
+ *   b[o][g]; the weight is w = s*q + b ([BATCH_MSL] fn_expert_qmm stages
+ *   fma(s, code, b)), so that
+ *       y[r][o] = sum_g ( s[o][g] * sum_{i in g} q[o][i]*x[r][i]
+ *                         + b[o][g] * xsum[r][g] )
+ *   ([BATCH_MSL] fn_q4_rows_h accumulates s*sum(q x) + b*xsum per chunk;
+ *   fn_qmv_small_b writes the same with the nibble order explicit).
+ *   The oracle evaluates the plain definition: it dequantises W explicitly and
+ *   forms the dot products in index order, in double precision.
+ *
+ * Parity pins: every exported function is checked in tests/test_oracle_pins.py
+ * against hand-worked examples (tests/golden/), closed forms, invariants and
+ * pure-Python brute force on tiny shapes.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define Q4O_EXPORT __attribute__((visibility("default")))
+
+/* ---- storage formats ---------------------------------------------------- */
+
+/* IEEE binary16 -> double (exact for every pattern). */
+static double half_value(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* zero / subnormal */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 1024), e - 25);     /* 1.m * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double (the upper half of an fp32 pattern; exact). */
+static double bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> IEEE binary16, round to nearest, ties to even. */
+static uint16_t half_round(double v)
+{
+    if (isnan(v))
+        return 0x7E00;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a >= 65520.0)                              /* max 65504 + half an ulp */
+        return sign | 0x7C00;
+    if (a < ldexp(1.0, -14)) {                     /* subnormal: m * 2^-24 */
+        double m = nearbyint(ldexp(a, 24));        /* 1024 rolls into 0x0400 */
+        return sign | (uint16_t)m;
+    }
+    int e;
+    double f = frexp(a, &e);                       /* a = f * 2^e, f in [0.5,1) */
+    double r = nearbyint(ldexp(f, 11));            /* 1024 .. 2048 */
+    int biased = e - 1 + 15;
+    if (r >= 2048.0) {
+        r = 1024.0;
+        biased += 1;
+    }
+    if (biased >= 31)
+        return sign | 0x7C00;
+    return sign | (uint16_t)(biased << 10) | (uint16_t)((int)r - 1024);
+}
+
+/* The code of element i of a packed row: low nibble of byte i/2 for even i,
+ * high nibble for odd i (spec layout; [BATCH_MSL] fn_q4_rows_h pairs the
+ * low nibbles with the even x stream and the high nibbles with the odd one). */
+static int code_at(const uint8_t* row, int64_t i)
+{
+    uint8_t byte = row[i >> 1];
+    return (i & 1) ? (byte >> 4) : (byte & 0x0F);
+}
+
+/* ---- exported helpers for the tests ------------------------------------- */
+
+Q4O_EXPORT double q4o_half_value(uint16_t h) { return half_value(h); }
+Q4O_EXPORT double q4o_bf16_value(uint16_t b) { return bf16_value(b); }
+Q4O_EXPORT uint16_t q4o_half_round(double v) { return half_round(v); }
+
+/* ---- A1: packing -------------------------------------------------------- */
+
+/* codes[rows][in_dim] (one code per byte, masked to 4 bits as the prefill
+ * helper fn_qmv_small_b masks each nibble) -> packed[rows][in_dim/2]. */
+Q4O_EXPORT void q4o_pack(uint8_t* packed, const uint8_t* codes, int64_t rows, int64_t in_dim)
+{
+    for (int64_t o = 0; o < rows; o++) {
+        for (int64_t k = 0; k < in_dim / 2; k++) {
+            int lo = codes[o * in_dim + 2 * k] & 0x0F;
+            int hi = codes[o * in_dim + 2 * k + 1] & 0x0F;
+            packed[o * (in_dim / 2) + k] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+Q4O_EXPORT void q4o_unpack(uint8_t* codes, const uint8_t* packed, int64_t rows, int64_t in_dim)
+{
+    for (int64_t o = 0; o < rows; o++)
+        for (int64_t i = 0; i < in_dim; i++)
+            codes[o * in_dim + i] = (uint8_t)code_at(packed + o * (in_dim / 2), i);
+}
+
+/* ---- explicit dequantisation -------------------------------------------- */
+
+static void dequant_row(double* w, const uint8_t* prow, const uint16_t* srow,
+                        const uint16_t* brow, int64_t in_dim)
+{
+    for (int64_t i = 0; i < in_dim; i++) {
+        double s = bf16_value(srow[i / 64]);
+        double b = bf16_value(brow[i / 64]);
+        w[i] = s * (double)code_at(prow, i) + b;
+    }
+}
+
+/* W[rows][in_dim] = s*q + b, in double (exact: a bf16 times a 4-bit integer
+ * has at most 12 significant bits). */
+Q4O_EXPORT void q4o_dequant(double* w, const uint8_t* packed, const uint16_t* s,
+                            const uint16_t* b, int64_t rows, int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    for (int64_t o = 0; o < rows; o++)
+        dequant_row(w + o * in_dim, packed + o * (in_dim / 2), s + o * groups,
+                    b + o * groups, in_dim);
+}
+
+/* ---- A2: per-64-group sums of the fp16 activations ---------------------- */
+
+/* xsum[r][g] = sum_{i in g} x[r][i], in double, index order. The pages keep
+ * per-32 sums (fn_norm_prep_b, fn_moe_act_b); one bias covers both halves of
+ * a 64-group, so the per-64 sum is the sum of the two. */
+Q4O_EXPORT void q4o_xsum(double* xsum, const uint16_t* x, int64_t nb, int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    for (int64_t r = 0; r < nb; r++)
+        for (int64_t g = 0; g < groups; g++) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < 64; i++)
+                acc += half_value(x[r * in_dim + g * 64 + i]);
+            xsum[r * groups + g] = acc;
+        }
+}
+
+/* ---- A4: the GEMV, plain definition ------------------------------------- */
+
+/* y[r][o] = sum_i W[o][i] * x[r][i] with W dequantised explicitly, and the
+ * per-element acceptance bound 2e-3 * sum_i |W[o][i] x[r][i]| + 1e-5.
+ * bound may be NULL. */
+Q4O_EXPORT void q4o_gemv(double* y, double* bound, const uint8_t* packed,
+                         const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                         int64_t nb, int64_t out_dim, int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    double* xv = (double*)malloc((size_t)(nb * in_dim) * sizeof(double));
+    for (int64_t i = 0; i < nb * in_dim; i++)
+        xv[i] = half_value(x[i]);
+    for (int64_t o = 0; o < out_dim; o++) {
+        dequant_row(w, packed + o * (in_dim / 2), s + o * groups, b + o * groups, in_dim);
+        for (int64_t r = 0; r < nb; r++) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < in_dim; i++) {
+                double p = w[i] * xv[r * in_dim + i];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[r * out_dim + o] = acc;
+            if (bound)
+                bound[r * out_dim + o] = 2e-3 * mag + 1e-5;
+        }
+    }
+    free(xv);
+    free(w);
+}
+
+/* The same product in the factored form the kernels use per group:
+ * sum_g ( s * sum q x + b * xsum ). Asserted equal to q4o_gemv (up to double
+ * rounding) by the pins; not used for parity. */
+Q4O_EXPORT void q4o_gemv_factored(double* y, const uint8_t* packed, const uint16_t* s,
+                                  const uint16_t* b, const uint16_t* x, int64_t nb,
+                                  int64_t out_dim, int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    for (int64_t o = 0; o < out_dim; o++) {
+        const uint8_t* prow = packed + o * (in_dim / 2);
+        for (int64_t r = 0; r < nb; r++) {
+            double acc = 0.0;
+            for (int64_t g = 0; g < groups; g++) {
+                double qx = 0.0, xs = 0.0;
+                for (int64_t i = g * 64; i < g * 64 + 64; i++) {
+                    double xv = half_value(x[r * in_dim + i]);
+                    qx += (double)code_at(prow, i) * xv;
+                    xs += xv;
+                }
+                acc += bf16_value(s[o * groups + g]) * qx + bf16_value(b[o * groups + g]) * xs;
+            }
+            y[r * out_dim + o] = acc;
+        }
+    }
+}
+
+/* Selected entries (r_idx[k], o_idx[k]) of the plain-definition product, one
+ * dot product each: the full-size parity checks sample outputs this way. */
+Q4O_EXPORT void q4o_gemv_entries(double* y, double* bound, const int64_t* r_idx,
+                                 const int64_t* o_idx, int64_t n, const uint8_t* packed,
+                                 const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                                 int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    for (int64_t k = 0; k < n; k++) {
+        int64_t o = o_idx[k], r = r_idx[k];
+        dequant_row(w, packed + o * (in_dim / 2), s + o * groups, b + o * groups, in_dim);
+        double acc = 0.0, mag = 0.0;
+        for (int64_t i = 0; i < in_dim; i++) {
+            double p = w[i] * half_value(x[r * in_dim + i]);
+            acc += p;
+            mag += fabs(p);
+        }
+        y[k] = acc;
+        if (bound)
+            bound[k] = 2e-3 * mag + 1e-5;
+    }
+    free(w);
+}
+
+/* ---- A6: routed-expert banks -------------------------------------------- */
+
+/* For segment a (expert e = expert_ids[a], slot rows token_offsets[a] ..
+ * token_offsets[a+1]-1): y[r] = W_e . x[x_rows ? x_rows[r] : r].
+ * The bank holds experts back to back: rows e*out_dim .. (e+1)*out_dim-1.
+ * A segment whose expert id is outside [0, n_experts) yields NaN rows
+ * (the library's device convention for such a segment). */
+Q4O_EXPORT void q4o_gemv_experts(double* y, double* bound, const uint8_t* w_bank,
+                                 const uint16_t* s_bank, const uint16_t* b_bank,
+                                 const uint16_t* x, const int32_t* x_rows,
+                                 const int32_t* expert_ids, const int32_t* token_offsets,
+                                 int64_t n_active, int64_t n_experts, int64_t out_dim,
+                                 int64_t in_dim)
+{
+    int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    for (int64_t a = 0; a < n_active; a++) {
+        int64_t e = expert_ids[a];
+        for (int64_t r = token_offsets[a]; r < token_offsets[a + 1]; r++) {
+            if (e < 0 || e >= n_experts) {
+                for (int64_t o = 0; o < out_dim; o++) {
+                    y[r * out_dim + o] = NAN;
+                    if (bound)
+                        bound[r * out_dim + o] = NAN;
+                }
+            }
+        }
+        if (e < 0 || e >= n_experts)
+            continue;
+        for (int64_t o = 0; o < out_dim; o++) {
+            int64_t row = e * out_dim + o;
+            dequant_row(w, w_bank + row * (in_dim / 2), s_bank + row * groups,
+                        b_bank + row * groups, in_dim);
+            for (int64_t r = token_offsets[a]; r < token_offsets[a + 1]; r++) {
+                int64_t src = x_rows ? x_rows[r] : r;
+                double acc = 0.0, mag = 0.0;
+                for (int64_t i = 0; i < in_dim; i++) {
+                    double p = w[i] * half_value(x[src * in_dim + i]);
+                    acc += p;
+                    mag += fabs(p);
+                }
+                y[r * out_dim + o] = acc;
+                if (bound)
+                    bound[r * out_dim + o] = 2e-3 * mag + 1e-5;
+            }
+        }
+    }
+    free(w);
+}
+
+/* ---- A3: RMSNorm prologue ------------------------------------------------ */
+
+/* [BATCH_MSL] fn_group_norm_b with one group per row:
+ *   xn[r][i] = x[r][i] * 1/sqrt(mean_i x[r][i]^2 + eps) * (w[i] + shift),
+ * evaluated in double and rounded once to binary16 (the fp16 operand the
+ * GEMV multiplies). inv_rms (may be NULL) receives the per-row factor. */
+Q4O_EXPORT void q4o_rmsnorm_f16(uint16_t* xn, double* inv_rms, const float* x,
+                                const uint16_t* w, double eps, double shift,
+                                int64_t nb, int64_t n)
+{
+    for (int64_t r = 0; r < nb; r++) {
+        double ss = 0.0;
+        for (int64_t i = 0; i < n; i++) {
+            double v = (double)x[r * n + i];
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / (double)n + eps);
+        if (inv_rms)
+            inv_rms[r] = inv;
+        for (int64_t i = 0; i < n; i++)
+            xn[r * n + i] = half_round((double)x[r * n + i] * inv * (bf16_value(w[i]) + shift));
+    }
+}
+
+/* ---- A7: SiLU(gate) * up -------------------------------------------------- */
+
+/* [BATCH_MSL] fn_moe_act_b: gate_up[r] = [gate (inter) | up (inter)],
+ * h[r][j] = silu(gate[j]) * up[j] with silu(v) = v / (1 + e^-v), in double,
+ * rounded once to binary16. */
+Q4O_EXPORT void q4o_silu_mul_f16(uint16_t* h, const float* gate_up, int64_t rows, int64_t inter)
+{
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t j = 0; j < inter; j++) {
+            double g = (double)gate_up[r * 2 * inter + j];
+            double u = (double)gate_up[r * 2 * inter + inter + j];
+            h[r * inter + j] = half_round(g / (1.0 + exp(-g)) * u);
+        }
+}
+
+/* ---- routing (input generation for the expert workload) ------------------ */
+
+/* [MEMRA] host_route_softmax_topk: softmax over the logits, order experts by
+ * probability (descending) then index (ascending), keep top_k, divide by
+ * max(sum of the kept probabilities, 6.1035156e-5). [BATCH_MSL]
+ * fn_topk_softmax_b breaks ties toward the lower index the same way.
+ * Double precision throughout. */
+Q4O_EXPORT void q4o_route_topk(int32_t* idx, double* wts, const float* logits,
+                               int64_t n_tok, int64_t n_exp, int64_t top_k)
+{
+    double* p = (double*)malloc((size_t)n_exp * sizeof(double));
+    char* taken = (char*)malloc((size_t)n_exp);
+    for (int64_t t = 0; t < n_tok; t++) {
+        const float* l = logits + t * n_exp;
+        double mx = -INFINITY;
+        for (int64_t e = 0; e < n_exp; e++)
+            if ((double)l[e] > mx)
+                mx = (double)l[e];
+        double sum = 0.0;
+        for (int64_t e = 0; e < n_exp; e++) {
+            p[e] = exp((double)l[e] - mx);
+            sum += p[e];
+        }
+        for (int64_t e = 0; e < n_exp; e++) {
+            p[e] /= sum;
+            taken[e] = 0;
+        }
+        double chosen = 0.0;
+        for (int64_t k = 0; k < top_k; k++) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < n_exp; e++)
+                if (!taken[e] && (best < 0 || p[e] > p[best]))
+                    best = e;                      /* strict '>' keeps the lower index on ties */
+            taken[best] = 1;
+            idx[t * top_k + k] = (int32_t)best;
+            wts[t * top_k + k] = p[best];
+            chosen += p[best];
+        }
+        double denom = chosen > 6.1035156e-5 ? chosen : 6.1035156e-5;
+        for (int64_t k = 0; k < top_k; k++)
+            wts[t * top_k + k] /= denom;
+    }
+    free(taken);
+    free(p);
+}

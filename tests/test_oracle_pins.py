@@ -1,0 +1,353 @@
+"""Pins for the CPU oracle: it is checked here against things other than itself.
+
+Hand-worked examples (tests/golden/), closed forms, invariants, exact rational
+arithmetic, numpy/math library routines and brute force on tiny inputs. Each
+pin is chosen so that a plausible slip in the oracle (swapped nibbles, a wrong
+group index, scale and bias exchanged, a dropped bias term, transposed rows and
+tokens, a wrong tie rule) fails at least one of them.
+"""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import q4a_workloads as wl
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def ramp_codes():
+    i = np.arange(64)
+    return np.stack([i % 16, 15 - (i % 16)]).astype(np.uint8)
+
+
+def bf16(vals):
+    return wl.f32_to_bf16_bits(np.asarray(vals, np.float32))
+
+
+# ---- storage-format decoders ------------------------------------------------------
+
+def test_half_decoder_matches_numpy_on_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_value(int(b)) for b in bits[::7]])
+    r = ref[::7]
+    both_nan = np.isnan(got) & np.isnan(r)
+    assert np.all(both_nan | (got == r))
+
+
+def test_bf16_decoder_matches_fp32_upper_half():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 65536, size=5000).astype(np.uint16)
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_value(int(b)) for b in bits])
+    assert np.all((got == ref) | (np.isnan(got) & np.isnan(ref)))
+
+
+def test_half_round_matches_numpy_round_to_nearest_even():
+    rng = np.random.default_rng(2)
+    vals = np.concatenate([
+        rng.normal(0, 1, 3000), rng.normal(0, 1e-5, 1000), rng.normal(0, 3e4, 500),
+        # exact ties between neighbouring binary16 values
+        (np.arange(1024, 1100) + 0.5) / 1024.0, (np.arange(0, 40) + 0.5) * 2.0 ** -24,
+        [65504.0, 65519.99, 65520.0, -65520.0, 1e9, 0.0, -0.0, 2.0 ** -25, 3 * 2.0 ** -26],
+    ])
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.half_round(v) for v in vals], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---- A1 packing ---------------------------------------------------------------------
+
+def test_pack_matches_hand_worked_bytes(golden):
+    g = golden("pack_ramp.txt")
+    packed = oracle.pack(ramp_codes())
+    for row, key in ((0, "row0_period_bytes"), (1, "row1_period_bytes")):
+        period = bytes(int(h, 16) for h in g[key])
+        assert bytes(packed[row]) == period * 4
+    words = packed.view("<u4")
+    assert [int(w) for w in words[0, :2]] == [int(v, 16) for v in g["row0_words"]]
+    assert [int(w) for w in words[1, :2]] == [int(v, 16) for v in g["row1_words"]]
+
+
+def test_pack_unpack_round_trip_and_mask():
+    codes = wl.codes(99, 0, 7, 192)
+    assert np.array_equal(oracle.unpack(oracle.pack(codes), 192), codes)
+    wide = np.random.default_rng(3).integers(0, 256, size=(3, 64), dtype=np.uint8)
+    assert np.array_equal(oracle.unpack(oracle.pack(wide), 64), wide & 0x0F)
+
+
+# ---- A4 GEMV --------------------------------------------------------------------------
+
+def test_gemv_hand_worked_2x64(golden):
+    g = golden("gemv_2x64.txt")
+    packed = oracle.pack(ramp_codes())
+    s = bf16([[float(v)] for v in g["scale"]])
+    b = bf16([[float(v)] for v in g["bias"]])
+    x1 = wl.f16_bits(np.ones((1, 64)))
+    x2 = wl.f16_bits(((-1.0) ** np.arange(64))[None, :])
+    y1, _ = oracle.gemv(packed, s, b, x1)
+    y2, _ = oracle.gemv(packed, s, b, x2)
+    assert list(y1[0]) == [float(v) for v in g["x_ones_y"]]
+    assert list(y2[0]) == [float(v) for v in g["x_alternating_y"]]
+
+
+def _brute_force(codes, s_bits, b_bits, x_bits):
+    """Dense float64 product from the UNPACKED codes (never the packed bytes)."""
+    s = wl.bf16_bits_to_f32(s_bits).astype(np.float64)
+    b = wl.bf16_bits_to_f32(b_bits).astype(np.float64)
+    w = codes.astype(np.float64) * np.repeat(s, 64, axis=1) + np.repeat(b, 64, axis=1)
+    x = x_bits.view(np.float16).astype(np.float64)
+    return x @ w.T, np.abs(x) @ np.abs(w).T
+
+
+@pytest.mark.parametrize("out_dim,in_dim,nb", [(1, 64, 1), (3, 128, 2), (8, 64, 3), (5, 192, 3), (2, 128, 1)])
+def test_gemv_brute_force_tiny(out_dim, in_dim, nb):
+    rng = np.random.default_rng(out_dim * 1000 + in_dim + nb)
+    codes = rng.integers(0, 16, size=(out_dim, in_dim), dtype=np.uint8)
+    codes[0, :16] = np.arange(16)            # every code value appears
+    s = bf16(np.abs(rng.normal(0, 0.5, (out_dim, in_dim // 64))))
+    b = bf16(rng.normal(0, 1.0, (out_dim, in_dim // 64)))
+    x = wl.f16_bits(rng.normal(0, 1, (nb, in_dim)))
+    y, bound = oracle.gemv(oracle.pack(codes), s, b, x)
+    ref, mag = _brute_force(codes, s, b, x)
+    assert y.shape == (nb, out_dim)
+    assert np.all(np.abs(y - ref) <= 1e-12 * mag + 1e-300)
+    assert np.allclose(bound, 2e-3 * mag + 1e-5, rtol=1e-12, atol=0)
+
+
+def test_gemv_exact_rational():
+    """Power-of-two scales, integer biases and integer x: every product and sum is
+    exact in double, so the oracle must equal the rational result exactly."""
+    rng = np.random.default_rng(5)
+    out_dim, in_dim, nb = 4, 128, 2
+    codes = rng.integers(0, 16, size=(out_dim, in_dim), dtype=np.uint8)
+    s_val = 2.0 ** rng.integers(-6, 2, size=(out_dim, 2))
+    b_val = rng.integers(-5, 6, size=(out_dim, 2)).astype(np.float64)
+    x_val = rng.integers(-8, 9, size=(nb, in_dim)).astype(np.float64)
+    y, _ = oracle.gemv(oracle.pack(codes), bf16(s_val), bf16(b_val), wl.f16_bits(x_val))
+    for r in range(nb):
+        for o in range(out_dim):
+            exact = sum(Fraction(s_val[o, i // 64]) * int(codes[o, i]) * int(x_val[r, i])
+                        + Fraction(b_val[o, i // 64]) * int(x_val[r, i]) for i in range(in_dim))
+            assert Fraction(y[r, o]) == exact
+
+
+def _case(seed, out_dim=6, in_dim=256, nb=3):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(out_dim, in_dim), dtype=np.uint8)
+    s = bf16(np.abs(rng.normal(0, 0.02, (out_dim, in_dim // 64))))
+    b = bf16(-8 * rng.normal(0, 0.01, (out_dim, in_dim // 64)))
+    x = wl.f16_bits(rng.normal(0, 1, (nb, in_dim)))
+    return codes, s, b, x
+
+
+def test_closed_forms_codes_zero_and_fifteen_and_scale_zero():
+    codes, s, b, x = _case(6)
+    xs = oracle.xsum(x)                                   # [nb][G]
+    sv = wl.bf16_bits_to_f32(s).astype(np.float64)
+    bv = wl.bf16_bits_to_f32(b).astype(np.float64)
+    zero = np.zeros_like(codes)
+    y0, _ = oracle.gemv(oracle.pack(zero), s, b, x)
+    assert np.allclose(y0, xs @ bv.T, rtol=1e-12, atol=1e-12)
+    fifteen = np.full_like(codes, 15)
+    y15, _ = oracle.gemv(oracle.pack(fifteen), s, bf16(np.zeros_like(bv)), x)
+    assert np.allclose(y15, 15 * (xs @ sv.T), rtol=1e-12, atol=1e-12)
+    ys0, _ = oracle.gemv(oracle.pack(codes), bf16(np.zeros_like(sv)), b, x)
+    assert np.allclose(ys0, xs @ bv.T, rtol=1e-12, atol=1e-12)
+
+
+def test_linearity_in_x():
+    codes, s, b, x = _case(7)
+    p = oracle.pack(codes)
+    y, _ = oracle.gemv(p, s, b, x)
+    neg = wl.f16_bits(-x.view(np.float16).astype(np.float32))
+    dbl = wl.f16_bits(2 * x.view(np.float16).astype(np.float32))
+    yn, _ = oracle.gemv(p, s, b, neg)
+    yd, _ = oracle.gemv(p, s, b, dbl)
+    assert np.array_equal(yn, -y)
+    assert np.array_equal(yd, 2 * y)
+    # additivity on integer activations (sums stay exact in binary16)
+    rng = np.random.default_rng(8)
+    x1 = rng.integers(-20, 21, size=x.shape).astype(np.float32)
+    x2 = rng.integers(-20, 21, size=x.shape).astype(np.float32)
+    ya, _ = oracle.gemv(p, s, b, wl.f16_bits(x1))
+    yb, _ = oracle.gemv(p, s, b, wl.f16_bits(x2))
+    yab, _ = oracle.gemv(p, s, b, wl.f16_bits(x1 + x2))
+    assert np.allclose(yab, ya + yb, rtol=1e-12, atol=1e-9)
+
+
+def test_explicit_equals_factored_form():
+    codes, s, b, x = _case(9, out_dim=5, in_dim=320, nb=4)
+    p = oracle.pack(codes)
+    y, bound = oracle.gemv(p, s, b, x)
+    yf = oracle.gemv_factored(p, s, b, x)
+    assert np.all(np.abs(y - yf) <= 1e-9 * bound)
+
+
+def test_rows_and_tokens_are_not_transposed():
+    codes, s, b, x = _case(10, out_dim=3, in_dim=128, nb=2)
+    y, _ = oracle.gemv(oracle.pack(codes), s, b, x)
+    ref, _ = _brute_force(codes, s, b, x)
+    assert y.shape == (2, 3)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # moving one token row moves only that output row
+    x2 = x.copy()
+    x2[1] = x[0]
+    y2, _ = oracle.gemv(oracle.pack(codes), s, b, x2)
+    assert np.array_equal(y2[0], y[0]) and np.array_equal(y2[1], y[0])
+
+
+def test_entries_match_full_product():
+    codes, s, b, x = _case(11, out_dim=9, in_dim=192, nb=3)
+    p = oracle.pack(codes)
+    y, bound = oracle.gemv(p, s, b, x)
+    r = np.array([0, 2, 1, 2]); o = np.array([8, 0, 4, 3])
+    ye, be = oracle.gemv_entries(p, s, b, x, r, o)
+    assert np.array_equal(ye, y[r, o]) and np.array_equal(be, bound[r, o])
+
+
+def test_adversarial_scales_propagate():
+    codes, s, b, x = _case(12, out_dim=4, in_dim=128, nb=1)
+    s = s.copy()
+    s[0, 0] = 0x7FC0    # NaN
+    s[1, 1] = 0x7F80    # +inf
+    s[2, 0] = 0x0001    # smallest bf16 subnormal
+    y, _ = oracle.gemv(oracle.pack(codes), s, b, x)
+    assert math.isnan(y[0, 0])
+    assert math.isinf(y[0, 1]) or math.isnan(y[0, 1])
+    assert np.isfinite(y[0, 2:]).all()
+
+
+# ---- A2 xsum -------------------------------------------------------------------------
+
+def test_xsum_groups_and_library_sum():
+    x = np.zeros((2, 192), np.float32)
+    x[0, 63] = 1.0
+    x[0, 64] = 2.0
+    x[1, 191] = -3.0
+    xs = oracle.xsum(wl.f16_bits(x))
+    assert xs.tolist() == [[1.0, 2.0, 0.0], [0.0, 0.0, -3.0]]
+    xr = wl.normal_f16(98, 0, (3, 256))
+    ref = xr.view(np.float16).astype(np.float64).reshape(3, 4, 64).sum(axis=2)
+    assert np.allclose(oracle.xsum(xr), ref, rtol=1e-14, atol=1e-14)
+
+
+# ---- A3 RMSNorm ------------------------------------------------------------------------
+
+def test_rmsnorm_closed_form_and_invariants():
+    x = np.array([[3.0, 4.0, 0.0, 0.0]], np.float32)
+    w = bf16([1.0, 1.0, 1.0, 1.0])
+    xn, inv = oracle.rmsnorm_f16(x, w, eps=0.0)
+    assert inv[0] == pytest.approx(1 / math.sqrt(25 / 4), rel=1e-15)
+    assert xn[0].view(np.float16).tolist() == [float(np.float16(3 * 0.4)), float(np.float16(4 * 0.4)), 0.0, 0.0]
+    a = wl.normal_f32(97, 0, (3, 512))
+    ones = bf16(np.ones(512))
+    xn, _ = oracle.rmsnorm_f16(a, ones, eps=0.0)
+    rms = np.sqrt((xn.view(np.float16).astype(np.float64) ** 2).mean(axis=1))
+    assert np.allclose(rms, 1.0, atol=2e-3)
+    # scale invariance (power-of-two scaling is exact; eps = 0)
+    xn8, _ = oracle.rmsnorm_f16(8 * a, ones, eps=0.0)
+    assert np.array_equal(xn8, xn)
+    # w + shift: (w = 0, shift = 1) equals (w = 1, shift = 0)
+    xs1, _ = oracle.rmsnorm_f16(a, bf16(np.zeros(512)), eps=0.0, shift=1.0)
+    assert np.array_equal(xs1, xn)
+    # weight applies per column
+    wv = wl.norm_weight(97, 1, 512)
+    xw, inv = oracle.rmsnorm_f16(a, wv, eps=1e-6)
+    ref = (a.astype(np.float64) * inv[:, None] * wl.bf16_bits_to_f32(wv).astype(np.float64))
+    assert np.array_equal(xw, wl.f16_bits(ref))
+
+
+# ---- A7 SiLU * up ---------------------------------------------------------------------
+
+def test_silu_mul_special_values_and_library():
+    gu = np.array([[0.0, 1.0, 30.0, -30.0, 2.0, 3.0, -1.5, 7.0]], np.float32)
+    h = oracle.silu_mul_f16(gu).view(np.float16).astype(np.float64)[0]
+    assert h[0] == 0.0
+    assert h[1] == np.float16(1 / (1 + math.exp(-1)) * 3.0)
+    assert h[2] == np.float16(30.0 * -1.5)
+    assert abs(h[3]) < 1e-10
+    rng = np.random.default_rng(13)
+    gu = rng.normal(0, 2, (3, 128)).astype(np.float32)
+    got = oracle.silu_mul_f16(gu)
+    g = gu[:, :64].astype(np.float64)
+    u = gu[:, 64:].astype(np.float64)
+    ref = np.vectorize(lambda a, c: a / (1 + math.exp(-a)) * c)(g, u)
+    assert np.array_equal(got, wl.f16_bits(ref))
+
+
+# ---- routing ----------------------------------------------------------------------------
+
+def test_route_topk_brute_force_and_ties():
+    logits = wl.moe_logits()
+    idx, w = oracle.route_topk(logits, 8)
+    for t in range(logits.shape[0]):
+        l = logits[t].astype(np.float64)
+        p = np.exp(l - l.max())
+        p /= p.sum()
+        order = sorted(range(64), key=lambda e: (-p[e], e))[:8]
+        assert idx[t].tolist() == order
+        assert np.allclose(w[t], p[order] / p[order].sum(), rtol=1e-12)
+        assert w[t].sum() == pytest.approx(1.0, rel=1e-12)
+    ties = np.zeros((1, 6), np.float32)
+    ties[0, 4] = 1.0
+    idx, _ = oracle.route_topk(ties, 3)
+    assert idx[0].tolist() == [4, 0, 1]
+    # the workload generator picks the same experts as the oracle's router
+    r = wl.route_by_logits(logits, 8)
+    oidx, _ = oracle.route_topk(logits, 8)
+    assert np.array_equal(r.chosen, oidx)
+
+
+def test_route_denominator_floor():
+    logits = np.zeros((1, 100000), np.float32)
+    _, w = oracle.route_topk(logits, 1)
+    assert w[0, 0] == pytest.approx(1e-5 / 6.1035156e-5, rel=1e-9)
+
+
+# ---- A6 expert banks -------------------------------------------------------------------
+
+def _bank(seed, n_exp=4, out_dim=6, in_dim=128):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(n_exp * out_dim, in_dim), dtype=np.uint8)
+    s = bf16(np.abs(rng.normal(0, 0.02, (n_exp * out_dim, in_dim // 64))))
+    b = bf16(-8 * rng.normal(0, 0.01, (n_exp * out_dim, in_dim // 64)))
+    return codes, s, b
+
+
+def test_experts_equal_per_expert_dense_product():
+    codes, s, b = _bank(14)
+    x = wl.normal_f16(96, 0, (5, 128))
+    experts = np.array([3, 0, 2], np.int32)
+    offsets = np.array([0, 2, 3, 6], np.int32)
+    x_rows = np.array([4, 1, 0, 2, 3, 1], np.int32)
+    y, _ = oracle.gemv_experts(oracle.pack(codes), s, b, x, x_rows, experts, offsets, 4, 6)
+    for a, e in enumerate(experts):
+        sl = slice(e * 6, (e + 1) * 6)
+        for r in range(offsets[a], offsets[a + 1]):
+            ref, _ = _brute_force(codes[sl], s[sl], b[sl], x[x_rows[r]][None])
+            assert np.allclose(y[r], ref[0], rtol=1e-12, atol=1e-12)
+
+
+def test_experts_permutation_and_invalid_id():
+    codes, s, b = _bank(15)
+    p = oracle.pack(codes)
+    x = wl.normal_f16(95, 0, (4, 128))
+    y, _ = oracle.gemv_experts(p, s, b, x, None, np.array([1, 3], np.int32),
+                               np.array([0, 2, 4], np.int32), 4, 6)
+    # swap the two segments (and their x rows): outputs swap accordingly
+    xs = x[[2, 3, 0, 1]]
+    y2, _ = oracle.gemv_experts(p, s, b, xs, None, np.array([3, 1], np.int32),
+                                np.array([0, 2, 4], np.int32), 4, 6)
+    assert np.array_equal(y2, y[[2, 3, 0, 1]])
+    # x_rows indirection equals a gathered x
+    y3, _ = oracle.gemv_experts(p, s, b, x, np.array([2, 3, 0, 1], np.int32),
+                                np.array([3, 1], np.int32), np.array([0, 2, 4], np.int32), 4, 6)
+    assert np.array_equal(y3, y2)
+    y4, _ = oracle.gemv_experts(p, s, b, x, None, np.array([7, 0], np.int32),
+                                np.array([0, 1, 4], np.int32), 4, 6)
+    assert np.isnan(y4[0]).all() and np.isfinite(y4[1:]).all()
