@@ -1,0 +1,211 @@
+// q4a_api.cu -- the C ABI of libq4a.so: argument validation, segment scheduling and
+// dispatch to the kernels. Every check runs on the host before anything is launched.
+#include <string.h>
+
+#include <vector>
+
+#include "q4a_internal.h"
+
+namespace q4a {
+
+static thread_local int t_last_cuda_error = 0;
+
+q4a_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return Q4A_ERR_CUDA;
+}
+
+q4a_status cuda_fail_drv(CUresult r) {
+    t_last_cuda_error = (int)r;
+    return Q4A_ERR_CUDA;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+q4a_status check_matrix_shape(int64_t out_dim, int64_t in_dim) {
+    if (out_dim < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (out_dim > (int64_t)1 << 30 || in_dim > (int64_t)1 << 24) return Q4A_ERR_UNSUPPORTED;
+    return Q4A_OK;
+}
+
+// Split an activation range into segments of at most 32 rows (the widest kernel variant).
+void push_segments(std::vector<Segment>& out, int32_t row0, int64_t tok0, int64_t ntok) {
+    for (int64_t t = 0; t < ntok; t += 32) {
+        Segment s;
+        s.row0 = row0;
+        s.tok0 = (int32_t)(tok0 + t);
+        s.ntok = (int32_t)(ntok - t < 32 ? ntok - t : 32);
+        s.pad = 0;
+        out.push_back(s);
+    }
+}
+
+}  // namespace
+}  // namespace q4a
+
+using namespace q4a;
+
+extern "C" {
+
+const char* q4a_status_string(q4a_status status) {
+    switch (status) {
+        case Q4A_OK: return "ok";
+        case Q4A_ERR_NULL: return "a required pointer is NULL";
+        case Q4A_ERR_SHAPE: return "a size or an index table is out of range";
+        case Q4A_ERR_ALIGN: return "a pointer misses its required alignment";
+        case Q4A_ERR_UNSUPPORTED: return "valid but unsupported (device or size limit)";
+        case Q4A_ERR_CUDA: return "a CUDA call failed";
+        case Q4A_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    }
+    return "unknown status";
+}
+
+int q4a_last_cuda_error(void) { return t_last_cuda_error; }
+
+q4a_status q4a_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64_t in_dim,
+                    q4a_stream_t stream) {
+    if (!w_packed || !codes) return Q4A_ERR_NULL;
+    if (rows < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (!aligned(w_packed, 16) || !aligned(codes, 16)) return Q4A_ERR_ALIGN;
+    return launch_pack(w_packed, codes, rows, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_dim, q4a_stream_t stream) {
+    if (!xsum || !x) return Q4A_ERR_NULL;
+    if (nb < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(xsum, 4)) return Q4A_ERR_ALIGN;
+    return launch_xsum(xsum, x, nb, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                    const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+    if (!y || !w || !s || !b || !x) return Q4A_ERR_NULL;
+    if (nb < 1) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
+    GemvLaunch L = {};
+    L.w = w;
+    L.tensor_rows = out_dim;
+    L.s = s;
+    L.b = b;
+    L.x = x;
+    L.y = y;
+    L.out_dim = out_dim;
+    L.in_dim = in_dim;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb < 32 ? nb : 32;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                            const float* x_raw, const uint16_t* norm_w, float eps, float shift,
+                            int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+    if (!y || !w || !s || !b || !x_raw || !norm_w) return Q4A_ERR_NULL;
+    if (nb < 1 || !(eps >= 0.0f)) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if (nb > 32) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(s, 2) ||
+        !aligned(b, 2) || !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    GemvLaunch L = {};
+    L.w = w;
+    L.tensor_rows = out_dim;
+    L.s = s;
+    L.b = b;
+    L.x = x_raw;
+    L.norm_w = norm_w;
+    L.eps = eps;
+    L.shift = shift;
+    L.y = y;
+    L.out_dim = out_dim;
+    L.in_dim = in_dim;
+    L.rmsnorm = true;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_bank,
+                            const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
+                            const int32_t* expert_ids, const int32_t* token_offsets, int n_active,
+                            int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
+                            q4a_stream_t stream) {
+    if (!y || !w_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets) return Q4A_ERR_NULL;
+    if (n_active < 1 || n_active > Q4A_MAX_SEGMENTS || n_experts < 1 || n_rows < 1) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if ((int64_t)n_experts * out_dim > ((int64_t)1 << 31) - 16) return Q4A_ERR_UNSUPPORTED;
+    if (n_rows > ((int64_t)1 << 31) - 1) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w_bank, 16) || !aligned(x, 16) || !aligned(s_bank, 2) || !aligned(b_bank, 2) ||
+        !aligned(y, 4) || (x_rows && !aligned(x_rows, 4)))
+        return Q4A_ERR_ALIGN;
+    if (token_offsets[0] != 0 || token_offsets[n_active] != n_rows) return Q4A_ERR_SHAPE;
+    for (int a = 0; a < n_active; ++a)
+        if (token_offsets[a + 1] < token_offsets[a]) return Q4A_ERR_SHAPE;
+
+    std::vector<Segment> segs;
+    std::vector<int> bad;
+    for (int a = 0; a < n_active; ++a) {
+        const int64_t n = token_offsets[a + 1] - token_offsets[a];
+        if (n == 0) continue;
+        const int32_t e = expert_ids[a];
+        if (e < 0 || e >= n_experts) {
+            bad.push_back(a);
+            continue;
+        }
+        push_segments(segs, (int32_t)((int64_t)e * out_dim), token_offsets[a], n);
+    }
+    if ((int)segs.size() > Q4A_MAX_SEGMENTS) return Q4A_ERR_UNSUPPORTED;
+    for (int a : bad) {
+        st = launch_fill_nan(y, token_offsets[a], token_offsets[a + 1] - token_offsets[a], out_dim,
+                             (cudaStream_t)stream);
+        if (st != Q4A_OK) return st;
+    }
+    if (segs.empty()) return Q4A_OK;
+    int max_ntok = 0;
+    for (const Segment& sg : segs) max_ntok = sg.ntok > max_ntok ? sg.ntok : max_ntok;
+    GemvLaunch L = {};
+    L.w = w_bank;
+    L.tensor_rows = (int64_t)n_experts * out_dim;
+    L.s = s_bank;
+    L.b = b_bank;
+    L.x = x;
+    L.x_rows = x_rows;
+    L.y = y;
+    L.out_dim = out_dim;
+    L.in_dim = in_dim;
+    L.experts = true;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = max_ntok;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,
+                             int64_t inter, q4a_stream_t stream) {
+    if (!h || !gate_up) return Q4A_ERR_NULL;
+    if (rows < 1 || inter < kGroup || inter % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (!aligned(h, 16) || !aligned(gate_up, 16) || (hsum && !aligned(hsum, 4))) return Q4A_ERR_ALIGN;
+    return launch_silu_mul_xsum(h, hsum, gate_up, rows, inter, (cudaStream_t)stream);
+}
+
+q4a_status q4a_check_device_error(q4a_stream_t stream) {
+    uint32_t word = 0;
+    q4a_status st = read_and_clear_device_error((cudaStream_t)stream, &word);
+    if (st != Q4A_OK) return st;
+    return word ? Q4A_ERR_TIMEOUT : Q4A_OK;
+}
+
+}  // extern "C"

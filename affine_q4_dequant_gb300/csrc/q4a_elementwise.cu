@@ -1,0 +1,158 @@
+// q4a_elementwise.cu -- the bandwidth-bound helpers around the GEMV:
+//   q4a_pack           (A1) codes -> 4-bit rows
+//   q4a_xsum           (A2) per-64-group sums of fp16 activations
+//   q4a_silu_mul_xsum  (A7) h = fp16(silu(gate) * up) plus group sums of h
+//   a NaN fill for routed-expert segments with an out-of-range expert id.
+// All are grid-stride kernels over 16-byte vectors, sized to a multiple of the SM
+// count, with no shared memory and no waits.
+#include <cuda_fp16.h>
+
+#include "q4a_internal.h"
+
+namespace q4a {
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Byte k of the output = code[2k] | code[2k+1] << 4: every output 16-byte vector
+// packs 32 consecutive codes (two input vectors). Codes are masked to 4 bits.
+__global__ void pack_kernel(uint4* __restrict__ out, const uint4* __restrict__ in, int64_t n_out_vec) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_out_vec;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 a = ld_nc_16(in + 2 * i);
+        const uint4 c = ld_nc_16(in + 2 * i + 1);
+        const uint32_t src[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        uint32_t dst[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // two input words (8 codes) -> one output word
+            const uint32_t lo = src[2 * k] & 0x0F0F0F0Fu;       // codes 0..3, one per byte
+            const uint32_t hi = src[2 * k + 1] & 0x0F0F0F0Fu;   // codes 4..7
+            // bytes (c0,c1,c2,c3) -> (c0 | c1<<4, c2 | c3<<4) in the low half word
+            const uint32_t plo = (lo | (lo >> 4)) & 0x00FF00FFu;      // (c0|c1<<4) at byte 0, (c2|c3<<4) at byte 2
+            const uint32_t phi = (hi | (hi >> 4)) & 0x00FF00FFu;
+            dst[k] = __byte_perm(plo, phi, 0x6420);
+        }
+        out[i] = make_uint4(dst[0], dst[1], dst[2], dst[3]);
+    }
+}
+
+// One thread per (row, group): 8 vectors of 8 halves summed in fp32 in index order.
+__global__ void xsum_kernel(float* __restrict__ xsum, const __half* __restrict__ x, int64_t n_groups_total) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_groups_total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const __half* p = x + i * kGroup;
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 v = ld_nc_16(p + 8 * k);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __half2 h = *reinterpret_cast<const __half2*>(&w[q]);
+                acc += __low2float(h);
+                acc += __high2float(h);
+            }
+        }
+        xsum[i] = acc;
+    }
+}
+
+// One thread per 8 outputs; 8 consecutive lanes cover one 64-group and sum it with
+// shuffles (the sum of the fp16-rounded values, as the activation step hands them on).
+__global__ void silu_mul_kernel(uint16_t* __restrict__ h, float* __restrict__ hsum,
+                                const float* __restrict__ gate_up, int64_t rows, int64_t inter) {
+    const int64_t per_row = inter / 8;
+    const int64_t total = rows * per_row;
+    for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const bool live = i < total;
+        float part = 0.f;
+        if (live) {
+            const int64_t r = i / per_row;
+            const int64_t j = (i - r * per_row) * 8;
+            const float* gp = gate_up + r * 2 * inter + j;
+            const float4 g0 = *reinterpret_cast<const float4*>(gp);
+            const float4 g1 = *reinterpret_cast<const float4*>(gp + 4);
+            const float4 u0 = *reinterpret_cast<const float4*>(gp + inter);
+            const float4 u1 = *reinterpret_cast<const float4*>(gp + inter + 4);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a = gv[2 * k] / (1.0f + expf(-gv[2 * k])) * uv[2 * k];
+                const float c = gv[2 * k + 1] / (1.0f + expf(-gv[2 * k + 1])) * uv[2 * k + 1];
+                const __half2 hv = __floats2half2_rn(a, c);
+                out[k] = *reinterpret_cast<const uint32_t*>(&hv);
+                part += __low2float(hv) + __high2float(hv);
+            }
+            *reinterpret_cast<uint4*>(h + r * inter + j) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        // lanes 8k..8k+7 hold one 64-group (inter % 64 == 0 and 32 % 8 == 0)
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        if (live && hsum && (threadIdx.x & 7) == 0) hsum[i / 8] = part;
+    }
+}
+
+__global__ void fill_nan_kernel(float* __restrict__ y, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = __int_as_float(0x7fc00000);
+}
+
+int grid_for(int64_t work, int threads) {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+q4a_status launch_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64_t in_dim,
+                       cudaStream_t stream) {
+    const int64_t n_out_vec = rows * in_dim / 32;
+    pack_kernel<<<grid_for(n_out_vec, 256), 256, 0, stream>>>(
+        reinterpret_cast<uint4*>(w_packed), reinterpret_cast<const uint4*>(codes), n_out_vec);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+}
+
+q4a_status launch_xsum(float* xsum, const uint16_t* x, int64_t nb, int64_t in_dim, cudaStream_t stream) {
+    const int64_t n = nb * in_dim / kGroup;
+    xsum_kernel<<<grid_for(n, 256), 256, 0, stream>>>(xsum, reinterpret_cast<const __half*>(x), n);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+}
+
+q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,
+                                int64_t inter, cudaStream_t stream) {
+    const int64_t n = rows * inter / 8;
+    silu_mul_kernel<<<grid_for(n, 256), 256, 0, stream>>>(h, hsum, gate_up, rows, inter);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+}
+
+q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim, cudaStream_t stream) {
+    const int64_t n = nrows * out_dim;
+    fill_nan_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y + row0 * out_dim, n);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+}
+
+}  // namespace q4a

@@ -1,0 +1,174 @@
+/*
+ * q4a.h -- C ABI of libq4a.so, the row-batched affine-4-bit dequantising
+ * matrix-vector product for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (restated from three web pages on the subject; citations name
+ * the page and the section of it):
+ *   W is [out_dim][in_dim] with 4-bit codes q in 0..15, packed two per byte:
+ *   byte k of a row holds element 2k in its low nibble and element 2k+1 in its
+ *   high nibble. Every run of 64 inputs (group g) of a row has a bfloat16 scale
+ *   s[o][g] and bias b[o][g]; the weight is w = s*q + b. For NB activation rows
+ *       y[r][o] = sum_g ( s[o][g] * sum_{i in g} q[o][i] * x[r][i]
+ *                         + b[o][g] * xsum[r][g] ),   xsum[r][g] = sum_{i in g} x[r][i].
+ *   ("BATCH_MSL" constant page, quantized_rows.metal: fn_q4_rows_h and
+ *   fn_q4_2rows_h; the prefill helper fn_qmv_small_b states the nibble order
+ *   explicitly; expert_gemm.metal stages w = fma(s, code, b).)
+ *
+ * Conventions shared by every entry point:
+ *   - Every buffer pointer is caller-owned DEVICE memory unless the argument
+ *     says "host". The library allocates no memory and keeps no per-call state.
+ *     It never reads device buffers from the host.
+ *   - fp16 buffers hold IEEE binary16 bit patterns, bf16 buffers bfloat16 bit
+ *     patterns (both as uint16_t). Matrices are row-major, rows contiguous.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and runs asynchronously; a call returns once its kernels are
+ *     launched. Outputs are fully overwritten (never accumulated into).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and leaves outputs untouched.
+ *   - Kernels never trap and never wait without a bound. A kernel that gives up
+ *     a bounded wait records it in a device error word; q4a_check_device_error
+ *     reports it.
+ *   - Results are deterministic: identical inputs give bit-identical outputs
+ *     (no floating-point atomics).
+ */
+#ifndef Q4A_H
+#define Q4A_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define Q4A_API __attribute__((visibility("default")))
+#else
+#define Q4A_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same underlying type). */
+typedef struct CUstream_st* q4a_stream_t;
+
+typedef enum q4a_status {
+    Q4A_OK = 0,
+    Q4A_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    Q4A_ERR_SHAPE = 2,       /* a size or an index table is out of range            */
+    Q4A_ERR_ALIGN = 3,       /* a pointer misses the alignment stated below         */
+    Q4A_ERR_UNSUPPORTED = 4, /* valid but not supported (device, size limit)        */
+    Q4A_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed (see q4a_last_cuda_error) */
+    Q4A_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (q4a_check_device_error) */
+} q4a_status;
+
+/* Upper limits of the host-side schedule. */
+#define Q4A_MAX_SEGMENTS 512   /* routed-expert segments per q4a_gemv_experts call */
+
+/* Static string for a status code (never NULL). */
+Q4A_API const char* q4a_status_string(q4a_status status);
+
+/* The cudaError_t value behind the most recent Q4A_ERR_CUDA on the calling
+ * host thread (0 if none). */
+Q4A_API int q4a_last_cuda_error(void);
+
+/*
+ * q4a_pack -- A1: pack one-code-per-byte matrices into the 4-bit row layout.
+ *   w_packed  out  uint8 [rows][in_dim/2]; byte k of a row = codes[2k] | codes[2k+1] << 4
+ *   codes     in   uint8 [rows][in_dim]; each code is masked to its low 4 bits
+ *                  (the prefill helper fn_qmv_small_b masks every nibble with 0xF)
+ *   Requires rows >= 1, in_dim >= 64, in_dim % 64 == 0, both pointers 16-byte aligned.
+ *   ("BATCH_MSL", quantized_rows.metal: low nibbles pair with the even x stream,
+ *   high nibbles with the odd one.)
+ */
+Q4A_API q4a_status q4a_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64_t in_dim,
+                    q4a_stream_t stream);
+
+/*
+ * q4a_xsum -- A2: per-64-group sums of fp16 activations, accumulated in fp32.
+ *   xsum  out  fp32 [nb][in_dim/64];  xsum[r][g] = sum_{i in g} x[r][i]
+ *   x     in   fp16 [nb][in_dim]
+ *   Requires nb >= 1, in_dim % 64 == 0, x 16-byte aligned, xsum 4-byte aligned.
+ *   (The pages keep per-32 sums: "BATCH_MSL" fn_norm_prep_b and fn_moe_act_b;
+ *   one bias covers both halves of a 64-group, so this is their pairwise sum.)
+ */
+Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_gemv -- A4: y = W.x for nb activation rows.
+ *   y        out  fp32 [nb][out_dim]
+ *   w        in   uint8 [out_dim][in_dim/2], packed as q4a_pack writes it
+ *   s, b     in   bf16 [out_dim][in_dim/64] scales and biases
+ *   x        in   fp16 [nb][in_dim]
+ *   Requires nb >= 1, out_dim >= 1 (any value, odd included), in_dim >= 64,
+ *   in_dim % 64 == 0; w and x 16-byte aligned; s and b 2-byte aligned.
+ *   ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b over quantized_rows.metal
+ *   fn_q4_rows_h; experts.metal fn_moe_down_b for the two-rows-per-pass form.)
+ */
+Q4A_API q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                    const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim,
+                    q4a_stream_t stream);
+
+/*
+ * q4a_gemv_experts -- A6: the GEMV over a routed-expert bank.
+ *   y              out   fp32 [n_rows][out_dim]; row r = W_e . x[x_rows ? x_rows[r] : r]
+ *                        for the segment a with token_offsets[a] <= r < token_offsets[a+1]
+ *                        and e = expert_ids[a]
+ *   w_bank         in    uint8 [n_experts*out_dim][in_dim/2], expert e at rows e*out_dim..
+ *   s_bank, b_bank in    bf16 [n_experts*out_dim][in_dim/64]
+ *   x              in    fp16 [*][in_dim]; with x_rows == NULL it has n_rows rows
+ *   x_rows         in    int32 [n_rows] device array or NULL; every entry must be a
+ *                        valid row index of x (device contents are not read by the host)
+ *   expert_ids     HOST  int32 [n_active]
+ *   token_offsets  HOST  int32 [n_active+1], token_offsets[0] == 0, non-decreasing,
+ *                        token_offsets[n_active] == n_rows
+ *   Requires 1 <= n_active <= Q4A_MAX_SEGMENTS, n_experts >= 1, n_rows >= 1, and the
+ *   q4a_gemv shape/alignment rules. A segment whose expert id lies outside
+ *   [0, n_experts) produces NaN rows (a loud failure, never an out-of-bounds read).
+ *   The expert list and offsets are host arrays because the host publishes the
+ *   union of routed experts after the router ("BATCH_MSL", experts.metal: the
+ *   grouped-expert section; fn_moe_gate_up_b and fn_moe_down_b run one pass per
+ *   unique expert over all of its rows).
+ */
+Q4A_API q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_bank,
+                            const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
+                            const int32_t* expert_ids, const int32_t* token_offsets,
+                            int n_active, int n_experts, int64_t n_rows, int64_t out_dim,
+                            int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_gemv_rmsnorm -- A3 + A4: RMSNorm prologue fused into the GEMV.
+ *   x_raw   in  fp32 [nb][in_dim] un-normalised activations
+ *   norm_w  in  bf16 [in_dim]
+ *   The GEMV input is xn = fp16( x_raw * rsqrt(mean(x_raw^2) + eps) * (norm_w + shift) )
+ *   per row (one normalisation group spanning the whole row), then y = W.xn as q4a_gemv.
+ *   ("BATCH_MSL", hyperconnection.metal fn_group_norm_b; fn_norm_prep_b hands the
+ *   GEMV an fp16 copy plus group sums of the normalised row.)
+ *   Requires eps >= 0, x_raw 16-byte aligned, norm_w 16-byte aligned; otherwise as q4a_gemv.
+ */
+Q4A_API q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                            const float* x_raw, const uint16_t* norm_w, float eps, float shift,
+                            int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_silu_mul_xsum -- A7: the step between the two routed-expert GEMVs.
+ *   h        out  fp16 [rows][inter];  h[r][j] = fp16( silu(gate) * up ),
+ *                 silu(v) = v / (1 + e^-v), gate = gate_up[r][j], up = gate_up[r][inter + j]
+ *   hsum     out  fp32 [rows][inter/64] group sums of the fp16 h values (may be NULL)
+ *   gate_up  in   fp32 [rows][2*inter]
+ *   Requires rows >= 1, inter % 64 == 0, gate_up and h 16-byte aligned, hsum 4-byte aligned.
+ *   ("BATCH_MSL", experts.metal fn_moe_act_b: sums of the fp16-rounded values.)
+ */
+Q4A_API q4a_status q4a_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,
+                             int64_t inter, q4a_stream_t stream);
+
+/*
+ * q4a_check_device_error -- synchronise `stream`, then report and clear the
+ * device error word: Q4A_ERR_TIMEOUT if a kernel of this library gave up a
+ * bounded wait since the last check (its outputs are then garbage),
+ * Q4A_ERR_CUDA if the synchronisation failed, Q4A_OK otherwise.
+ */
+Q4A_API q4a_status q4a_check_device_error(q4a_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4A_H */
