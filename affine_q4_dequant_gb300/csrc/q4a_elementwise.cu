@@ -12,6 +12,11 @@
 namespace q4a {
 namespace {
 
+// Programmatic dependent launch (see the GEMV kernel): wait for the previous kernel of
+// the stream before touching any global data, and let the next one start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -22,7 +27,10 @@ __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
 
 // Byte k of the output = code[2k] | code[2k+1] << 4: every output 16-byte vector
 // packs 32 consecutive codes (two input vectors). Codes are masked to 4 bits.
+// It lets dependent kernels launch only after its last store, behind a device-scope
+// fence: a GEMV launched right after it streams the packed weights without waiting.
 __global__ void pack_kernel(uint4* __restrict__ out, const uint4* __restrict__ in, int64_t n_out_vec) {
+    grid_dep_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_out_vec;
          i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 a = ld_nc_16(in + 2 * i);
@@ -41,10 +49,14 @@ __global__ void pack_kernel(uint4* __restrict__ out, const uint4* __restrict__ i
         }
         out[i] = make_uint4(dst[0], dst[1], dst[2], dst[3]);
     }
+    __threadfence();
+    grid_dep_launch();
 }
 
 // One thread per (row, group): 8 vectors of 8 halves summed in fp32 in index order.
 __global__ void xsum_kernel(float* __restrict__ xsum, const __half* __restrict__ x, int64_t n_groups_total) {
+    grid_dep_wait();
+    grid_dep_launch();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_groups_total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const __half* p = x + i * kGroup;
@@ -68,6 +80,8 @@ __global__ void xsum_kernel(float* __restrict__ xsum, const __half* __restrict__
 // shuffles (the sum of the fp16-rounded values, as the activation step hands them on).
 __global__ void silu_mul_kernel(uint16_t* __restrict__ h, float* __restrict__ hsum,
                                 const float* __restrict__ gate_up, int64_t rows, int64_t inter) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t per_row = inter / 8;
     const int64_t total = rows * per_row;
     for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
@@ -104,8 +118,25 @@ __global__ void silu_mul_kernel(uint16_t* __restrict__ h, float* __restrict__ hs
 }
 
 __global__ void fill_nan_kernel(float* __restrict__ y, int64_t n) {
+    grid_dep_wait();
+    grid_dep_launch();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         y[i] = __int_as_float(0x7fc00000);
+}
+
+template <typename... KArgs, typename... Args>
+q4a_status launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
 }
 
 int grid_for(int64_t work, int threads) {
@@ -127,32 +158,24 @@ int grid_for(int64_t work, int threads) {
 q4a_status launch_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64_t in_dim,
                        cudaStream_t stream) {
     const int64_t n_out_vec = rows * in_dim / 32;
-    pack_kernel<<<grid_for(n_out_vec, 256), 256, 0, stream>>>(
-        reinterpret_cast<uint4*>(w_packed), reinterpret_cast<const uint4*>(codes), n_out_vec);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+    return launch_pdl(pack_kernel, grid_for(n_out_vec, 256), 256, stream, reinterpret_cast<uint4*>(w_packed),
+                      reinterpret_cast<const uint4*>(codes), n_out_vec);
 }
 
 q4a_status launch_xsum(float* xsum, const uint16_t* x, int64_t nb, int64_t in_dim, cudaStream_t stream) {
     const int64_t n = nb * in_dim / kGroup;
-    xsum_kernel<<<grid_for(n, 256), 256, 0, stream>>>(xsum, reinterpret_cast<const __half*>(x), n);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+    return launch_pdl(xsum_kernel, grid_for(n, 256), 256, stream, xsum, reinterpret_cast<const __half*>(x), n);
 }
 
 q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,
                                 int64_t inter, cudaStream_t stream) {
     const int64_t n = rows * inter / 8;
-    silu_mul_kernel<<<grid_for(n, 256), 256, 0, stream>>>(h, hsum, gate_up, rows, inter);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+    return launch_pdl(silu_mul_kernel, grid_for(n, 256), 256, stream, h, hsum, gate_up, rows, inter);
 }
 
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim, cudaStream_t stream) {
     const int64_t n = nrows * out_dim;
-    fill_nan_kernel<<<grid_for(n, 256), 256, 0, stream>>>(y + row0 * out_dim, n);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? Q4A_OK : cuda_fail(e);
+    return launch_pdl(fill_nan_kernel, grid_for(n, 256), 256, stream, y + row0 * out_dim, n);
 }
 
 }  // namespace q4a

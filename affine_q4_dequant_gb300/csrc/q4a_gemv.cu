@@ -24,7 +24,11 @@
 //    ldmatrix gives it and the activation fragments carry the same permutation.
 //    The per-group result is scaled by s (times 2^24) and b*xsum is added, both
 //    in fp32: the tensor cores never see a rounded weight.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <stdio.h>
+#include <stdlib.h>
 
 #include <map>
 #include <mutex>
@@ -57,14 +61,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// try_wait with a suspend-time hint: a waiting warp sleeps in hardware until the phase
+// completes (or the hint elapses) instead of spinning and taking issue slots from the
+// warps that compute.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -84,7 +91,7 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatil
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return;
-        if ((it & 31) == 0) {
+        if ((it & 3) == 0) {
             if (*abort_flag) return;
             if (global_ns() - t0 > kWaitLimitNs) {
                 atomicOr(&g_device_error, 1u);
@@ -104,16 +111,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Programmatic dependent launch: the kernel may start while the previous kernel of the
+// stream is finishing; grid_dep_wait() returns once that kernel has completed and its
+// memory is visible. Nothing a previous kernel may write is touched before it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -209,76 +222,174 @@ __device__ __forceinline__ bool next_job(const P& p, int& t, int t_end, Job& j) 
 // Writes the CTA's K-slice of the activation rows of one segment as mma B fragments
 // (xfrag) and fp32 group sums (xsum). Item (tok, gl, t) covers elements 8t..8t+7 and
 // 32+8t..32+8t+7 of group gl for activation row tok; the four t of an item sit in one
-// lane quad, which sums its group.
+// lane quad, which sums its group. Each batch issues all of its global loads before
+// any arithmetic, so the staging costs about one memory latency per batch.
 template <int NT, bool RMS, class P>
 __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                         float* xsum_s, const float* inv_s, int ctid) {
     constexpr int NTOK = NT * 8;
-    const int items = NTOK * gsz * 4;
+    constexpr int BATCH = RMS ? 2 : 4;
+    constexpr int NTH = kConsumerWarps * 32;
+    const int items = sg.ntok * gsz * 4;
+    const int ntm = p.ntok_max;
     const uint32_t scale_odd = 0x2C002C00u;   // half2(1/16, 1/16)
-    for (int base = 0; base < items; base += kConsumerWarps * 32) {
-        const int i = base + ctid;
-        const bool live = i < items;
-        const int t = i & 3;
-        const int rest = i >> 2;
-        const int gl = live ? rest % gsz : 0;
-        const int tok = live ? rest / gsz : 0;
-        uint32_t v[4] = {0, 0, 0, 0}, u[4] = {0, 0, 0, 0};
-        float part = 0.f;
-        if (live && tok < sg.ntok) {
-            const int slot = sg.tok0 + tok;
-            const int64_t src = p.x_rows ? (int64_t)p.x_rows[slot] : (int64_t)slot;
-            const int64_t col = (int64_t)(kg0 + gl) * kGroup + 8 * t;
+    for (int base = 0; base < items; base += BATCH * NTH) {
+        // phase 1: loads
+        uint4 ld[BATCH][RMS ? 6 : 2];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int i = base + k * NTH + ctid;
+            const int rest = i >> 2;
+            const int gl = rest % gsz;
+            const int tok = rest / gsz;
+            const bool on = i < items;
+#pragma unroll
+            for (int q = 0; q < (RMS ? 6 : 2); ++q) ld[k][q] = make_uint4(0, 0, 0, 0);
+            if (on) {
+                const int slot = sg.tok0 + tok;
+                const int64_t src = p.x_rows ? (int64_t)p.x_rows[slot] : (int64_t)slot;
+                const int64_t col = (int64_t)(kg0 + gl) * kGroup + 8 * (i & 3);
+                if constexpr (!RMS) {
+                    const __half* xr = static_cast<const __half*>(p.x) + src * p.in_dim + col;
+                    ld[k][0] = ld_nc_16(xr);
+                    ld[k][1] = ld_nc_16(xr + 32);
+                } else {
+                    const float* xr = static_cast<const float*>(p.x) + src * p.in_dim + col;
+                    ld[k][0] = ld_nc_16(xr);
+                    ld[k][1] = ld_nc_16(xr + 4);
+                    ld[k][2] = ld_nc_16(xr + 32);
+                    ld[k][3] = ld_nc_16(xr + 36);
+                    ld[k][4] = ld_nc_16(p.norm_w + col);
+                    ld[k][5] = ld_nc_16(p.norm_w + col + 32);
+                }
+            }
+        }
+        // phase 2: fragments, sums, stores
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int i = base + k * NTH + ctid;
+            const bool live = i < items;
+            const int t = i & 3;
+            const int rest = i >> 2;
+            const int gl = rest % gsz;
+            const int tok = rest / gsz;
+            uint32_t v[4], u[4];
             if constexpr (!RMS) {
-                const __half* xr = static_cast<const __half*>(p.x) + src * p.in_dim + col;
-                const uint4 a = ld_nc_16(xr);
-                const uint4 c = ld_nc_16(xr + 32);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                u[0] = c.x; u[1] = c.y; u[2] = c.z; u[3] = c.w;
+                v[0] = ld[k][0].x; v[1] = ld[k][0].y; v[2] = ld[k][0].z; v[3] = ld[k][0].w;
+                u[0] = ld[k][1].x; u[1] = ld[k][1].y; u[2] = ld[k][1].z; u[3] = ld[k][1].w;
             } else {
-                const float* xr = static_cast<const float*>(p.x) + src * p.in_dim + col;
-                const float inv = inv_s[tok];
+                const float inv = live ? inv_s[tok] : 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const float4 f0 = *reinterpret_cast<const float4*>(xr + 32 * half);
-                    const float4 f1 = *reinterpret_cast<const float4*>(xr + 32 * half + 4);
-                    const uint4 wv = ld_nc_16(p.norm_w + col + 32 * half);
-                    const float xs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                    const uint4 f0 = ld[k][2 * half], f1 = ld[k][2 * half + 1], wv = ld[k][4 + half];
+                    const uint32_t xs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
                     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
                     uint32_t* dst = half ? u : v;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float w0 = bf16_to_f32(ww[k] & 0xFFFFu) + p.shift;
-                        const float w1 = bf16_to_f32(ww[k] >> 16) + p.shift;
-                        __half2 h = __floats2half2_rn(xs[2 * k] * inv * w0, xs[2 * k + 1] * inv * w1);
-                        dst[k] = *reinterpret_cast<uint32_t*>(&h);
+                    for (int q = 0; q < 4; ++q) {
+                        const float w0 = bf16_to_f32(ww[q] & 0xFFFFu) + p.shift;
+                        const float w1 = bf16_to_f32(ww[q] >> 16) + p.shift;
+                        __half2 h = __floats2half2_rn(__uint_as_float(xs[2 * q]) * inv * w0,
+                                                      __uint_as_float(xs[2 * q + 1]) * inv * w1);
+                        dst[q] = *reinterpret_cast<uint32_t*>(&h);
                     }
                 }
             }
+            float part = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) part += half2_sum(v[k]) + half2_sum(u[k]);
+            for (int q = 0; q < 4; ++q) part += half2_sum(v[q]) + half2_sum(u[q]);
+            // B fragments for the 4 mma steps: step j pairs element j with j+4 (v: word t,
+            // u: word t+4). Odd steps come from the high nibbles (16x) -> scale by 1/16.
+            uint32_t b01[4], b23[4];
+            b01[0] = __byte_perm(v[0], v[2], 0x5410);
+            b01[1] = hmul2_u32(__byte_perm(v[0], v[2], 0x7632), scale_odd);
+            b01[2] = __byte_perm(v[1], v[3], 0x5410);
+            b01[3] = hmul2_u32(__byte_perm(v[1], v[3], 0x7632), scale_odd);
+            b23[0] = __byte_perm(u[0], u[2], 0x5410);
+            b23[1] = hmul2_u32(__byte_perm(u[0], u[2], 0x7632), scale_odd);
+            b23[2] = __byte_perm(u[1], u[3], 0x5410);
+            b23[3] = hmul2_u32(__byte_perm(u[1], u[3], 0x7632), scale_odd);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (live) {
+                uint8_t* f = xfrag + ((size_t)(gl * 2) * ntm + tok) * 64 + t * 16;
+                *reinterpret_cast<uint4*>(f) = make_uint4(b01[0], b23[0], b01[1], b23[1]);
+                *reinterpret_cast<uint4*>(f + (size_t)ntm * 64) = make_uint4(b01[2], b23[2], b01[3], b23[3]);
+                // kept in units of 2^-24, the scale of the mma partial sums (see the epilogue)
+                if (t == 0) xsum_s[gl * NTOK + tok] = part * 5.9604644775390625e-08f;
+            }
         }
-        // B fragments for the 4 mma steps: step j pairs element j with j+4 (v: words t,
-        // u: words t+4). Odd steps come from the high nibbles (16x) -> scale by 1/16.
-        uint32_t b01[4], b23[4];
-        b01[0] = __byte_perm(v[0], v[2], 0x5410);
-        b01[1] = hmul2_u32(__byte_perm(v[0], v[2], 0x7632), scale_odd);
-        b01[2] = __byte_perm(v[1], v[3], 0x5410);
-        b01[3] = hmul2_u32(__byte_perm(v[1], v[3], 0x7632), scale_odd);
-        b23[0] = __byte_perm(u[0], u[2], 0x5410);
-        b23[1] = hmul2_u32(__byte_perm(u[0], u[2], 0x7632), scale_odd);
-        b23[2] = __byte_perm(u[1], u[3], 0x5410);
-        b23[3] = hmul2_u32(__byte_perm(u[1], u[3], 0x7632), scale_odd);
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (live) {
-            const int nt = tok >> 3;
-            const int lane = ((tok & 7) << 2) | t;
-            uint8_t* f = xfrag + ((size_t)(gl * NT + nt) * 2) * 512 + lane * 16;
-            *reinterpret_cast<uint4*>(f) = make_uint4(b01[0], b23[0], b01[1], b23[1]);
-            *reinterpret_cast<uint4*>(f + 512) = make_uint4(b01[2], b23[2], b01[3], b23[3]);
-            if (t == 0) xsum_s[gl * NTOK + tok] = part;
+    }
+}
+
+// B fragments of the bias term sum_g b[o][g] * xsum[r][g], an m16n8k16 contraction over
+// groups (bf16 operands): per 16-group block, activation row tok and lane quad t, the
+// pairs of groups (2t, 2t+1) and (2t+8, 2t+9) of xsum (already times 2^-24), split into
+// a bf16 high part and a bf16 remainder, so that hi + lo carries ~16 bits.
+__device__ void stage_xbias(const float* xsum_s, int ntok_seg, int ntok_max, int ntok_stride, int gsz,
+                            uint8_t* xbias, int ctid) {
+    const int nblk = (gsz + 15) / 16;
+    const int items = nblk * ntok_seg * 4;
+    for (int i = ctid; i < items; i += kConsumerWarps * 32) {
+        const int t = i & 3;
+        const int rest = i >> 2;
+        const int tok = rest % ntok_seg;
+        const int gb = rest / ntok_seg;
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            float v[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int gl = gb * 16 + 2 * t + 8 * pr + e;
+                v[e] = gl < gsz ? xsum_s[gl * ntok_stride + tok] : 0.f;
+            }
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(v[0] - hf.x, v[1] - hf.y);
+            hi[pr] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[pr] = *reinterpret_cast<const uint32_t*>(&l);
         }
+        *reinterpret_cast<uint4*>(xbias + ((size_t)gb * ntok_max + tok) * 64 + t * 16) = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+    }
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+        " {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Sum of squares of this CTA's K-slice of every activation row (the RMSNorm prologue).
+// Warp w owns rows w, w+8, ...; each lane issues up to 16 independent 16-byte loads per
+// round before accumulating.
+template <int NT, class P>
+__device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, float* ssq_s, int warp,
+                            int lane) {
+    constexpr int NTOK = NT * 8;
+    constexpr int U = 16;
+    const int chunks = gsz * (kGroup / 4);     // float4 chunks per row slice
+    for (int tok = warp; tok < NTOK; tok += kConsumerWarps) {
+        float acc = 0.f;
+        if (tok < sg.ntok) {
+            const float4* xr = reinterpret_cast<const float4*>(
+                static_cast<const float*>(p.x) + (int64_t)(sg.tok0 + tok) * p.in_dim + (int64_t)kg0 * kGroup);
+            for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
+                float4 f[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    f[u] = c < chunks ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) acc += f[u].x * f[u].x + f[u].y * f[u].y + f[u].z * f[u].z + f[u].w * f[u].w;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) ssq_s[tok] = acc;
     }
 }
 
@@ -288,7 +399,8 @@ template <int NT, bool RMS, int MAXSEG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> p) {
     constexpr int NTOK = NT * 8;
-    constexpr int TPW = (NT <= 2) ? 4 : 2;   // tiles per consumer warp (row half)
+    constexpr int MT = tiles_per_block(NT);  // tiles per row block
+    constexpr int TPW = MT / 2;              // tiles per consumer warp (row half)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -296,17 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = smem + L.ring;
     uint8_t* xfrag = smem + L.xfrag;
     float* xsum_s = reinterpret_cast<float*>(smem + L.xsum);
+    uint8_t* sbuf = smem + L.sb;                              // [2][s rows | b rows]
     float* wpart = reinterpret_cast<float*>(smem + L.wpart);
     float* cpart = reinterpret_cast<float*>(smem + L.cpart);
     float* ssq_s = reinterpret_cast<float*>(smem + L.ssq);   // [NTOK] sum of squares, [NTOK] inv
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * p.stages);
+    const int S = p.stages;
+    uint64_t* full_b = bars;              // [S]  TMA bytes of a stage landed
+    uint64_t* empty_b = bars + S;         // [S]  every consumer warp is done with a stage
+    uint64_t* sbfull_b = bars + 2 * S;    // [2]  a row block's scales/biases landed
+    uint64_t* sbempty_b = bars + 2 * S + 2;  // [2] every consumer warp is done with them
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int S = p.stages;
     const int C = p.cluster;
-    const int crank = (int)cluster_rank();
+    const int crank = C > 1 ? (int)cluster_rank() : 0;
     const int cid = blockIdx.x / C;
 
     // This CTA's K-slice (in groups) and its stage count per row block.
@@ -319,10 +436,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_begin = (int)(((int64_t)cid * p.n_tiles) / p.n_clusters);
     const int t_end = (int)(((int64_t)(cid + 1) * p.n_tiles) / p.n_clusters);
 
+    grid_dep_launch();
+    if (warp == kConsumerWarps && lane < 3 * kNumMaps) {
+        // fetch the tensor-map descriptors in parallel before their first use
+        const CUtensorMap* m = lane < kNumMaps ? &p.tmap_w[lane]
+                               : lane < 2 * kNumMaps ? &p.tmap_s[lane - kNumMaps] : &p.tmap_b[lane - 2 * kNumMaps];
+        if (lane < kNumMaps || p.sb_mode == kSbTma)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_addr(bars + s), 33);                   // TMA arrive + 32 copy arrivals
-            mbar_init(smem_addr(bars + S + s), kConsumerWarps);   // one arrival per consumer warp
+            mbar_init(smem_addr(full_b + s), 1);
+            mbar_init(smem_addr(empty_b + s), kConsumerWarps);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(smem_addr(sbfull_b + q), 1);
+            mbar_init(smem_addr(sbempty_b + q), kConsumerWarps);
         }
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -331,12 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ======================= producer warp =======================
+        // The producer reads only the weights (codes, scales, biases), which are inputs of
+        // the whole call, so it never waits for the previous kernel of the stream: under
+        // programmatic dependent launch its streaming overlaps that kernel's tail.
         const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
         const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
         const int64_t srow_bytes = (int64_t)p.groups * 2;
-        int it = 0;
+        int it = 0, blk = 0;
+        int rs = 0;             // ring slot and its phase
+        uint32_t rph = 0;
         bool pending = false;   // an un-waited cluster-barrier arrival
-        if (RMS) {              // matches the consumers' norm exchange
+        if (RMS && C > 1) {     // matches the consumers' norm exchange
             cluster_arrive();
             pending = true;
         }
@@ -347,101 +481,137 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t lrow0 = (int64_t)j.tile * 16;                 // row within the segment
             const int rows_valid = (int)llmin((int64_t)j.ntile * 16, p.out_dim - lrow0);
             const int64_t trow0 = (int64_t)sg.row0 + lrow0;              // row within the tensor
+            // -- scales and biases of the whole row block, full rows of the K-slice --
+            {
+                const int nsb = (int)L.n_sb;
+                const int q = blk % nsb;
+                if (blk >= nsb) mbar_wait(smem_addr(sbempty_b + q), (uint32_t)(blk / nsb - 1) & 1u, abort_flag);
+                uint8_t* sdst = sbuf + (size_t)q * L.sb_buf;
+                const uint32_t bar = smem_addr(sbfull_b + q);
+                if (p.sb_mode == kSbTma) {
+                    if (lane == 0) {
+                        const int nchunk = (gsz + 63) / 64;
+                        mbar_arrive_expect_tx(bar, (uint32_t)(2 * nchunk * j.ntile * kTileBytes));
+                        int m0 = 0;
+                        for (int lg = kNumMaps - 1; lg >= 0; --lg) {
+                            const int h = 1 << lg;
+                            if (j.ntile - m0 < h) continue;
+                            for (int c = 0; c < nchunk; ++c) {
+                                const uint32_t o = (uint32_t)((c * MT + m0) * kTileBytes);
+                                tma_load_2d(smem_addr(sdst + o), &p.tmap_s[lg], kg0 + 64 * c, (int)(trow0 + 16 * m0), bar);
+                                tma_load_2d(smem_addr(sdst + L.sb_pitch + o), &p.tmap_b[lg], kg0 + 64 * c,
+                                            (int)(trow0 + 16 * m0), bar);
+                            }
+                            m0 += h;
+                        }
+                    }
+                } else {
+                    // element copies into the swizzled layout (full K: one CTA per cluster);
+                    // groups up to the next 16-group block are zeroed for the bias contraction
+                    const int gpad = (gsz + 15) / 16 * 16;
+                    const int n = 2 * rows_valid * gpad;
+                    for (int i = lane; i < n; i += 32) {
+                        const int k = i % gpad;
+                        const int rr = i / gpad;
+                        const int isb = rr >= rows_valid;
+                        const int r = rr - isb * rows_valid;
+                        uint16_t v = 0;
+                        if (k < gsz)
+                            v = *reinterpret_cast<const uint16_t*>((isb ? b8 : s8) + (trow0 + r) * srow_bytes +
+                                                                   (int64_t)(kg0 + k) * 2);
+                        const uint32_t o = (uint32_t)(((k >> 6) * MT * 16 + r) * 128) +
+                                           ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
+                        *reinterpret_cast<uint16_t*>(sdst + (size_t)isb * L.sb_pitch + o) = v;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar);
+                }
+                __syncwarp();
+            }
+            // -- the packed weights, one stage per 8 groups --
             for (int ks = 0; ks < nks; ++ks, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (uint32_t)(it / S) & 1u;
-                if (it >= S) mbar_wait(smem_addr(bars + S + s), ph ^ 1u, abort_flag);
-                const uint32_t full = smem_addr(bars + s);
+                const int s = rs;
+                const uint32_t ph = rph;
+                if (++rs == S) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (it >= S) mbar_wait(smem_addr(empty_b + s), ph ^ 1u, abort_flag);
+                const uint32_t full = smem_addr(full_b + s);
                 uint8_t* st = ring + (size_t)s * L.stage_bytes;
                 const int g0 = kg0 + ks * kStageGroups;
                 const int ng = min(kStageGroups, kg1 - g0);
                 const int nbox = (ng + 3) / 4;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full, (uint32_t)(j.ntile * nbox * kBoxBytesTotal));
-                    for (int m = 0; m < j.ntile; ++m)
+                    // One tall box per box column for each power-of-two run of tiles: the
+                    // TMA engine pays per box, so few large boxes keep HBM streaming.
+                    mbar_arrive_expect_tx(full, (uint32_t)(j.ntile * nbox * kTileBytes));
+                    int m0 = 0;
+                    for (int lg = kNumMaps - 1; lg >= 0; --lg) {
+                        const int h = 1 << lg;
+                        if (j.ntile - m0 < h) continue;
                         for (int c = 0; c < nbox; ++c)
-                            tma_load_2d(smem_addr(st + (m * 2 + c) * kBoxBytesTotal), &p.tmap_w,
-                                        (g0 + 4 * c) * 32, (int)(trow0 + 16 * m), full);
+                            tma_load_2d(smem_addr(st + (c * MT + m0) * kTileBytes), &p.tmap_w[lg],
+                                        (g0 + 4 * c) * 32, (int)(trow0 + 16 * m0), full);
+                        m0 += h;
+                    }
                 }
-                uint8_t* sdst = st + L.stage_w_bytes;                 // s: [rows][16 B]
-                uint8_t* bdst = sdst + (size_t)16 * 16 * p.mt;        // b: [rows][16 B]
-                if (p.sb_mode == kSb16) {
-                    for (int i = lane; i < 2 * rows_valid; i += 32) {
-                        const int r = i >> 1;
-                        const bool isb = i & 1;
-                        const uint8_t* src = (isb ? b8 : s8) + (trow0 + r) * srow_bytes + (int64_t)g0 * 2;
-                        cp_async_16(smem_addr((isb ? bdst : sdst) + r * 16), src);
-                    }
-                    cp_async_arrive_noinc(full);
-                } else if (p.sb_mode == kSb4) {
-                    const int per_row = (ng + 1) >> 1;                // 4-byte granules per row
-                    for (int i = lane; i < 2 * rows_valid * per_row; i += 32) {
-                        const int k = i % per_row;
-                        const int rr = i / per_row;
-                        const int r = rr >> 1;
-                        const bool isb = rr & 1;
-                        const uint8_t* src =
-                            (isb ? b8 : s8) + (trow0 + r) * srow_bytes + (int64_t)g0 * 2 + 4 * k;
-                        cp_async_4(smem_addr((isb ? bdst : sdst) + r * 16 + 4 * k), src);
-                    }
-                    cp_async_arrive_noinc(full);
-                } else {
-                    for (int i = lane; i < 2 * rows_valid * ng; i += 32) {
-                        const int k = i % ng;
-                        const int rr = i / ng;
-                        const int r = rr >> 1;
-                        const bool isb = rr & 1;
-                        const uint16_t v = *reinterpret_cast<const uint16_t*>(
-                            (isb ? b8 : s8) + (trow0 + r) * srow_bytes + (int64_t)(g0 + k) * 2);
-                        *reinterpret_cast<uint16_t*>((isb ? bdst : sdst) + r * 16 + 2 * k) = v;
-                    }
-                    mbar_arrive(full);
-                }
+                __syncwarp();
             }
-            if (pending) cluster_wait();
-            cluster_arrive();
-            pending = true;
+            if (C > 1) {
+                if (pending) cluster_wait();
+                cluster_arrive();
+                pending = true;
+            }
+            ++blk;
         }
         if (pending) cluster_wait();
     } else {
         // ======================= consumer warps =======================
-        const int ctid = threadIdx.x;       // 0 .. 255
-        const int wr = warp >> 2;           // row half
-        const int wg = warp & 3;            // group slot
+        const int ctid = threadIdx.x;       // 0 .. 32 * kConsumerWarps - 1
+        const int wr = warp / kGroupSlots;  // row half
+        const int wg = warp % kGroupSlots;  // group slot = group index within each stage
         const int g = lane >> 2;
         const int tq = lane & 3;
+        grid_dep_wait();   // activations, the row map and y may belong to the previous kernel
 
         if (RMS) {
             // Sum of squares of this CTA's K-slice per activation row, exchanged across the
             // cluster so every CTA normalises with the full-row statistics.
-            const Segment& sg = p.seg[0];
-            for (int tok = warp; tok < NTOK; tok += kConsumerWarps) {
-                float acc = 0.f;
-                if (tok < sg.ntok) {
-                    const float* xr = static_cast<const float*>(p.x) +
-                                      (int64_t)(sg.tok0 + tok) * p.in_dim + (int64_t)kg0 * kGroup;
-                    for (int i = lane * 4; i < gsz * kGroup; i += 128) {
-                        const float4 f = *reinterpret_cast<const float4*>(xr + i);
-                        acc += f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (lane == 0) ssq_s[tok] = acc;
+            rms_partial<NT>(p, p.seg[0], kg0, gsz, ssq_s, warp, lane);
+            if (C > 1) {
+                cluster_arrive();
+                cluster_wait();
+            } else {
+                consumer_sync();
             }
-            cluster_arrive();
-            cluster_wait();
             if (ctid < NTOK) {
                 float tot = 0.f;
-                for (int c = 0; c < C; ++c) tot += ld_peer_f32(map_peer(smem_addr(ssq_s + ctid), c));
+                for (int c = 0; c < C; ++c)
+                    tot += C > 1 ? ld_peer_f32(map_peer(smem_addr(ssq_s + ctid), c)) : ssq_s[ctid];
                 ssq_s[NTOK + ctid] = rsqrtf(tot / (float)p.in_dim + p.eps);
             }
             consumer_sync();
         }
 
         float acc[TPW][NT][4];
+        uint8_t* xbias = smem + L.xbias;
+        // Per-warp constants (32-bit shared addresses; per-tile steps are immediates).
+        // ldmatrix: rows 0-7 / 8-15 of a tile, 16-byte granules 2*(wg&3) and 2*(wg&3)+1 of
+        // its box column; 128-byte swizzle granule ^= row & 7.
+        const uint32_t lrow = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
+        const uint32_t lgran = (uint32_t)(wg & 3) * 2 + (uint32_t)(lane >> 4);
+        const uint32_t ldsm_base = smem_addr(ring) + lrow * 128 + ((lgran ^ (lrow & 7)) << 4) +
+                                   (uint32_t)(((wg >> 2) * MT + wr * TPW) * kTileBytes);
+        // B fragments of group gl, row tok: xfrag + ((gl*2 + jp)*ntok_max + tok)*64 + tq*16
+        const uint32_t xf_jp = (uint32_t)p.ntok_max * 64u;
+        const uint32_t xf_base = smem_addr(xfrag) + (uint32_t)wg * 2u * xf_jp + (uint32_t)g * 64u + (uint32_t)tq * 16u;
+        const uint32_t xf_stage = (uint32_t)kStageGroups * 2u * xf_jp;
+        // scales: [chunk][row][128 B]; this lane's rows g (and g+8) of the warp's first tile
+        const uint32_t s_lane = (uint32_t)(g * 128 + wr * TPW * kTileBytes) + 2u * (uint32_t)wg;
         int staged_seg = -1;
-        int it = 0;
+        int rs = 0;            // ring slot and its phase
+        uint32_t rph = 0;
         int blk = 0;
         int t = t_begin;
         Job j;
@@ -450,8 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j.seg != staged_seg) {
                 stage_x<NT, RMS>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK, ctid);
                 consumer_sync();
+                stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
+                consumer_sync();
                 staged_seg = j.seg;
             }
+            const int ntok = sg.ntok;
 #pragma unroll
             for (int mi = 0; mi < TPW; ++mi)
 #pragma unroll
@@ -459,54 +632,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) acc[mi][nt][k] = 0.f;
 
-            for (int ks = 0; ks < nks; ++ks, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (uint32_t)(it / S) & 1u;
-                mbar_wait(smem_addr(bars + s), ph, abort_flag);
-                const uint8_t* st = ring + (size_t)s * L.stage_bytes;
-                const uint8_t* sst = st + L.stage_w_bytes;
-                const uint8_t* bst = sst + (size_t)16 * 16 * p.mt;
-                const int ng = min(kStageGroups, gsz - ks * kStageGroups);
+            const int q = blk % (int)L.n_sb;
+            mbar_wait(smem_addr(sbfull_b + q), (uint32_t)(blk / (int)L.n_sb) & 1u, abort_flag);
+            const uint8_t* sbs = sbuf + (size_t)q * L.sb_buf;         // scales
+            const uint8_t* sbb = sbs + L.sb_pitch;                    // biases
+            const uint32_t s_blk = smem_addr(sbs) + s_lane;
+            bool tok_ok[NT];
 #pragma unroll
-                for (int gi = 0; gi < 2; ++gi) {
-                    const int gg = wg + 4 * gi;                 // group within the stage
-                    if (gg >= ng) continue;
-                    const int gl = ks * kStageGroups + gg;       // group within the K-slice
+            for (int nt = 0; nt < NT; ++nt) tok_ok[nt] = nt * 8 + g < ntok;
+            for (int ks = 0; ks < nks; ++ks) {
+                mbar_wait(smem_addr(full_b + rs), rph, abort_flag);
+                if (wg < min(kStageGroups, gsz - ks * kStageGroups)) {
+                    // Slots beyond the row block read stale stage data and are never stored.
+                    uint32_t w[TPW][4];
+                    const uint32_t st = ldsm_base + (uint32_t)rs * L.stage_bytes;
+#pragma unroll
+                    for (int mi = 0; mi < TPW; ++mi)
+                        ldsm_x4(st + (uint32_t)(mi * kTileBytes), w[mi][0], w[mi][1], w[mi][2], w[mi][3]);
                     uint32_t bf[NT][8];
-                    float2 xs[NT];
+                    const uint32_t xf = xf_base + (uint32_t)ks * xf_stage;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint8_t* f = xfrag + ((size_t)(gl * NT + nt) * 2) * 512 + lane * 16;
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(f);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(f + 512);
+                        // activation row nt*8 + g of the segment; rows beyond it multiply zeros
+                        uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+                        if (tok_ok[nt]) {
+                            q0 = lds_v4(xf + (uint32_t)(nt * 512));
+                            q1 = lds_v4(xf + xf_jp + (uint32_t)(nt * 512));
+                        }
                         bf[nt][0] = q0.x; bf[nt][1] = q0.y; bf[nt][2] = q0.z; bf[nt][3] = q0.w;
                         bf[nt][4] = q1.x; bf[nt][5] = q1.y; bf[nt][6] = q1.z; bf[nt][7] = q1.w;
-                        xs[nt] = *reinterpret_cast<const float2*>(xsum_s + gl * NTOK + nt * 8 + 2 * tq);
                     }
-                    const uint32_t gran0 = (uint32_t)(gg & 3) * 2;
+                    // group gl = 8ks + wg: chunk ks/8, granule (ks & 7) ^ g, element wg
+                    const uint32_t sa = s_blk + (uint32_t)((ks >> 3) * MT * kTileBytes) +
+                                        ((uint32_t)((ks & 7) ^ g) << 4);
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
-                        const int m = wr * TPW + mi;
-                        if (m >= j.ntile) continue;
-                        // ldmatrix x4: rows 0-7 / 8-15 of the tile, 16-byte granules gran0 and
-                        // gran0+1 of the box (128-byte swizzle: granule ^= row & 7).
-                        const uint32_t box = smem_addr(st + (m * 2 + (gg >> 2)) * kBoxBytesTotal);
-                        const uint32_t row = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
-                        const uint32_t gran = gran0 + (uint32_t)(lane >> 4);
-                        uint32_t w[4];
-                        ldsm_x4(box + row * 128 + ((gran ^ (row & 7)) << 4), w[0], w[1], w[2], w[3]);
-                        // scale and bias of rows g and g+8 for this group
-                        const int r0 = m * 16 + g;
-                        const float s0 = bf16_to_f32(*reinterpret_cast<const uint16_t*>(sst + r0 * 16 + 2 * gg)) * 16777216.0f;
-                        const float s1 = bf16_to_f32(*reinterpret_cast<const uint16_t*>(sst + (r0 + 8) * 16 + 2 * gg)) * 16777216.0f;
-                        const float bb0 = bf16_to_f32(*reinterpret_cast<const uint16_t*>(bst + r0 * 16 + 2 * gg));
-                        const float bb1 = bf16_to_f32(*reinterpret_cast<const uint16_t*>(bst + (r0 + 8) * 16 + 2 * gg));
+                        // The mma partial sums are sum(q x) * 2^-24; s multiplies them as is and
+                        // the result is multiplied by 2^24 once at the end (no scale overflows).
+                        const float s0 = bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes)));
+                        const float s1 = bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes + 1024)));
                         uint32_t h[4][4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint32_t v8 = w[k] >> 8;
-                            h[k][0] = w[k] & 0x000F000Fu;
-                            h[k][1] = w[k] & 0x00F000F0u;
+                            const uint32_t v8 = w[mi][k] >> 8;
+                            h[k][0] = w[mi][k] & 0x000F000Fu;
+                            h[k][1] = w[mi][k] & 0x00F000F0u;
                             h[k][2] = v8 & 0x000F000Fu;
                             h[k][3] = v8 & 0x00F000F0u;
                         }
@@ -518,16 +688,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mma_f16(d, h[0][jj], h[1][jj], h[2][jj], h[3][jj], bf[nt][2 * jj],
                                         bf[nt][2 * jj + 1]);
                             float* a = acc[mi][nt];
-                            a[0] = fmaf(s0, d[0], fmaf(bb0, xs[nt].x, a[0]));
-                            a[1] = fmaf(s0, d[1], fmaf(bb0, xs[nt].y, a[1]));
-                            a[2] = fmaf(s1, d[2], fmaf(bb1, xs[nt].x, a[2]));
-                            a[3] = fmaf(s1, d[3], fmaf(bb1, xs[nt].y, a[3]));
+                            a[0] = fmaf(s0, d[0], a[0]);
+                            a[1] = fmaf(s0, d[1], a[1]);
+                            a[2] = fmaf(s1, d[2], a[2]);
+                            a[3] = fmaf(s1, d[3], a[3]);
                         }
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(bars + S + s));
+                if (lane == 0) mbar_arrive(smem_addr(empty_b + rs));
+                if (++rs == S) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
             }
+
+            // ---- bias term: sum_g b[o][g] * xsum[r][g], once per row block ----
+            // bf16 mma over 16-group blocks; A (biases) comes straight from the swizzled smem
+            // rows through ldmatrix, B is the hi/lo split group sums.
+            {
+                const int nblk = (gsz + 15) / 16;
+                for (int gb = wg; gb < nblk; gb += kGroupSlots) {
+                    uint32_t bx[NT][4];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (tok_ok[nt])
+                            v = lds_v4(smem_addr(xbias) + (uint32_t)((gb * p.ntok_max + nt * 8 + g) * 64 + tq * 16));
+                        bx[nt][0] = v.x; bx[nt][1] = v.y; bx[nt][2] = v.z; bx[nt][3] = v.w;
+                    }
+                    // groups 16gb..16gb+15 = granules 2*(gb&3), +1 of 64-group chunk gb>>2
+                    const uint32_t gran = (uint32_t)(gb & 3) * 2 + (uint32_t)(lane >> 4);
+                    const uint32_t boff = smem_addr(sbb) + (uint32_t)((gb >> 2) * MT * kTileBytes) + lrow * 128 +
+                                          ((gran ^ (lrow & 7)) << 4) + (uint32_t)(wr * TPW * kTileBytes);
+#pragma unroll
+                    for (int mi = 0; mi < TPW; ++mi) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(boff + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_bf16(acc[mi][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                            mma_bf16(acc[mi][nt], a0, a1, a2, a3, bx[nt][2], bx[nt][3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(sbempty_b + q));
 
             // ---- end of the row block: reduce over group slots, then over the cluster ----
             const int R = j.ntile * 16;
@@ -537,19 +744,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m >= j.ntile) continue;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float* w0 = wpart + ((size_t)wg * (16 * p.mt) + m * 16 + g) * NTOK + nt * 8 + 2 * tq;
+                    float* w0 = wpart + ((size_t)wg * (16 * MT) + m * 16 + g) * NTOK + nt * 8 + 2 * tq;
                     *reinterpret_cast<float2*>(w0) = make_float2(acc[mi][nt][0], acc[mi][nt][1]);
                     *reinterpret_cast<float2*>(w0 + 8 * NTOK) = make_float2(acc[mi][nt][2], acc[mi][nt][3]);
                 }
             }
             consumer_sync();
-            float* cp = cpart + (size_t)(blk & 1) * (16 * p.mt) * NTOK;
+            float* cp = cpart + (size_t)(blk & 1) * (16 * MT) * NTOK;
             for (int e = ctid; e < R * NTOK; e += kConsumerWarps * 32) {
-                const size_t stride = (size_t)(16 * p.mt) * NTOK;
-                cp[e] = ((wpart[e] + wpart[e + stride]) + wpart[e + 2 * stride]) + wpart[e + 3 * stride];
+                const size_t stride = (size_t)(16 * MT) * NTOK;
+                float v = wpart[e];
+#pragma unroll
+                for (int qq = 1; qq < kGroupSlots; ++qq) v += wpart[e + qq * stride];
+                cp[e] = v;
             }
-            cluster_arrive();
-            cluster_wait();
+            if (C > 1) {
+                cluster_arrive();
+                cluster_wait();
+            } else {
+                consumer_sync();
+            }
             const int64_t lrow0 = (int64_t)j.tile * 16;
             const int rows_valid = (int)llmin((int64_t)R, p.out_dim - lrow0);
             const int rc = (R + C - 1) / C;
@@ -562,18 +776,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tok = e / nr;
                     const int row = ra + (e - tok * nr);
                     if (row >= rows_valid) continue;
-                    const uint32_t off = (uint32_t)((row * NTOK + tok) * 4);
-                    float v = 0.f;
-                    for (int c = 0; c < C; ++c) v += ld_peer_f32(map_peer(cp_addr + off, (uint32_t)c));
-                    p.y[(int64_t)(sg.tok0 + tok) * p.out_dim + lrow0 + row] = v;
+                    float v;
+                    if (C > 1) {
+                        const uint32_t off = (uint32_t)((row * NTOK + tok) * 4);
+                        v = 0.f;
+                        for (int c = 0; c < C; ++c) v += ld_peer_f32(map_peer(cp_addr + off, (uint32_t)c));
+                    } else {
+                        v = cp[row * NTOK + tok];
+                    }
+                    p.y[(int64_t)(sg.tok0 + tok) * p.out_dim + lrow0 + row] = v * 16777216.0f;
                 }
             }
             ++blk;
         }
     }
-    // No CTA leaves while a peer may still read its shared memory.
-    cluster_arrive();
-    cluster_wait();
+    if (C > 1) {
+        // No CTA leaves while a peer may still read its shared memory.
+        cluster_arrive();
+        cluster_wait();
+    }
 }
 
 template <int MAXSEG>
@@ -650,11 +871,13 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     if (e != cudaSuccess) return cuda_fail(e);
     const DeviceInfo di = device_info();
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)prm.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
@@ -674,6 +897,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
         if (it == g_occ_cache.end()) {
             // How many clusters fit at once (GPC granularity can strand SMs for C > 1).
             cfg.gridDim = dim3((unsigned)(max_clusters * prm.cluster), 1, 1);
+            cfg.numAttrs = 1;
             int occ = 0;
             if (cudaOccupancyMaxActiveClusters(&occ, kern, &cfg) != cudaSuccess || occ <= 0) {
                 cudaGetLastError();
@@ -685,6 +909,14 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     }
     prm.n_clusters = max_clusters < prm.n_tiles ? max_clusters : prm.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
+    cfg.numAttrs = 2;
+    static const bool debug = getenv("Q4A_DEBUG") != nullptr;
+    if (debug)
+        fprintf(stderr,
+                "q4a gemv: nt=%d rms=%d segs=%d out=%lld in=%lld cluster=%d gs=%d mt=%d stages=%d "
+                "clusters=%d (max %d) tiles=%d smem=%u sb_mode=%d\n",
+                NT, (int)RMS, prm.nseg, (long long)prm.out_dim, (long long)prm.in_dim, prm.cluster, prm.gs,
+                prm.mt, prm.stages, prm.n_clusters, max_clusters, prm.n_tiles, smem_bytes, prm.sb_mode);
     e = cudaLaunchKernelEx(&cfg, kern, prm);
     if (e != cudaSuccess) return cuda_fail(e);
     return Q4A_OK;
@@ -700,32 +932,58 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     if (L.nseg > MAXSEG) return Q4A_ERR_SHAPE;
 
     const int nt = L.max_ntok <= 8 ? 1 : (L.max_ntok <= 16 ? 2 : 4);
-    const int mt = nt <= 2 ? 8 : 4;
+    const int mt = tiles_per_block(nt);
     const int G = (int)(L.in_dim / kGroup);
 
-    // Cluster size: the smallest power of two whose K-slice of activation fragments fits.
+    // Cluster size (K split): the smallest power of two whose K-slice leaves room for a
+    // ring of at least 4 stages, preferring enough tiles per cluster for a full row block.
+    const int ntm = L.max_ntok;
+    auto slice = [&](int c) {
+        int g = (G + c - 1) / c;
+        if (c > 1) g = (g + 7) / 8 * 8;         // slices start on a stage boundary
+        return g;
+    };
+    const int64_t n_tiles = (int64_t)((L.out_dim + 15) / 16) * L.nseg;
+    // Scale/bias fetch mode: TMA needs 16-byte row strides (groups % 8 == 0) and 16-byte
+    // aligned bases; a K split needs it too (its slabs are strided).
+    const bool al16 = (reinterpret_cast<uintptr_t>(L.s) % 16 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 16 == 0);
+    const int sbm_full = (G % 8 == 0 && al16) ? kSbTma : kSbPlain;
+    auto sbmode = [&](int c) { return c == 1 ? sbm_full : kSbTma; };
+    // One scale/bias buffer suffices when no cluster gets more than one row block.
+    auto sbufs = [&](int c) {
+        const int64_t clusters = di.sm_count / c;
+        return (n_tiles + clusters - 1) / clusters <= mt && L.nseg == 1 ? 1 : 2;
+    };
+    auto fits = [&](int c, int stages) {
+        const int g = slice(c);
+        if (c > 1 && sbm_full != kSbTma) return false;
+        if (xfrag_bytes(g, ntm) > (uint32_t)kXFragBudget) return false;
+        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c)).total + 1024) <= di.max_smem_optin;
+    };
     int C = 1;
-    while (C < 8 && ((G + C - 1) / C) * nt * 1024 > kXFragBudget) C *= 2;
-    int gs = (G + C - 1) / C;
-    if (C > 1) gs = (gs + 3) / 4 * 4;           // slices start on a TMA box boundary
-    while (C > 1 && (int64_t)gs * (C - 1) >= G) { C /= 2; gs = (G + C - 1) / C; if (C > 1) gs = (gs + 3) / 4 * 4; }
-    if ((int64_t)gs * nt * 1024 > kXFragBudget) return Q4A_ERR_UNSUPPORTED;
-
-    int stages = 4;
-    SmemLayout lay = smem_layout(nt, mt, stages, gs);
-    while (stages > 2 && (int)(lay.total + 1024) > di.max_smem_optin) lay = smem_layout(nt, mt, --stages, gs);
-    if ((int)(lay.total + 1024) > di.max_smem_optin) return Q4A_ERR_UNSUPPORTED;
+    for (int c = 2; c <= 8; c *= 2) {
+        const bool need = !fits(C, 4) || 5 * n_tiles * C < 4 * (int64_t)di.sm_count * mt;
+        if (!need) break;
+        if ((int64_t)slice(c) * (c - 1) < G && fits(c, 4)) C = c;
+    }
+    const int gs = slice(C);
+    int stages = 8;
+    while (stages > 2 && !fits(C, stages)) --stages;
+    if (!fits(C, stages)) return Q4A_ERR_UNSUPPORTED;
+    const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C));
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
     memset(&prm, 0, sizeof(prm));
     const cuuint64_t dims[2] = {(cuuint64_t)(L.in_dim / 2), (cuuint64_t)L.tensor_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(L.in_dim / 2)};
-    const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, 16u};
     const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+    for (int i = 0; i < kNumMaps; ++i) {
+        const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)(16 << i)};
+        CUresult r = enc(&prm.tmap_w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+    }
 
     prm.s = L.s;
     prm.b = L.b;
@@ -744,15 +1002,23 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.nseg = L.nseg;
     prm.n_tiles = prm.tiles_per_seg * L.nseg;
     prm.mt = mt;
+    prm.ntok_max = ntm;
     prm.stages = stages;
-    const bool al16 = (reinterpret_cast<uintptr_t>(L.s) % 16 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 16 == 0);
-    const bool al4 = (reinterpret_cast<uintptr_t>(L.s) % 4 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 4 == 0);
-    if (G % 8 == 0 && gs % 8 == 0 && al16)
-        prm.sb_mode = kSb16;
-    else if (G % 2 == 0 && al4)
-        prm.sb_mode = kSb4;
-    else
-        prm.sb_mode = kSb2;
+    prm.sb_mode = sbmode(C);
+    if (prm.sb_mode == kSbTma) {
+        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
+        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
+        for (int i = 0; i < kNumMaps; ++i) {
+            const cuuint32_t box[2] = {64u, (cuuint32_t)(16 << i)};
+            for (int k = 0; k < 2; ++k) {
+                CUresult r = enc(k ? &prm.tmap_b[i] : &prm.tmap_s[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t*>(k ? L.b : L.s), sdims, sstrides, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+            }
+        }
+    }
     prm.lay = lay;
     for (int i = 0; i < L.nseg; ++i) prm.seg[i] = L.seg[i];
 

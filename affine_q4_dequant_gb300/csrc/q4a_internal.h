@@ -13,15 +13,22 @@ namespace q4a {
 constexpr int kGroup = 64;              // inputs per scale/bias group
 constexpr int kStageGroups = 8;         // groups per pipeline stage (512 inputs)
 constexpr int kBoxBytes = 128;          // TMA box width in bytes (4 groups), 128B swizzle
-constexpr int kBoxBytesTotal = 16 * kBoxBytes;  // one box: 16 rows x 128 bytes
-constexpr int kConsumerWarps = 8;       // 2 row halves x 4 group slots
+constexpr int kTileBytes = 16 * kBoxBytes;      // one 16-row tile of one box column: 2 KB
+constexpr int kNumMaps = 4;                     // box heights 16, 32, 64, 128 rows
+constexpr int kGroupSlots = kStageGroups; // consumer warps per row half: one stage group each
+constexpr int kConsumerWarps = 2 * kGroupSlots;   // 2 row halves x 8 group slots
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDenseMaxSeg = 8;         // token chunks of one dense call
 constexpr int kXFragBudget = 64 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
+constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 
-// s/b copy modes of the producer warp
-enum SbMode : int { kSb16 = 0, kSb4 = 1, kSb2 = 2 };
+// How the producer fetches a row block's scales and biases into shared memory. Both modes
+// write the same layout: [64-group chunk][row][128 bytes], 16-byte granule u of row r
+// stored at granule u ^ (r & 7) (the TMA 128-byte swizzle).
+//   kSbTma   2D TMA boxes of 64 groups x rows (groups % 8 == 0, 16-byte aligned bases)
+//   kSbPlain producer lanes copy element by element (anything else; full K only)
+enum SbMode : int { kSbTma = 0, kSbPlain = 2 };
 
 struct Segment {
     int32_t row0;   // first row of this segment's matrix in the (bank) tensor
@@ -32,30 +39,57 @@ struct Segment {
 
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-    uint32_t stage_bytes, stage_w_bytes, ring, xfrag, xsum, wpart, cpart, ssq, bars, total;
+    uint32_t stage_bytes;   // one ring stage: mt tiles x 2 box columns x 2 KB of packed weights
+    uint32_t ring, xfrag, xsum, xbias, sb, sb_pitch, sb_buf, n_sb, wpart, cpart, ssq, bars, total;
+    // sb_pitch: bytes of one row block's scales (the biases follow); sb_buf: both
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, int gs) {
+// Row tiles (16 rows) per row block: each of the two row halves of consumer warps holds
+// mt/2 tiles of accumulators: 12-16 fp32 per lane at every NB (the 17 warps of a CTA
+// leave 96 registers per thread).
+__host__ __device__ constexpr int tiles_per_block(int nt) { return nt == 1 ? 6 : (nt == 2 ? 4 : 2); }
+
+// Staged activation fragments: [group][step pair][activation row][lane quad] x 16 bytes,
+// i.e. 128 bytes per (group, row) -- the size of the fp16 activations themselves.
+__host__ __device__ inline uint32_t xfrag_bytes(int gs, int ntok_max) { return (uint32_t)gs * ntok_max * 128u; }
+
+// Row pitch of the staged scale/bias rows: at least the K-slice's groups, padded so that
+// its 32-bit word count is 4 mod 8 -- the 8 rows a warp reads at once then fall in 8
+// different banks.
+// Bytes of one row block's scales (or biases): swizzled 64-group chunks.
+__host__ __device__ inline uint32_t sb_bytes(int /*sb_mode*/, int gs, int rows) {
+    return (uint32_t)((gs + 63) / 64) * rows * 128u;
+}
+
+__host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, int gs, int ntok_max,
+                                                  int sb_mode, int sb_bufs) {
     SmemLayout L;
     const uint32_t ntok = 8u * nt, rows = 16u * mt;
-    L.stage_w_bytes = (uint32_t)mt * 2u * kBoxBytesTotal;
-    L.stage_bytes = L.stage_w_bytes + rows * 32u;          // + s and b, 16 bytes per row each
+    L.stage_bytes = (uint32_t)mt * 2u * kTileBytes;        // [box column][rows][128 B]
     L.ring = 0;                                             // relative to a 1024-aligned base
     L.xfrag = L.ring + (uint32_t)stages * L.stage_bytes;
-    L.xsum = L.xfrag + (uint32_t)gs * nt * 1024u;
-    L.wpart = align_up(L.xsum + (uint32_t)gs * ntok * 4u, 16);
-    L.cpart = L.wpart + 4u * rows * ntok * 4u;
+    L.xsum = L.xfrag + align_up(xfrag_bytes(gs, ntok_max), 16);
+    L.sb_pitch = sb_bytes(sb_mode, gs, rows);               // scales, then biases
+    L.sb_buf = 2u * L.sb_pitch;
+    L.xbias = align_up(L.xsum + (uint32_t)gs * ntok * 4u, 16);   // bf16 hi/lo group sums
+    L.sb = align_up(L.xbias + (uint32_t)((gs + 15) / 16) * ntok_max * 64u, 1024);
+    L.n_sb = (uint32_t)sb_bufs;                             // 2 when a CTA has several row blocks
+    L.wpart = L.sb + L.n_sb * L.sb_buf;
+    L.cpart = L.wpart + (uint32_t)kGroupSlots * rows * ntok * 4u;
     L.ssq = L.cpart + 2u * rows * ntok * 4u;
     L.bars = align_up(L.ssq + 2u * ntok * 4u, 8);
-    L.total = L.bars + 2u * (uint32_t)stages * 8u + 16u;
+    L.total = L.bars + (2u * (uint32_t)stages + 4u) * 8u + 16u;
     return L;
 }
 
 template <int MAXSEG>
 struct GemvParams {
-    CUtensorMap tmap_w;       // 2D uint8: dim0 = in_dim/2 bytes, dim1 = tensor rows
+    CUtensorMap tmap_w[kNumMaps];  // 2D uint8: dim0 = in_dim/2 bytes, dim1 = tensor rows;
+                                   // box 128 bytes x (16 << i) rows, 128-byte swizzle
+    CUtensorMap tmap_s[kNumMaps];  // 2D bf16 scales/biases: dim0 = groups, dim1 = rows;
+    CUtensorMap tmap_b[kNumMaps];  // box 64 groups x (16 << i) rows, 128-byte swizzle
     const uint16_t* s;        // bf16 [rows][G]
     const uint16_t* b;
     const void* x;            // fp16 [*][in_dim] (or fp32 x_raw for the RMSNorm variant)
@@ -73,6 +107,7 @@ struct GemvParams {
     int32_t n_tiles;          // nseg * tiles_per_seg
     int32_t nseg;
     int32_t mt;               // tiles per row block
+    int32_t ntok_max;         // activation rows of the widest segment (<= 8 * NT)
     int32_t stages;           // ring depth
     int32_t sb_mode;
     SmemLayout lay;
