@@ -863,13 +863,67 @@ std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
 template <int NT, bool RMS, int MAXSEG>
-q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
+int occupancy_clusters(int cluster, uint32_t smem_bytes) {
     auto kern = gemv_kernel<NT, RMS, MAXSEG>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const DeviceInfo di = device_info();
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    uint32_t& set = g_smem_set[{fn, dev}];
+    if (set < (uint32_t)di.max_smem_optin) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        set = (uint32_t)di.max_smem_optin;
+    }
+    const OccKey key{fn, dev, cluster, smem_bytes};
+    auto it = g_occ_cache.find(key);
+    if (it == g_occ_cache.end()) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((unsigned)(di.sm_count / cluster * cluster), 1, 1);
+        int occ = 0;
+        if (cudaOccupancyMaxActiveClusters(&occ, kern, &cfg) != cudaSuccess || occ <= 0) {
+            cudaGetLastError();
+            occ = di.sm_count / cluster;
+        }
+        it = g_occ_cache.emplace(key, occ).first;
+    }
+    return it->second;
+}
+
+template <int MAXSEG>
+int cluster_capacity_t(int nt, bool rms, int cluster, uint32_t smem_bytes) {
+    if constexpr (MAXSEG == kDenseMaxSeg) {
+        if (rms) {
+            if (nt == 1) return occupancy_clusters<1, true, MAXSEG>(cluster, smem_bytes);
+            if (nt == 2) return occupancy_clusters<2, true, MAXSEG>(cluster, smem_bytes);
+            return occupancy_clusters<4, true, MAXSEG>(cluster, smem_bytes);
+        }
+    }
+    if (nt == 1) return occupancy_clusters<1, false, MAXSEG>(cluster, smem_bytes);
+    if (nt == 2) return occupancy_clusters<2, false, MAXSEG>(cluster, smem_bytes);
+    return occupancy_clusters<4, false, MAXSEG>(cluster, smem_bytes);
+}
+
+int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_bytes) {
+    return experts ? cluster_capacity_t<Q4A_MAX_SEGMENTS>(nt, rms, cluster, smem_bytes)
+                   : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes);
+}
+
+template <int NT, bool RMS, int MAXSEG>
+q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
+    auto kern = gemv_kernel<NT, RMS, MAXSEG>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -883,30 +937,8 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = di.sm_count / prm.cluster;
-    {
-        std::lock_guard<std::mutex> lock(g_cache_mu);
-        uint32_t& set = g_smem_set[{fn, dev}];
-        if (set < (uint32_t)di.max_smem_optin) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin);
-            if (e != cudaSuccess) return cuda_fail(e);
-            set = (uint32_t)di.max_smem_optin;
-        }
-        const OccKey key{fn, dev, prm.cluster, smem_bytes};
-        auto it = g_occ_cache.find(key);
-        if (it == g_occ_cache.end()) {
-            // How many clusters fit at once (GPC granularity can strand SMs for C > 1).
-            cfg.gridDim = dim3((unsigned)(max_clusters * prm.cluster), 1, 1);
-            cfg.numAttrs = 1;
-            int occ = 0;
-            if (cudaOccupancyMaxActiveClusters(&occ, kern, &cfg) != cudaSuccess || occ <= 0) {
-                cudaGetLastError();
-                occ = max_clusters;
-            }
-            it = g_occ_cache.emplace(key, occ).first;
-        }
-        max_clusters = it->second;
-    }
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG>(prm.cluster, smem_bytes);
+    if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.n_tiles ? max_clusters : prm.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
     cfg.numAttrs = 2;
@@ -917,7 +949,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
                 "clusters=%d (max %d) tiles=%d smem=%u sb_mode=%d\n",
                 NT, (int)RMS, prm.nseg, (long long)prm.out_dim, (long long)prm.in_dim, prm.cluster, prm.gs,
                 prm.mt, prm.stages, prm.n_clusters, max_clusters, prm.n_tiles, smem_bytes, prm.sb_mode);
-    e = cudaLaunchKernelEx(&cfg, kern, prm);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
     if (e != cudaSuccess) return cuda_fail(e);
     return Q4A_OK;
 }
@@ -935,8 +967,10 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     const int mt = tiles_per_block(nt);
     const int G = (int)(L.in_dim / kGroup);
 
-    // Cluster size (K split): the smallest power of two whose K-slice leaves room for a
-    // ring of at least 4 stages, preferring enough tiles per cluster for a full row block.
+    // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
+    // ring of at least 4 stages. Among them: the smallest that gives every cluster >= 3 row
+    // tiles (a row block worth a few TMA boxes) while its co-resident clusters still cover
+    // >= 90% of the SMs (clusters must fit inside a GPC, which can strand SMs).
     const int ntm = L.max_ntok;
     auto slice = [&](int c) {
         int g = (G + c - 1) / c;
@@ -944,12 +978,9 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         return g;
     };
     const int64_t n_tiles = (int64_t)((L.out_dim + 15) / 16) * L.nseg;
-    // Scale/bias fetch mode: TMA needs 16-byte row strides (groups % 8 == 0) and 16-byte
-    // aligned bases; a K split needs it too (its slabs are strided).
     const bool al16 = (reinterpret_cast<uintptr_t>(L.s) % 16 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 16 == 0);
     const int sbm_full = (G % 8 == 0 && al16) ? kSbTma : kSbPlain;
     auto sbmode = [&](int c) { return c == 1 ? sbm_full : kSbTma; };
-    // One scale/bias buffer suffices when no cluster gets more than one row block.
     auto sbufs = [&](int c) {
         const int64_t clusters = di.sm_count / c;
         return (n_tiles + clusters - 1) / clusters <= mt && L.nseg == 1 ? 1 : 2;
@@ -957,15 +988,24 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     auto fits = [&](int c, int stages) {
         const int g = slice(c);
         if (c > 1 && sbm_full != kSbTma) return false;
+        if (c > 1 && (int64_t)g * (c - 1) >= G) return false;
         if (xfrag_bytes(g, ntm) > (uint32_t)kXFragBudget) return false;
         return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c)).total + 1024) <= di.max_smem_optin;
     };
-    int C = 1;
-    for (int c = 2; c <= 8; c *= 2) {
-        const bool need = !fits(C, 4) || 5 * n_tiles * C < 4 * (int64_t)di.sm_count * mt;
-        if (!need) break;
-        if ((int64_t)slice(c) * (c - 1) < G && fits(c, 4)) C = c;
+    int C = 0;
+    for (int c = 1; c <= 8; c *= 2) {
+        if (!fits(c, 4)) continue;
+        if (C == 0) C = c;                       // smallest that fits at all
+        const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
+                                       smem_layout(nt, mt, 4, slice(c), ntm, sbmode(c), sbufs(c)).total + 1024);
+        if (q <= 0) continue;
+        if (n_tiles >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
+            C = c;
+            break;
+        }
+        if (c == C && n_tiles >= 3 * (int64_t)q) break;
     }
+    if (C == 0) return Q4A_ERR_UNSUPPORTED;
     const int gs = slice(C);
     int stages = 8;
     while (stages > 2 && !fits(C, stages)) --stages;

@@ -66,7 +66,7 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -74,13 +74,17 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.tmp = None
+        self.window = None   # (start, end) wall-clock seconds of the timed region
+
+    def mark(self, start: float, end: float):
+        self.window = (start, end)
 
     def __enter__(self):
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -103,10 +107,22 @@ class ClockSampler:
             os.unlink(self.tmp.name)
         except Exception:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        import datetime
+
+        def when(r):
+            try:
+                return datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except Exception:
+                return None
+
+        rows = [r for r in rows if len(r) >= 10]
+        if self.window:
+            inside = [r for r in rows if when(r) is not None and self.window[0] - 0.05 <= when(r) <= self.window[1] + 0.05]
+            rows = inside or rows
+        sm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
 
@@ -214,26 +230,24 @@ def run_ours(args, rank, world, local_rank):
             }
     torch.cuda.synchronize()
 
-    def layer_call(nb, l, evs=None):
+    def gate_up_call(nb, l):
         ly, ac = layers[l], acts[nb]
-        w, s, b = ly["gu"]
-        if evs: evs[0].record(stream)
-        q4a.gemv_rmsnorm(w, s, b, ac["a"], ly["norm_w"], eps=1e-6, out=ac["y_gu"], stream=stream)
-        if evs: evs[1].record(stream)
+        w, s_, b_ = ly["gu"]
+        q4a.gemv_rmsnorm(w, s_, b_, ac["a"], ly["norm_w"], eps=1e-6, out=ac["y_gu"], stream=stream)
+
+    def act_call(nb, l):
+        ac = acts[nb]
         q4a.silu_mul_xsum(ac["y_gu"], h=ac["h"], hsum=ac["hsum"], stream=stream)
-        if evs: evs[2].record(stream)
-        w, s, b = ly["dn"]
-        q4a.gemv(w, s, b, ac["x_dn"], out=ac["y_dn"], stream=stream)
-        if evs: evs[3].record(stream)
 
-    # ---- graphs: one per (step, NB), each with event nodes around every launch ----
-    total_steps = args.warmup + args.steps
+    def down_call(nb, l):
+        ly, ac = layers[l], acts[nb]
+        w, s_, b_ = ly["dn"]
+        q4a.gemv(w, s_, b_, ac["x_dn"], out=ac["y_dn"], stream=stream)
 
-    def new_event():
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return None
+    def layer_call(nb, l):
+        gate_up_call(nb, l)
+        act_call(nb, l)
+        down_call(nb, l)
 
     # eager warm-up: first calls fill the library's per-device caches before capture
     with torch.cuda.stream(stream):
@@ -241,31 +255,31 @@ def run_ours(args, rank, world, local_rank):
             layer_call(nb, 0)
     stream.synchronize()
 
-    graphs, gevents = {}, {}
-    use_graph_events = new_event() is not None
-    for k in range(total_steps):
-        for nb in nbs:
-            evs = [[new_event() for _ in range(4)] for _ in range(L)] if use_graph_events else None
+    # Graphs per NB (no event nodes inside, so programmatic dependent launch overlaps
+    # consecutive kernels): the decode layer over the L weight sets, and one chain per
+    # kernel kind (L gate|up launches, L SiLU*up launches, L down launches) whose replay
+    # time gives the per-launch kernel duration.
+    kinds = {"layer": layer_call, "gate_up": gate_up_call, "act": act_call, "down": down_call}
+    graphs = {}
+    for nb in nbs:
+        for kind, fn in kinds.items():
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for l in range(L):
-                    layer_call(nb, l, evs[l] if evs else None)
-            graphs[(k, nb)] = g
-            gevents[(k, nb)] = evs
+                    fn(nb, l)
+            graphs[(kind, nb)] = g
     torch.cuda.synchronize()
 
-    step_start = [torch.cuda.Event(enable_timing=True) for _ in range(total_steps)]
-    step_end = [torch.cuda.Event(enable_timing=True) for _ in range(total_steps)]
-    nb_start = {(k, nb): torch.cuda.Event(enable_timing=True) for k in range(total_steps) for nb in nbs}
-    nb_end = {(k, nb): torch.cuda.Event(enable_timing=True) for k in range(total_steps) for nb in nbs}
+    total_steps = args.warmup + args.steps
+    ev = {(k, kind, nb, e): torch.cuda.Event(enable_timing=True)
+          for k in range(total_steps) for kind in kinds for nb in nbs for e in (0, 1)}
 
     def run_step(k):
-        step_start[k].record(stream)
         for nb in nbs:
-            nb_start[(k, nb)].record(stream)
-            graphs[(k, nb)].replay()
-            nb_end[(k, nb)].record(stream)
-        step_end[k].record(stream)
+            for kind in kinds:
+                ev[(k, kind, nb, 0)].record(stream)
+                graphs[(kind, nb)].replay()
+                ev[(k, kind, nb, 1)].record(stream)
 
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
@@ -280,6 +294,7 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        w0 = time.time()
         t0.record(stream)
         with torch.cuda.stream(stream):
             for k in range(args.warmup, total_steps):
@@ -287,38 +302,33 @@ def run_ours(args, rank, world, local_rank):
         t1.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
+        clk.mark(w0, time.time())
     if dist is not None:
         dist.barrier()
     q4a.check_device_error(stream)
     elapsed_ms = t0.elapsed_time(t1)
 
-    # per-NB and per-kernel times from the timed steps
     timed = range(args.warmup, total_steps)
-    per_nb = {}
-    gemv_bytes_total, gemv_ms_total, gemv_launches = 0.0, 0.0, 0
-    for nb in nbs:
-        nb_ms = sum(nb_start[(k, nb)].elapsed_time(nb_end[(k, nb)]) for k in timed)
-        gu_b, act_b, dn_b = layer_bytes(nb)
-        rec = {"layer_us": nb_ms / (args.steps * L) * 1e3}
-        if use_graph_events:
-            gu_ms = act_ms = dn_ms = 0.0
-            for k in timed:
-                for ev in gevents[(k, nb)]:
-                    gu_ms += ev[0].elapsed_time(ev[1])
-                    act_ms += ev[1].elapsed_time(ev[2])
-                    dn_ms += ev[2].elapsed_time(ev[3])
-            n = args.steps * L
-            rec.update({
-                "gate_up_us": gu_ms / n * 1e3, "gate_up_gbs": gu_b / (gu_ms / n * 1e-3) / 1e9,
-                "act_us": act_ms / n * 1e3,
-                "down_us": dn_ms / n * 1e3, "down_gbs": dn_b / (dn_ms / n * 1e-3) / 1e9,
-            })
-            gemv_bytes_total += (gu_b + dn_b) * n
-            gemv_ms_total += gu_ms + dn_ms
-            gemv_launches += 2 * n
-        per_nb[str(nb)] = rec
 
-    step_bytes = sum(sum(layer_bytes(nb)) for nb in nbs) * L
+    def kind_ms(kind, nb):
+        return sum(ev[(k, kind, nb, 0)].elapsed_time(ev[(k, kind, nb, 1)]) for k in timed)
+
+    per_nb = {}
+    gemv_bytes_total, gemv_ms_total, step_bytes = 0.0, 0.0, 0.0
+    n = args.steps * L
+    for nb in nbs:
+        gu_b, act_b, dn_b = layer_bytes(nb)
+        gu_ms, act_ms, dn_ms, lay_ms = (kind_ms(k, nb) for k in ("gate_up", "act", "down", "layer"))
+        per_nb[str(nb)] = {
+            "layer_us": lay_ms / n * 1e3,
+            "gate_up_us": gu_ms / n * 1e3, "gate_up_gbs": gu_b / (gu_ms / n * 1e-3) / 1e9,
+            "act_us": act_ms / n * 1e3,
+            "down_us": dn_ms / n * 1e3, "down_gbs": dn_b / (dn_ms / n * 1e-3) / 1e9,
+        }
+        gemv_bytes_total += (gu_b + dn_b) * n
+        gemv_ms_total += gu_ms + dn_ms
+        step_bytes += 2 * (gu_b + act_b + dn_b) * L     # the layer chain + the per-kind chains
+    gemv_launches = 2 * n * len(nbs)
     ms_per_step = elapsed_ms / args.steps
     if dist is not None:
         import torch.distributed as dist
@@ -338,8 +348,11 @@ def run_ours(args, rank, world, local_rank):
         achieved = gemv_bytes_total / (gemv_ms_total * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_kind": peak_kind,
-                    "kernel": "q4a gemv (gemv_kernel, all NB, gate|up with RMSNorm + down)",
-                    "launches": gemv_launches, "traffic": load_traffic()}
+                    "kernel": "gemv_kernel: every q4a_gemv / q4a_gemv_rmsnorm launch of the step",
+                    "kernel_source_sha256_16": kernel_source_hash(),
+                    "launches": gemv_launches, "traffic": load_traffic(),
+                    "timing": "CUDA events around graph replays of back-to-back launches of one kind, "
+                              "inside the timed region"}
 
     if rank != 0:
         return
@@ -349,6 +362,8 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xu4->f32", "data": "synthetic",
         "config": {"workload": "dense decode-layer MLP: 4096->12288 gate|up (fused RMSNorm) + "
                                "silu*up (6144) + 12288->4096 down; affine-Q4 group 64",
+                   "step": "per NB: the decode layer on each of the weight sets, then the same "
+                           "gate|up, silu*up and down launches as one back-to-back chain per kind",
                    "nbs": nbs, "layers_cycled": L,
                    "l2": f"weights cycled over {L} layers ({L * 2 * 28.3:.0f} MB > 3 x L2); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -356,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
         "us_per_decode_layer": {k: v["layer_us"] for k, v in per_nb.items()},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * len(nbs) * L * 3,
+        "gpu_launches": args.steps * len(nbs) * L * 6,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -365,14 +380,94 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def kernel_source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in ("q4a_gemv.cu", "q4a_internal.h"):
+        with open(os.path.join(ROOT, "affine_q4_dequant_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic():
-    """Per-launch DRAM bytes of the GEMV kernel from a committed ncu summary, if present."""
-    path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    """Mean DRAM bytes per GEMV launch of this step from a committed ncu summary; None when
+    the summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemv_step_traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get("traffic_per_launch_bytes")
+            d = json.load(f)
+        if d.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return d.get("traffic_per_launch_bytes")
     except Exception:
         return None
+
+
+KERNEL_SHAPES = {"gate_up": (INTER2, HIDDEN), "down": (DOWN_OUT, DOWN_IN), "lm_head": (151936, HIDDEN),
+                 "small": (256, 512)}
+
+
+def run_kernel_mode(args):
+    """Per-launch time of one GEMV shape: a CUDA graph of back-to-back q4a_gemv calls
+    cycling through weight copies that total > 3 x L2 (every launch streams from HBM)."""
+    import torch
+
+    import affine_q4_dequant_gb300 as q4a
+
+    out_dim, in_dim = KERNEL_SHAPES[args.kernel]
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    wbytes = out_dim * in_dim * BYTES_PER_WEIGHT
+    copies = max(2, int(3 * 130e6 // wbytes) + 1)
+    ws = []
+    for _ in range(copies):
+        codes = torch.randint(0, 16, (out_dim, in_dim), dtype=torch.uint8, device=dev, generator=g)
+        ws.append((q4a.pack(codes), (torch.rand(out_dim, in_dim // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
+                   (torch.randn(out_dim, in_dim // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
+        del codes
+    for nb in [int(v) for v in args.nbs.split(",")]:
+        x = torch.randn(nb, in_dim, device=dev, generator=g).half()
+        y = torch.empty(nb, out_dim, device=dev)
+
+        def call(i):
+            w, s_, b_ = ws[i % copies]
+            q4a.gemv(w, s_, b_, x, out=y)
+
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        if args.profile:
+            # plain launches for a profiler: no graph, no timing
+            for i in range(args.reps):
+                call(3 + i)
+            torch.cuda.synchronize()
+            print(json.dumps({"kernel": "q4a_gemv", "shape": f"{in_dim}->{out_dim}", "nb": nb,
+                              "profile_launches": args.reps + 3}), flush=True)
+            continue
+        n = copies * max(1, args.reps // copies)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(n):
+                call(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / n * 1e3)
+        us = statistics.median(times)
+        nbytes = gemv_bytes(out_dim, in_dim, nb, 2)
+        peak, kind = load_peaks()
+        print(json.dumps({"kernel": "q4a_gemv", "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us,
+                          "gbs": nbytes / us / 1e3, "frac_of_peak": nbytes / us / 1e3 / peak, "peak": peak,
+                          "peak_kind": kind, "weights_per_s": out_dim * in_dim / (us * 1e-6),
+                          "launches_timed": n, "weight_copies": copies}), flush=True)
 
 
 def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
@@ -421,14 +516,22 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--nbs", default="1,2,4,8,16")
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES), default=None,
+                    help="time one GEMV shape per launch instead of the decode-layer step")
+    ap.add_argument("--reps", type=int, default=60)
+    ap.add_argument("--profile", action="store_true",
+                    help="with --kernel: eager launches only (a target for ncu), no timing")
     args = ap.parse_args()
+    if args.kernel:
+        run_kernel_mode(args)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
