@@ -17,8 +17,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libq4a.so")
 BUILD_DIR = os.path.join(ROOT, "_build", "q4a")
-SOURCES = ["q4a_api.cu", "q4a_gemv.cu", "q4a_elementwise.cu"]
-HEADERS = [os.path.join(CSRC, "q4a_internal.h"), os.path.join(ROOT, "include", "q4a.h")]
+SOURCES = ["q4a_api.cu", "q4a_gemv.cu", "q4a_dense_tc.cu", "q4a_elementwise.cu"]
+HEADERS = [os.path.join(CSRC, "q4a_internal.h"), os.path.join(CSRC, "q4a_device.cuh"),
+           os.path.join(ROOT, "include", "q4a.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

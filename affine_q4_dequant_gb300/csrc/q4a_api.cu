@@ -87,6 +87,8 @@ q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_
     if (st != Q4A_OK) return st;
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
         return Q4A_ERR_ALIGN;
+    if (dense_tc_eligible(s, b, nb, in_dim))
+        return launch_dense_tc(w, s, b, x, y, nb, out_dim, in_dim, (cudaStream_t)stream);
     std::vector<Segment> segs;
     push_segments(segs, 0, 0, nb);
     if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
@@ -205,7 +207,10 @@ q4a_status q4a_check_device_error(q4a_stream_t stream) {
     uint32_t word = 0;
     q4a_status st = read_and_clear_device_error((cudaStream_t)stream, &word);
     if (st != Q4A_OK) return st;
-    return word ? Q4A_ERR_TIMEOUT : Q4A_OK;
+    uint32_t word_tc = 0;
+    st = read_and_clear_dense_tc_error(&word_tc);
+    if (st != Q4A_OK) return st;
+    return (word | word_tc) ? Q4A_ERR_TIMEOUT : Q4A_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,628 @@
+// q4a_dense_tc.cu -- the dense path of q4a_gemv for wide activation batches (NB >= 64).
+//
+// Operation: the same y as the GEMV kernel (the "BATCH_MSL" constant page,
+// quantized_rows.metal, fn_q4_rows_h; dequantisation w = s*q + b as in expert_gemm.metal),
+//     y[r][o] = sum_i w[o][i] x[r][i],   w[o][i] = s[o][i/64] * q[o][i] + b[o][i/64].
+// At NB >= 64 this is a real contraction (2*NB flops per 0.5625 bytes of weights), so the
+// weights are dequantised once per call into binary16 tiles in shared memory and multiplied
+// on the 5th-generation tensor cores: tcgen05.mma (kind::f16, fp32 accumulators in TMEM).
+//
+// Precision: every row o gets a power-of-two factor 2^-e_o that puts its largest possible
+// weight, max_g (15|s| + |b|), in [2^13, 2^14). The tile holds w' = fp16(w * 2^-e_o),
+// computed from exact binary16 operands with one fused multiply-add (the codes become
+// exact binary16 integers), so |w' 2^e_o - w| <= 2^-11 |w| for every weight that is not
+// 2^27 below its row's largest; the accumulation is fp32 and the epilogue multiplies by
+// 2^e_o (exact).
+//
+// CTA (448 threads, one per SM, persistent over work units of 256 weight rows):
+//   warp 0       TMA producer: packed codes (128 bytes x 128 rows per box, 4 groups) into a
+//                code ring; the x tile of every group (64 inputs x NB rows) into the
+//                operand ring.
+//   warp 1       allocates TMEM; one thread issues the MMAs: per group, per 128-row tile,
+//                4 x (M 128, N NB, K 16); commits free operand stages and signal the
+//                accumulator.
+//   warps 2..5   epilogue, one TMEM lane quarter each: exponents of the next unit's rows
+//                (ahead of time), then tcgen05.ld of the accumulators, * 2^e, y stores.
+//   warps 6..13  dequantisation, one weight row per thread: codes from the code ring, scale
+//                and bias from global memory, binary16 weights into the operand ring's A
+//                tiles (K-major, 128-byte swizzle: the layout the TMA gives the codes).
+// Both 128-row tiles of a unit multiply the same x tile, which halves x traffic from L2.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+
+#include "q4a_device.cuh"
+#include "q4a_internal.h"
+
+namespace q4a {
+namespace {
+
+constexpr int kTcM = 128;                   // rows of one MMA tile (one TMEM lane per row)
+constexpr int kTcUm = 2;                    // MMA tiles per work unit
+constexpr int kTcUnitRows = kTcM * kTcUm;   // 256
+constexpr int kTcChunkGroups = 4;           // groups per code stage: 128 bytes of each row
+constexpr int kTcTileBytes = kTcM * 128;    // one 128-row tile of 128-byte rows: 16 KB
+constexpr int kTcWarpProducer = 0;
+constexpr int kTcWarpMma = 1;
+constexpr int kTcWarpEpi0 = 2;
+constexpr int kTcEpiWarps = 4;
+constexpr int kTcWarpDq0 = kTcWarpEpi0 + kTcEpiWarps;
+constexpr int kTcDqWarps = 8;
+constexpr int kTcThreads = (kTcWarpDq0 + kTcDqWarps) * 32;   // 448
+constexpr int kTcMaxN = 256;                // MMA N limit = activation rows per launch
+static_assert(kTcDqWarps * 32 == kTcUnitRows, "one dequantisation thread per unit row");
+static_assert(kTcEpiWarps * 32 == kTcM, "one epilogue thread per TMEM lane");
+
+struct TcLayout {
+    uint32_t code;        // code ring: cs stages of kTcUm tiles
+    uint32_t code_stage;
+    uint32_t op;          // operand ring: os stages of [kTcUm A tiles | x tile]
+    uint32_t op_stage;
+    uint32_t op_x;        // offset of the x tile within an operand stage
+    uint32_t exps;        // [2][kTcUnitRows] fp32 2^-e of the rows of the next two units
+    uint32_t bars;
+    uint32_t tmem_slot;
+    uint32_t abort;
+    uint32_t total;
+    int32_t cs, os;
+};
+
+__host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int os) {
+    TcLayout L;
+    L.cs = cs;
+    L.os = os;
+    L.code = 0;
+    L.code_stage = (uint32_t)kTcUm * kTcTileBytes;
+    L.op = L.code + (uint32_t)cs * L.code_stage;
+    L.op_x = (uint32_t)kTcUm * kTcTileBytes;
+    L.op_stage = L.op_x + (uint32_t)n_pad * 128u;          // n_pad % 16 == 0: 2 KB multiples
+    L.exps = L.op + (uint32_t)os * L.op_stage;
+    L.bars = L.exps + 2u * kTcUnitRows * 4u;
+    // code_full[cs] code_empty[cs] op_full[os] op_empty[os] acc_full[2] acc_empty[2]
+    // exp_full[2] exp_empty[2]
+    L.tmem_slot = L.bars + (uint32_t)(2 * cs + 2 * os + 8) * 8u;
+    L.abort = L.tmem_slot + 4u;
+    L.total = L.abort + 4u;
+    return L;
+}
+
+struct TcParams {
+    CUtensorMap tmap_w;   // uint8 [out_dim][in_dim/2], box 128 bytes x 128 rows, 128B swizzle
+    CUtensorMap tmap_x;   // fp16 [nb][in_dim], box 64 x n_pad, 128B swizzle
+    const uint16_t* s;    // bf16 [out_dim][groups]
+    const uint16_t* b;
+    float* y;             // fp32 [nb][out_dim]
+    int64_t out_dim;
+    int32_t groups;
+    int32_t nb;           // activation rows of this launch, 1 .. 256
+    int32_t n_pad;        // nb rounded up to 16: the MMA N
+    int32_t n_units;      // ceil(out_dim / 256)
+    int32_t acc_bufs;     // TMEM accumulator sets: 2 lets one unit's epilogue overlap the next
+    uint32_t tmem_cols;
+    uint32_t idesc;       // tcgen05 instruction descriptor (f16 x f16 -> f32, M 128, N n_pad)
+    TcLayout lay;
+};
+
+// ---- tcgen05 wrappers --------------------------------------------------------------------
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_alloc(uint32_t slot_smem, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand of 128-byte rows, 128-byte swizzle,
+// 8-row groups 1024 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on the mbarrier once every tcgen05.mma this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 TMEM lanes (this warp's quarter) x 16 fp32 columns: thread i gets lane base+i.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint2 ld_nc_8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Byte k of a packed word holds elements 2k (low nibble) and 2k+1 (high nibble). Returns
+// (w[2k], w[2k+1]) as binary16: the byte is copied into both halves, masked to the low
+// nibble (half 0) and the high nibble (half 1, at 16x), turned into 1024 + code with the
+// binary16 exponent of 1024 (exact: codes are integers below 1024), 1024 is taken off
+// (exact), and one fused multiply-add applies (s', s'/16) and (b', b').
+template <int K>
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, __half2 sc, __half2 bi) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(word), "n"(0x4040 | (K << 8) | K));
+    t = (t & 0x00F0000Fu) | 0x64006400u;
+    const __half2 q = __hsub2(bits_h2(t), bits_h2(0x64006400u));
+    return h2_bits(__hfma2(q, sc, bi));
+}
+
+// 2^-e for a row whose largest weight magnitude is at most m: e = floor(log2 m) - 13, so
+// m * 2^-e lies in [2^13, 2^14); e is clamped to [-120, 120] (2^-e and 2^e stay normal fp32).
+__device__ __forceinline__ int row_exponent(float m) {
+    if (!(m > 0.f) || !(m <= 3.0e38f)) return 0;
+    const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+    int e = E - 13;
+    return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// max over the row's groups of 15|s| + |b| (bf16 values, exact in fp32)
+__device__ __forceinline__ float row_weight_bound(const uint16_t* srow, const uint16_t* brow, int G) {
+    float m = 0.f;
+    for (int k = 0; k < G; k += 32) {
+        uint4 sv[4], bv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool on = k + 8 * j < G;
+            sv[j] = on ? ld_nc_16(srow + k + 8 * j) : make_uint4(0, 0, 0, 0);
+            bv[j] = on ? ld_nc_16(brow + k + 8 * j) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t ss[4] = {sv[j].x, sv[j].y, sv[j].z, sv[j].w};
+            const uint32_t bb[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float s0 = fabsf(bf16_to_f32(ss[h] & 0xFFFFu)), s1 = fabsf(bf16_to_f32(ss[h] >> 16));
+                const float b0 = fabsf(bf16_to_f32(bb[h] & 0xFFFFu)), b1 = fabsf(bf16_to_f32(bb[h] >> 16));
+                m = fmaxf(m, fmaxf(fmaf(15.f, s0, b0), fmaf(15.f, s1, b1)));
+            }
+        }
+    }
+    return m;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const TcLayout& L = p.lay;
+    const int CS = L.cs, OS = L.os;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* code_full = bars;
+    uint64_t* code_empty = code_full + CS;
+    uint64_t* op_full = code_empty + CS;
+    uint64_t* op_empty = op_full + OS;
+    uint64_t* acc_full = op_empty + OS;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* exp_full = acc_empty + 2;
+    uint64_t* exp_empty = exp_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L.abort);
+    float* exps = reinterpret_cast<float*>(smem + L.exps);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.groups;
+    const int nchunks = (G + kTcChunkGroups - 1) / kTcChunkGroups;
+
+    grid_dep_launch();
+    if (warp == kTcWarpProducer && lane < 2) prefetch_tensormap(lane ? &p.tmap_x : &p.tmap_w);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < CS; ++i) {
+            mbar_init(smem_addr(code_full + i), 1);
+            mbar_init(smem_addr(code_empty + i), kTcDqWarps);
+        }
+        for (int i = 0; i < OS; ++i) {
+            mbar_init(smem_addr(op_full + i), 1 + kTcDqWarps);
+            mbar_init(smem_addr(op_empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(acc_full + i), 1);
+            mbar_init(smem_addr(acc_empty + i), kTcEpiWarps);
+            mbar_init(smem_addr(exp_full + i), kTcEpiWarps);
+            mbar_init(smem_addr(exp_empty + i), kTcDqWarps);
+        }
+        *abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcWarpMma) tc_alloc(smem_addr(tmem_slot), p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTcWarpProducer) {
+        // ======================= TMA producer =======================
+        if (lane == 0) {
+            int ci = 0, oi = 0;
+            bool dep = false;
+            for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+                const int64_t row0 = (int64_t)unit * kTcUnitRows;
+                const int tiles = (int)llmin((int64_t)kTcUm, (p.out_dim - row0 + kTcM - 1) / kTcM);
+                for (int c = 0; c < nchunks; ++c, ++ci) {
+                    const int s = ci % CS;
+                    if (ci >= CS) mbar_wait(smem_addr(code_empty + s), (uint32_t)(ci / CS - 1) & 1u, abort_flag);
+                    const uint32_t full = smem_addr(code_full + s);
+                    mbar_arrive_expect_tx(full, (uint32_t)(tiles * kTcTileBytes));
+                    for (int u = 0; u < tiles; ++u)
+                        tma_load_2d(smem_addr(smem + L.code + s * L.code_stage + u * kTcTileBytes), &p.tmap_w,
+                                    c * 128, (int)(row0 + u * kTcM), full);
+                    if (!dep) {   // x may be written by the previous kernel of the stream
+                        grid_dep_wait();
+                        dep = true;
+                    }
+                    const int g1 = min(G, (c + 1) * kTcChunkGroups);
+                    for (int g = c * kTcChunkGroups; g < g1; ++g, ++oi) {
+                        const int so = oi % OS;
+                        if (oi >= OS) mbar_wait(smem_addr(op_empty + so), (uint32_t)(oi / OS - 1) & 1u, abort_flag);
+                        const uint32_t of = smem_addr(op_full + so);
+                        mbar_arrive_expect_tx(of, (uint32_t)p.n_pad * 128u);
+                        tma_load_2d(smem_addr(smem + L.op + so * L.op_stage + L.op_x), &p.tmap_x, g * 64, 0, of);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kTcWarpMma) {
+        // ======================= MMA issuer =======================
+        if (lane == 0) {
+            int oi = 0, li = 0;
+            for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
+                const int buf = li % p.acc_bufs;
+                if (li >= p.acc_bufs)
+                    mbar_wait(smem_addr(acc_empty + buf), (uint32_t)(li / p.acc_bufs - 1) & 1u, abort_flag);
+                tc_fence_after();
+                const uint32_t d0 = tmem + (uint32_t)(buf * kTcUm * p.n_pad);
+                for (int g = 0; g < G; ++g, ++oi) {
+                    const int so = oi % OS;
+                    mbar_wait(smem_addr(op_full + so), (uint32_t)(oi / OS) & 1u, abort_flag);
+                    tc_fence_after();
+                    const uint32_t a0 = smem_addr(smem + L.op + so * L.op_stage);
+                    const uint64_t bd = smem_desc(a0 + L.op_x);
+#pragma unroll
+                    for (int u = 0; u < kTcUm; ++u) {
+                        const uint64_t ad = smem_desc(a0 + (uint32_t)(u * kTcTileBytes));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // K 16 per MMA: +32 bytes along each row
+                            tc_mma(d0 + (uint32_t)(u * p.n_pad), ad + 2u * k, bd + 2u * k, p.idesc,
+                                   (uint32_t)(g | k));
+                    }
+                    tc_commit(smem_addr(op_empty + so));
+                }
+                tc_commit(smem_addr(acc_full + buf));
+            }
+        }
+        __syncwarp();
+    } else if (warp < kTcWarpDq0) {
+        // ======================= epilogue =======================
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+        const int rl = quarter * 32 + lane;           // row within each 128-row tile
+        float esc_next[kTcUm];
+        auto exponents = [&](int unit, int slot) {
+#pragma unroll
+            for (int u = 0; u < kTcUm; ++u) {
+                const int64_t row = (int64_t)unit * kTcUnitRows + u * kTcM + rl;
+                int e = 0;
+                float dq = 0.f;                       // rows beyond out_dim dequantise to 0
+                if (row < p.out_dim) {
+                    e = row_exponent(row_weight_bound(p.s + row * G, p.b + row * G, G));
+                    dq = pow2f(-e);
+                }
+                esc_next[u] = pow2f(e);
+                exps[slot * kTcUnitRows + u * kTcM + rl] = dq;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(exp_full + slot));
+        };
+        if ((int)blockIdx.x < p.n_units) exponents(blockIdx.x, 0);
+        grid_dep_wait();                              // y may belong to the previous kernel
+        int li = 0;
+        for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
+            float esc[kTcUm];
+#pragma unroll
+            for (int u = 0; u < kTcUm; ++u) esc[u] = esc_next[u];
+            const int nxt = unit + gridDim.x;
+            if (nxt < p.n_units) {
+                const int slot = (li + 1) & 1;
+                if (li + 1 >= 2) mbar_wait(smem_addr(exp_empty + slot), (uint32_t)((li + 1) / 2 - 1) & 1u, abort_flag);
+                exponents(nxt, slot);
+            }
+            const int buf = li % p.acc_bufs;
+            mbar_wait(smem_addr(acc_full + buf), (uint32_t)(li / p.acc_bufs) & 1u, abort_flag);
+            tc_fence_after();
+#pragma unroll
+            for (int u = 0; u < kTcUm; ++u) {
+                const int64_t row = (int64_t)unit * kTcUnitRows + u * kTcM + rl;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kTcUm + u) * p.n_pad);
+                for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
+                    float v[16];
+                    tc_ld16(taddr + (uint32_t)c0, v);
+                    if (row < p.out_dim) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = v[j] * esc[u];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(acc_empty + buf));
+        }
+    } else {
+        // ======================= dequantisation =======================
+        const int r = (warp - kTcWarpDq0) * 32 + lane;    // row within the unit
+        const int u = r / kTcM;
+        const uint32_t rr = (uint32_t)(r % kTcM);
+        const uint32_t rsw = rr & 7u;
+        const uint32_t row_off = (uint32_t)(u * kTcTileBytes) + rr * 128u;   // same in both rings
+        const uint32_t code_base = smem_addr(smem + L.code) + row_off;
+        const uint32_t a_base = smem_addr(smem + L.op) + row_off;
+        int ci = 0, oi = 0, li = 0;
+        for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
+            const int slot = li & 1;
+            mbar_wait(smem_addr(exp_full + slot), (uint32_t)(li >> 1) & 1u, abort_flag);
+            const float dq = exps[slot * kTcUnitRows + r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(exp_empty + slot));
+            const int64_t row = (int64_t)unit * kTcUnitRows + r;
+            const bool valid = row < p.out_dim;
+            const uint16_t* srow = p.s + (valid ? row : 0) * G;
+            const uint16_t* brow = p.b + (valid ? row : 0) * G;
+            uint2 s_nx = valid ? ld_nc_8(srow) : make_uint2(0, 0);
+            uint2 b_nx = valid ? ld_nc_8(brow) : make_uint2(0, 0);
+            for (int c = 0; c < nchunks; ++c, ++ci) {
+                const uint2 s_cur = s_nx, b_cur = b_nx;
+                if (c + 1 < nchunks && valid) {
+                    s_nx = ld_nc_8(srow + (c + 1) * kTcChunkGroups);
+                    b_nx = ld_nc_8(brow + (c + 1) * kTcChunkGroups);
+                }
+                const int cs_ = ci % CS;
+                mbar_wait(smem_addr(code_full + cs_), (uint32_t)(ci / CS) & 1u, abort_flag);
+                const uint32_t cb = code_base + (uint32_t)cs_ * L.code_stage;
+                const int ng = min(kTcChunkGroups, G - c * kTcChunkGroups);
+                for (int gi = 0; gi < ng; ++gi, ++oi) {
+                    const int so = oi % OS;
+                    if (oi >= OS) mbar_wait(smem_addr(op_empty + so), (uint32_t)(oi / OS - 1) & 1u, abort_flag);
+                    const uint32_t sb16 = (gi & 1) ? ((gi < 2 ? s_cur.x : s_cur.y) >> 16) : ((gi < 2 ? s_cur.x : s_cur.y) & 0xFFFFu);
+                    const uint32_t bb16 = (gi & 1) ? ((gi < 2 ? b_cur.x : b_cur.y) >> 16) : ((gi < 2 ? b_cur.x : b_cur.y) & 0xFFFFu);
+                    const float sf = bf16_to_f32(sb16) * dq;
+                    const float bfv = bf16_to_f32(bb16) * dq;
+                    const __half2 sc = __floats2half2_rn(sf, sf * 0.0625f);
+                    const __half2 bi = __floats2half2_rn(bfv, bfv);
+                    const uint4 q0 = lds_v4(cb + ((((uint32_t)(2 * gi)) ^ rsw) << 4));
+                    const uint4 q1 = lds_v4(cb + ((((uint32_t)(2 * gi + 1)) ^ rsw) << 4));
+                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint32_t ab = a_base + (uint32_t)so * L.op_stage;
+#pragma unroll
+                    for (int w8 = 0; w8 < 8; ++w8) {
+                        const uint32_t wd = words[w8];
+                        sts_v4(ab + ((((uint32_t)w8) ^ rsw) << 4), dequant_pair<0>(wd, sc, bi),
+                               dequant_pair<1>(wd, sc, bi), dequant_pair<2>(wd, sc, bi), dequant_pair<3>(wd, sc, bi));
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(op_full + so));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(code_empty + cs_));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kTcWarpMma) tc_dealloc(tmem, p.tmem_cols);
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tc_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct TcDevice {
+    int sm_count = 0;
+    int max_smem = 0;
+    bool attr_set = false;
+};
+
+std::mutex g_tc_mu;
+std::map<int, TcDevice> g_tc_dev;
+
+// Layout choice: the deepest rings that fit, operand stages first at small N (the MMA
+// needs no more than double buffering when it is the slower side), code stages first at
+// large N. The smem request never drops below half an SM, so two CTAs never share one SM's
+// TMEM (the allocation can then never wait).
+bool tc_pick_layout(int n_pad, int max_smem, TcLayout& out, uint32_t& smem_bytes) {
+    static const int order_small[4][2] = {{3, 3}, {2, 3}, {3, 2}, {2, 2}};
+    static const int order_large[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
+    const int(*order)[2] = n_pad <= 64 ? order_small : order_large;
+    for (int i = 0; i < 4; ++i) {
+        const TcLayout L = tc_layout(n_pad, order[i][0], order[i][1]);
+        const uint32_t need = L.total + 1024u;
+        if ((int)need <= max_smem) {
+            out = L;
+            smem_bytes = need < (uint32_t)max_smem / 2u + 4096u ? (uint32_t)max_smem / 2u + 4096u : need;
+            return true;
+        }
+    }
+    return false;
+}
+
+q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                        const uint16_t* x, float* y, int nb, int64_t out_dim, int64_t in_dim,
+                        cudaStream_t stream) {
+    EncodeTiledFn enc = tc_encode_fn();
+    if (!enc) return Q4A_ERR_UNSUPPORTED;
+    TcParams prm;
+    memset(&prm, 0, sizeof(prm));
+    const cuuint32_t estr[2] = {1u, 1u};
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(in_dim / 2), (cuuint64_t)out_dim};
+        const cuuint64_t strides[1] = {(cuuint64_t)(in_dim / 2)};
+        const cuuint32_t box[2] = {128u, (cuuint32_t)kTcM};
+        CUresult r = enc(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+    }
+    const int n_pad = (nb + 15) / 16 * 16;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)in_dim, (cuuint64_t)nb};
+        const cuuint64_t strides[1] = {(cuuint64_t)in_dim * 2};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)n_pad};
+        CUresult r = enc(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+    }
+    uint32_t smem_bytes = 0;
+    if (!tc_pick_layout(n_pad, dev.max_smem, prm.lay, smem_bytes)) return Q4A_ERR_UNSUPPORTED;
+    prm.s = s;
+    prm.b = b;
+    prm.y = y;
+    prm.out_dim = out_dim;
+    prm.groups = (int32_t)(in_dim / kGroup);
+    prm.nb = nb;
+    prm.n_pad = n_pad;
+    prm.n_units = (int32_t)((out_dim + kTcUnitRows - 1) / kTcUnitRows);
+    prm.acc_bufs = 2 * kTcUm * n_pad <= 512 ? 2 : 1;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(prm.acc_bufs * kTcUm * n_pad)) cols *= 2;
+    prm.tmem_cols = cols;
+    prm.idesc = (1u << 4)                          // D: fp32
+                | (0u << 7) | (0u << 10)           // A, B: fp16
+                | (0u << 15) | (0u << 16)          // both K-major
+                | ((uint32_t)(n_pad >> 3) << 17)   // N
+                | ((uint32_t)(kTcM >> 4) << 24);   // M
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(prm.n_units < dev.sm_count ? prm.n_units : dev.sm_count), 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static const bool debug = getenv("Q4A_DEBUG") != nullptr;
+    if (debug)
+        fprintf(stderr, "q4a dense_tc: out=%lld in=%lld nb=%d n_pad=%d units=%d grid=%u cs=%d os=%d acc_bufs=%d "
+                "tmem_cols=%u smem=%u\n", (long long)out_dim, (long long)in_dim, nb, n_pad, prm.n_units,
+                cfg.gridDim.x, prm.lay.cs, prm.lay.os, prm.acc_bufs, prm.tmem_cols, smem_bytes);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, dense_tc_kernel, prm);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return Q4A_OK;
+}
+
+}  // namespace
+
+bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_dim) {
+    return nb >= kDenseTcMinRows && (in_dim / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(s) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(b) % 16 == 0;
+}
+
+q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                           int nb, int64_t out_dim, int64_t in_dim, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    TcDevice d;
+    {
+        std::lock_guard<std::mutex> lock(g_tc_mu);
+        TcDevice& c = g_tc_dev[dev];
+        if (!c.attr_set) {
+            cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev);
+            cudaDeviceGetAttribute(&c.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
+            if (e != cudaSuccess) return cuda_fail(e);
+            c.attr_set = c.sm_count > 0;
+        }
+        d = c;
+    }
+    if (!d.attr_set) return Q4A_ERR_CUDA;
+    for (int t0 = 0; t0 < nb; t0 += kTcMaxN) {
+        const int n = nb - t0 < kTcMaxN ? nb - t0 : kTcMaxN;
+        const q4a_status st = launch_chunk(d, w, s, b, x + (int64_t)t0 * in_dim, y + (int64_t)t0 * out_dim, n,
+                                           out_dim, in_dim, stream);
+        if (st != Q4A_OK) return st;
+    }
+    return Q4A_OK;
+}
+
+q4a_status read_and_clear_dense_tc_error(uint32_t* word) {
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v) {
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *word = v;
+    return Q4A_OK;
+}
+
+}  // namespace q4a

@@ -33,89 +33,13 @@
 #include <map>
 #include <mutex>
 
+#include "q4a_device.cuh"
 #include "q4a_internal.h"
 
 namespace q4a {
-
-__device__ uint32_t g_device_error;
-
 namespace {
 
 // ---- PTX wrappers ----------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// try_wait with a suspend-time hint: a waiting warp sleeps in hardware until the phase
-// completes (or the hint elapses) instead of spinning and taking issue slots from the
-// warps that compute.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: after kWaitLimitNs the thread records the failure in the device
-// error word and in the CTA's abort flag, then carries on. Control flow never
-// depends on shared-memory data, so a give-up can only produce garbage values,
-// never a hang, a skipped barrier or an out-of-range address.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return;
-        if ((it & 3) == 0) {
-            if (*abort_flag) return;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(&g_device_error, 1u);
-                *abort_flag = 1u;
-                return;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Programmatic dependent launch: the kernel may start while the previous kernel of the
-// stream is finishing; grid_dep_wait() returns once that kernel has completed and its
-// memory is visible. Nothing a previous kernel may write is touched before it.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     uint32_t v;
@@ -174,15 +98,7 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
-__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 __device__ __forceinline__ float half2_sum(uint32_t h2) {
     const __half2 v = *reinterpret_cast<const __half2*>(&h2);
@@ -418,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty_b = bars + S;         // [S]  every consumer warp is done with a stage
     uint64_t* sbfull_b = bars + 2 * S;    // [2]  a row block's scales/biases landed
     uint64_t* sbempty_b = bars + 2 * S + 2;  // [2] every consumer warp is done with them
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 4);
+    uint64_t* rawfull_b = bars + 2 * S + 4;  // [2] raw mode: a row block's raw scales/biases landed
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 6);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -443,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : lane < 2 * kNumMaps ? &p.tmap_s[lane - kNumMaps] : &p.tmap_b[lane - 2 * kNumMaps];
         if (lane < kNumMaps || p.sb_mode == kSbTma)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+        if (p.sb_mode == kSbRaw && lane < 2) prefetch_tensormap(lane ? &p.tmap_b1 : &p.tmap_s1);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -452,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 2; ++q) {
             mbar_init(smem_addr(sbfull_b + q), 1);
             mbar_init(smem_addr(sbempty_b + q), kConsumerWarps);
+            mbar_init(smem_addr(rawfull_b + q), 1);
         }
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -474,8 +393,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             cluster_arrive();
             pending = true;
         }
+        uint8_t* raw = smem + L.raw;   // raw mode: [2 buffers][scales | biases][raw_elems] bf16
+        // Raw mode: 1D boxes over the contiguous [rows][groups] scales and biases of a row
+        // block. The first element is rounded down to a 16-byte boundary (TMA rule); the
+        // transform skips the difference.
+        auto raw_issue = [&](const Job& jb, int buf) {
+            if (lane != 0) return;
+            const Segment& sgb = p.seg[jb.seg];
+            const int64_t r0 = (int64_t)sgb.row0 + (int64_t)jb.tile * 16;
+            const int rv = (int)llmin((int64_t)jb.ntile * 16, p.out_dim - (int64_t)jb.tile * 16);
+            const int64_t e0 = r0 * p.groups;
+            const int64_t e0a = e0 & ~(int64_t)7;
+            const int nbx = (int)((e0 - e0a + (int64_t)rv * p.groups + kRawBox - 1) / kRawBox);
+            const uint32_t bar = smem_addr(rawfull_b + buf);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the last transform's reads
+            mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbx * kRawBox * 2));
+            uint8_t* dst = raw + (size_t)buf * 2u * L.raw_elems * 2u;
+            for (int k = 0; k < nbx; ++k) {
+                tma_load_1d(smem_addr(dst + k * kRawBox * 2), &p.tmap_s1, (int)(e0a + (int64_t)k * kRawBox), bar);
+                tma_load_1d(smem_addr(dst + L.raw_elems * 2u + k * kRawBox * 2), &p.tmap_b1,
+                            (int)(e0a + (int64_t)k * kRawBox), bar);
+            }
+        };
         int t = t_begin;
         Job j;
+        if (p.sb_mode == kSbRaw) {
+            int t2 = t;
+            Job j0;
+            if (next_job(p, t2, t_end, j0)) raw_issue(j0, 0);
+            __syncwarp();
+        }
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = p.seg[j.seg];
             const int64_t lrow0 = (int64_t)j.tile * 16;                 // row within the segment
@@ -505,6 +452,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m0 += h;
                         }
                     }
+                } else if (p.sb_mode == kSbRaw) {
+                    {   // the next row block's raw scales/biases, while this one is rearranged
+                        int t2 = t;
+                        Job jn;
+                        if (next_job(p, t2, t_end, jn)) raw_issue(jn, (blk + 1) & 1);
+                    }
+                    mbar_wait(smem_addr(rawfull_b + (blk & 1)), (uint32_t)(blk >> 1) & 1u, abort_flag);
+                    const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(raw + (size_t)(blk & 1) * 2u * L.raw_elems * 2u);
+                    const int64_t e0 = trow0 * p.groups;
+                    const int off = (int)(e0 - (e0 & ~(int64_t)7));
+                    const int gpad = (gsz + 15) / 16 * 16;   // zero groups up to the next 16-group block
+                    for (int r = lane; r < rows_valid; r += 32) {
+                        const uint16_t* srw = rs_ + off + r * gsz;
+                        for (int k = 0; k < gpad; ++k) {
+                            const uint32_t o = (uint32_t)(((k >> 6) * MT * 16 + r) * 128) +
+                                               ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
+                            const bool in = k < gsz;
+                            *reinterpret_cast<uint16_t*>(sdst + o) = in ? srw[k] : (uint16_t)0;
+                            *reinterpret_cast<uint16_t*>(sdst + L.sb_pitch + o) = in ? srw[L.raw_elems + k] : (uint16_t)0;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar);
                 } else {
                     // element copies into the swizzled layout (full K: one CTA per cluster);
                     // groups up to the next 16-group block are zeroed for the bias contraction
@@ -979,7 +949,14 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     };
     const int64_t n_tiles = (int64_t)((L.out_dim + 15) / 16) * L.nseg;
     const bool al16 = (reinterpret_cast<uintptr_t>(L.s) % 16 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 16 == 0);
-    const int sbm_full = (G % 8 == 0 && al16) ? kSbTma : kSbPlain;
+    // Scales/biases of a full-K row block: 2D TMA when rows are 16-byte multiples, else 1D
+    // TMA of the contiguous block when it fits the raw staging budget, else element copies.
+    int sbm_full = kSbPlain;
+    if (G % 8 == 0 && al16)
+        sbm_full = kSbTma;
+    else if (al16 && L.tensor_rows * G < ((int64_t)1 << 31) - kRawBox &&
+             (uint64_t)(16 * mt) * (uint64_t)G + 7u <= kRawBudget)
+        sbm_full = kSbRaw;
     auto sbmode = [&](int c) { return c == 1 ? sbm_full : kSbTma; };
     auto sbufs = [&](int c) {
         const int64_t clusters = di.sm_count / c;
@@ -1057,6 +1034,18 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
             }
+        }
+    }
+    if (prm.sb_mode == kSbRaw) {
+        const cuuint64_t rdims[1] = {(cuuint64_t)(L.tensor_rows * G)};
+        const cuuint64_t rstrides[1] = {0};
+        const cuuint32_t rbox[1] = {(cuuint32_t)kRawBox};
+        for (int k = 0; k < 2; ++k) {
+            CUresult r = enc(k ? &prm.tmap_b1 : &prm.tmap_s1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1,
+                             const_cast<uint16_t*>(k ? L.b : L.s), rdims, rstrides, rbox, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
         }
     }
     prm.lay = lay;

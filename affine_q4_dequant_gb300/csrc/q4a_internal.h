@@ -22,13 +22,20 @@ constexpr int kDenseMaxSeg = 8;         // token chunks of one dense call
 constexpr int kXFragBudget = 64 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
+constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path
 
 // How the producer fetches a row block's scales and biases into shared memory. Both modes
 // write the same layout: [64-group chunk][row][128 bytes], 16-byte granule u of row r
 // stored at granule u ^ (r & 7) (the TMA 128-byte swizzle).
 //   kSbTma   2D TMA boxes of 64 groups x rows (groups % 8 == 0, 16-byte aligned bases)
+//   kSbRaw   the row block's [rows][groups] scales (and biases) are contiguous: 1D TMA boxes
+//            of 256 elements fetch them, one row block ahead, into a raw staging buffer,
+//            and the producer lanes rearrange them in shared memory (16-byte aligned bases,
+//            any group count up to a staging budget; full K only)
 //   kSbPlain producer lanes copy element by element (anything else; full K only)
-enum SbMode : int { kSbTma = 0, kSbPlain = 2 };
+enum SbMode : int { kSbTma = 0, kSbRaw = 1, kSbPlain = 2 };
+constexpr int kRawBox = 256;                 // elements per 1D box of the raw mode
+constexpr uint32_t kRawBudget = 4096;        // raw staging elements per array and buffer
 
 struct Segment {
     int32_t row0;   // first row of this segment's matrix in the (bank) tensor
@@ -40,7 +47,8 @@ struct Segment {
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
     uint32_t stage_bytes;   // one ring stage: mt tiles x 2 box columns x 2 KB of packed weights
-    uint32_t ring, xfrag, xsum, xbias, sb, sb_pitch, sb_buf, n_sb, wpart, cpart, ssq, bars, total;
+    uint32_t ring, xfrag, xsum, xbias, sb, sb_pitch, sb_buf, n_sb, wpart, cpart, ssq, raw, raw_elems, bars, total;
+    // raw, raw_elems: the raw mode's staging buffers [2 buffers][scales | biases][raw_elems] bf16
     // sb_pitch: bytes of one row block's scales (the biases follow); sb_buf: both
 };
 
@@ -79,8 +87,12 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     L.wpart = L.sb + L.n_sb * L.sb_buf;
     L.cpart = L.wpart + (uint32_t)kGroupSlots * rows * ntok * 4u;
     L.ssq = L.cpart + 2u * rows * ntok * 4u;
-    L.bars = align_up(L.ssq + 2u * ntok * 4u, 8);
-    L.total = L.bars + (2u * (uint32_t)stages + 4u) * 8u + 16u;
+    L.raw = align_up(L.ssq + 2u * ntok * 4u, 128);
+    // a row block's elements plus up to 7 in front (the box start is rounded down to 16 bytes)
+    L.raw_elems = sb_mode == kSbRaw ? align_up(rows * (uint32_t)gs + 7u, (uint32_t)kRawBox) : 0u;
+    L.bars = align_up(L.raw + 2u * 2u * L.raw_elems * 2u, 8);
+    // full[stages] empty[stages] sbfull[2] sbempty[2] rawfull[2], then the abort flag
+    L.total = L.bars + (2u * (uint32_t)stages + 6u) * 8u + 16u;
     return L;
 }
 
@@ -90,6 +102,8 @@ struct GemvParams {
                                    // box 128 bytes x (16 << i) rows, 128-byte swizzle
     CUtensorMap tmap_s[kNumMaps];  // 2D bf16 scales/biases: dim0 = groups, dim1 = rows;
     CUtensorMap tmap_b[kNumMaps];  // box 64 groups x (16 << i) rows, 128-byte swizzle
+    CUtensorMap tmap_s1;           // raw mode: 1D bf16 views of s and b (rows * groups
+    CUtensorMap tmap_b1;           // elements), box kRawBox elements
     const uint16_t* s;        // bf16 [rows][G]
     const uint16_t* b;
     const void* x;            // fp16 [*][in_dim] (or fp32 x_raw for the RMSNorm variant)
@@ -143,6 +157,13 @@ q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, 
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim,
                            cudaStream_t stream);
 q4a_status read_and_clear_device_error(cudaStream_t stream, uint32_t* word);
+
+// Dense path for wide batches (q4a_dense_tc.cu): dequantise to binary16 tiles, tcgen05.mma.
+// Eligible when nb >= kDenseTcMinRows, in_dim % 512 == 0 and s, b are 16-byte aligned.
+bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_dim);
+q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                           int nb, int64_t out_dim, int64_t in_dim, cudaStream_t stream);
+q4a_status read_and_clear_dense_tc_error(uint32_t* word);   // after a stream synchronisation
 
 // Records a CUDA error for q4a_last_cuda_error and returns Q4A_ERR_CUDA.
 q4a_status cuda_fail(cudaError_t e);

@@ -384,7 +384,7 @@ def kernel_source_hash():
     import hashlib
 
     h = hashlib.sha256()
-    for name in ("q4a_gemv.cu", "q4a_internal.h"):
+    for name in ("q4a_gemv.cu", "q4a_internal.h", "q4a_device.cuh"):
         with open(os.path.join(ROOT, "affine_q4_dequant_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -470,6 +470,100 @@ def run_kernel_mode(args):
                           "launches_timed": n, "weight_copies": copies}), flush=True)
 
 
+def graph_us(torch, fn, n, trials=5):
+    """Median per-call time of a CUDA graph of n back-to-back fn(i) calls."""
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(n):
+            fn(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(trials):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / n * 1e3)
+    return statistics.median(times)
+
+
+def run_moe_mode(args):
+    """One routed MoE layer on the 64-expert bank (hidden 2048, inter 640, 16 tokens,
+    top-8 by N(0,1) logits): q4a_gemv_experts on gate|up with the token map, the
+    SiLU*up activation, q4a_gemv_experts on down. Bank replicas total > 3 x L2."""
+    import torch
+
+    import affine_q4_dequant_gb300 as q4a
+
+    E, H, I, T = wl.MOE_EXPERTS, wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_TOKENS
+    r = wl.route_by_logits(wl.moe_logits(), wl.MOE_TOP_K)
+    U, slots = int(r.expert_ids.shape[0]), int(r.token_offsets[-1])
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+
+    def bank(rows, cols):
+        codes = torch.randint(0, 16, (rows, cols), dtype=torch.uint8, device=dev, generator=g)
+        return (q4a.pack(codes), (torch.rand(rows, cols // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
+                (torch.randn(rows, cols // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16))
+
+    per_expert = (2 * I * H + H * I) * BYTES_PER_WEIGHT
+    copies = max(2, int(3 * 130e6 // (E * per_expert)) + 1)
+    banks = [(bank(E * 2 * I, H), bank(E * H, I)) for _ in range(copies)]
+    x = torch.randn(T, H, device=dev, generator=g).half()
+    x_rows = torch.from_numpy(r.x_rows).to(dev)
+    y_gu = torch.empty(slots, 2 * I, device=dev)
+    h = torch.empty(slots, I, dtype=torch.float16, device=dev)
+    hs = torch.empty(slots, I // 64, device=dev)
+    y_dn = torch.empty(slots, H, device=dev)
+
+    def gate_up(i):
+        w, s_, b_ = banks[i % copies][0]
+        q4a.gemv_experts(w, s_, b_, x, x_rows, r.expert_ids, r.token_offsets, E, 2 * I, out=y_gu)
+
+    def act(i):
+        q4a.silu_mul_xsum(y_gu, h=h, hsum=hs)
+
+    def down(i):
+        w, s_, b_ = banks[i % copies][1]
+        q4a.gemv_experts(w, s_, b_, h, None, r.expert_ids, r.token_offsets, E, H, out=y_dn)
+
+    def layer(i):
+        gate_up(i)
+        act(i)
+        down(i)
+
+    for i in range(3):
+        layer(i)
+    torch.cuda.synchronize()
+    if args.profile:
+        for i in range(args.reps):
+            layer(3 + i)
+        torch.cuda.synchronize()
+        q4a.check_device_error()
+        print(json.dumps({"kernel": "moe_layer", "profile_layers": args.reps + 3}), flush=True)
+        return
+    n = copies * max(1, args.reps // copies)
+    us = {k: graph_us(torch, fn, n) for k, fn in (("gate_up", gate_up), ("act", act), ("down", down),
+                                                   ("layer", layer))}
+    q4a.check_device_error()
+    gu_b = U * 2 * I * H * BYTES_PER_WEIGHT + T * H * 2 + slots * 2 * I * 4
+    act_b = slots * 2 * I * 4 + slots * I * 2 + slots * (I // 64) * 4
+    dn_b = U * H * I * BYTES_PER_WEIGHT + slots * I * 2 + slots * H * 4
+    peak, kind = load_peaks()
+    print(json.dumps({
+        "kernel": "moe_layer", "experts": E, "union_experts": U, "slots": slots,
+        "touched_weight_bytes": U * per_expert, "us_per_moe_layer": us["layer"],
+        "gate_up_us": us["gate_up"], "gate_up_gbs": gu_b / us["gate_up"] / 1e3,
+        "act_us": us["act"], "down_us": us["down"], "down_gbs": dn_b / us["down"] / 1e3,
+        "layer_gbs": (gu_b + act_b + dn_b) / us["layer"] / 1e3,
+        "frac_of_peak_gate_up": gu_b / us["gate_up"] / 1e3 / peak,
+        "frac_of_peak_down": dn_b / us["down"] / 1e3 / peak, "peak": peak, "peak_kind": kind,
+        "launches_timed": n, "bank_copies": copies}), flush=True)
+
+
 def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
     """Public API, host buffers: every step copies each NB's activations in from pinned
     memory, runs one decode-layer MLP per NB through the binding (eager launches, no
@@ -523,12 +617,15 @@ def main():
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES), default=None,
+    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe"], default=None,
                     help="time one GEMV shape per launch instead of the decode-layer step")
     ap.add_argument("--reps", type=int, default=60)
     ap.add_argument("--profile", action="store_true",
                     help="with --kernel: eager launches only (a target for ncu), no timing")
     args = ap.parse_args()
+    if args.kernel == "moe":
+        run_moe_mode(args)
+        return
     if args.kernel:
         run_kernel_mode(args)
         return
