@@ -4,29 +4,37 @@
 // quantized_rows.metal, fn_q4_rows_h; dequantisation w = s*q + b as in expert_gemm.metal),
 //     y[r][o] = sum_i w[o][i] x[r][i],   w[o][i] = s[o][i/64] * q[o][i] + b[o][i/64].
 // At NB >= 64 this is a real contraction (2*NB flops per 0.5625 bytes of weights), so the
-// weights are dequantised once per call into binary16 tiles in shared memory and multiplied
-// on the 5th-generation tensor cores: tcgen05.mma (kind::f16, fp32 accumulators in TMEM).
+// weights are dequantised once per call into binary16 and multiplied on the 5th-generation
+// tensor cores: tcgen05.mma kind::f16, A (the weights) in TMEM, B (x) in shared memory,
+// fp32 accumulators in TMEM.
 //
 // Precision: every row o gets a power-of-two factor 2^-e_o that puts its largest possible
-// weight, max_g (15|s| + |b|), in [2^13, 2^14). The tile holds w' = fp16(w * 2^-e_o),
+// weight, max_g (15|s| + |b|), in [2^13, 2^14). The operand holds w' = fp16(w * 2^-e_o),
 // computed from exact binary16 operands with one fused multiply-add (the codes become
 // exact binary16 integers), so |w' 2^e_o - w| <= 2^-11 |w| for every weight that is not
 // 2^27 below its row's largest; the accumulation is fp32 and the epilogue multiplies by
 // 2^e_o (exact).
 //
-// CTA (448 threads, one per SM, persistent over work units of 256 weight rows):
-//   warp 0       TMA producer: packed codes (128 bytes x 128 rows per box, 4 groups) into a
-//                code ring; the x tile of every group (64 inputs x NB rows) into the
-//                operand ring.
-//   warp 1       allocates TMEM; one thread issues the MMAs: per group, per 128-row tile,
-//                4 x (M 128, N NB, K 16); commits free operand stages and signal the
-//                accumulator.
+// Why A lives in TMEM: a 128 x N x 16 MMA costs the tensor core about 55 cycles for N <= 64
+// and 64 cycles at N = 128, while staging A through shared memory (written by the
+// dequantising threads, read by the MMA) adds 64 KB of shared-memory traffic per 64-input
+// group of a 256-row unit -- more than the 128 bytes/cycle the SM's shared memory moves in
+// that time. tcgen05.st writes the dequantised rows straight into TMEM, so shared memory
+// only carries the packed codes and the x tiles.
+//
+// CTA (480 threads, one per SM, persistent over work units of 256 weight rows = two MMA
+// tiles of 128 rows that share every x tile):
+//   warp 0       TMA producer of the packed codes (128 bytes x 128 rows per box, 4 groups)
+//                into a code ring; it waits only for that ring.
+//   warp 1       allocates TMEM; one thread issues the MMAs: per group, per tile,
+//                4 x (M 128, N NB, K 16) with A from TMEM; commits free the A stage and the
+//                x stage, and signal the accumulator after a unit's last group.
 //   warps 2..5   epilogue, one TMEM lane quarter each: exponents of the next unit's rows
 //                (ahead of time), then tcgen05.ld of the accumulators, * 2^e, y stores.
-//   warps 6..13  dequantisation, one weight row per thread: codes from the code ring, scale
-//                and bias from global memory, binary16 weights into the operand ring's A
-//                tiles (K-major, 128-byte swizzle: the layout the TMA gives the codes).
-// Both 128-row tiles of a unit multiply the same x tile, which halves x traffic from L2.
+//   warps 6..13  dequantisation, one weight row per thread (warp w owns TMEM lane quarter
+//                w % 4 of tile (w - 6) / 4): codes from the code ring, scale and bias from
+//                global memory, 64 binary16 weights per group into a TMEM A stage.
+//   warp 14      TMA producer of the x tile of every group (64 inputs x NB rows).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,45 +56,47 @@ constexpr int kTcUm = 2;                    // MMA tiles per work unit
 constexpr int kTcUnitRows = kTcM * kTcUm;   // 256
 constexpr int kTcChunkGroups = 4;           // groups per code stage: 128 bytes of each row
 constexpr int kTcTileBytes = kTcM * 128;    // one 128-row tile of 128-byte rows: 16 KB
+constexpr int kTcACols = 32;                // TMEM columns of one tile's group: 64 fp16
+constexpr int kTcAStages = 4;               // A stages in TMEM
 constexpr int kTcWarpProducer = 0;
 constexpr int kTcWarpMma = 1;
 constexpr int kTcWarpEpi0 = 2;
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcWarpDq0 = kTcWarpEpi0 + kTcEpiWarps;
 constexpr int kTcDqWarps = 8;
-constexpr int kTcThreads = (kTcWarpDq0 + kTcDqWarps) * 32;   // 448
-constexpr int kTcMaxN = 256;                // MMA N limit = activation rows per launch
+constexpr int kTcWarpX = kTcWarpDq0 + kTcDqWarps;          // x-tile producer
+constexpr int kTcThreads = (kTcWarpX + 1) * 32;              // 480
+constexpr int kTcMaxN = 128;                // activation rows per launch (MMA N, TMEM budget)
 static_assert(kTcDqWarps * 32 == kTcUnitRows, "one dequantisation thread per unit row");
 static_assert(kTcEpiWarps * 32 == kTcM, "one epilogue thread per TMEM lane");
+static_assert(kTcDqWarps == 4 * kTcUm, "one dequantisation warp per TMEM lane quarter and tile");
 
 struct TcLayout {
     uint32_t code;        // code ring: cs stages of kTcUm tiles
     uint32_t code_stage;
-    uint32_t op;          // operand ring: os stages of [kTcUm A tiles | x tile]
-    uint32_t op_stage;
-    uint32_t op_x;        // offset of the x tile within an operand stage
+    uint32_t xr;          // x ring: xs stages of [n_pad rows][128 bytes]
+    uint32_t x_stage;
     uint32_t exps;        // [2][kTcUnitRows] fp32 2^-e of the rows of the next two units
     uint32_t bars;
     uint32_t tmem_slot;
     uint32_t abort;
     uint32_t total;
-    int32_t cs, os;
+    int32_t cs, xs;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int os) {
+__host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
     TcLayout L;
     L.cs = cs;
-    L.os = os;
+    L.xs = xs;
     L.code = 0;
     L.code_stage = (uint32_t)kTcUm * kTcTileBytes;
-    L.op = L.code + (uint32_t)cs * L.code_stage;
-    L.op_x = (uint32_t)kTcUm * kTcTileBytes;
-    L.op_stage = L.op_x + (uint32_t)n_pad * 128u;          // n_pad % 16 == 0: 2 KB multiples
-    L.exps = L.op + (uint32_t)os * L.op_stage;
+    L.xr = L.code + (uint32_t)cs * L.code_stage;
+    L.x_stage = (uint32_t)n_pad * 128u;                     // n_pad % 16 == 0: 2 KB multiples
+    L.exps = L.xr + (uint32_t)xs * L.x_stage;
     L.bars = L.exps + 2u * kTcUnitRows * 4u;
-    // code_full[cs] code_empty[cs] op_full[os] op_empty[os] acc_full[2] acc_empty[2]
-    // exp_full[2] exp_empty[2]
-    L.tmem_slot = L.bars + (uint32_t)(2 * cs + 2 * os + 8) * 8u;
+    // code_full[cs] code_empty[cs] x_full[xs] x_empty[xs] a_full[A] a_empty[A]
+    // acc_full[2] acc_empty[2] exp_full[2] exp_empty[2]
+    L.tmem_slot = L.bars + (uint32_t)(2 * cs + 2 * xs + 2 * kTcAStages + 8) * 8u;
     L.abort = L.tmem_slot + 4u;
     L.total = L.abort + 4u;
     return L;
@@ -100,10 +110,11 @@ struct TcParams {
     float* y;             // fp32 [nb][out_dim]
     int64_t out_dim;
     int32_t groups;
-    int32_t nb;           // activation rows of this launch, 1 .. 256
+    int32_t nb;           // activation rows of this launch, 1 .. kTcMaxN
     int32_t n_pad;        // nb rounded up to 16: the MMA N
     int32_t n_units;      // ceil(out_dim / 256)
     int32_t acc_bufs;     // TMEM accumulator sets: 2 lets one unit's epilogue overlap the next
+    uint32_t a_col0;      // first TMEM column of the A stages (after the accumulators)
     uint32_t tmem_cols;
     uint32_t idesc;       // tcgen05 instruction descriptor (f16 x f16 -> f32, M 128, N n_pad)
     TcLayout lay;
@@ -131,13 +142,28 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
            ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D (TMEM) += A (TMEM, 128 lanes x 8 columns of fp16 pairs) * B (shared memory descriptor).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// 32 TMEM lanes (this warp's quarter) x 32 columns from 32 registers per thread; returns
+// once the stores have completed.
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrives on the mbarrier once every tcgen05.mma this thread issued before has completed.
@@ -164,10 +190,6 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
-}
-
-__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ uint2 ld_nc_8(const void* p) {
@@ -235,13 +257,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const TcLayout& L = p.lay;
-    const int CS = L.cs, OS = L.os;
+    const int CS = L.cs, XS = L.xs;
+    constexpr int AS = kTcAStages;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* code_full = bars;
     uint64_t* code_empty = code_full + CS;
-    uint64_t* op_full = code_empty + CS;
-    uint64_t* op_empty = op_full + OS;
-    uint64_t* acc_full = op_empty + OS;
+    uint64_t* x_full = code_empty + CS;
+    uint64_t* x_empty = x_full + XS;
+    uint64_t* a_full = x_empty + XS;
+    uint64_t* a_empty = a_full + AS;
+    uint64_t* acc_full = a_empty + AS;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* exp_full = acc_empty + 2;
     uint64_t* exp_empty = exp_full + 2;
@@ -254,15 +279,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     const int nchunks = (G + kTcChunkGroups - 1) / kTcChunkGroups;
 
     grid_dep_launch();
-    if (warp == kTcWarpProducer && lane < 2) prefetch_tensormap(lane ? &p.tmap_x : &p.tmap_w);
+    if (warp == kTcWarpProducer && lane == 0) prefetch_tensormap(&p.tmap_w);
+    if (warp == kTcWarpX && lane == 0) prefetch_tensormap(&p.tmap_x);
     if (threadIdx.x == 0) {
         for (int i = 0; i < CS; ++i) {
             mbar_init(smem_addr(code_full + i), 1);
             mbar_init(smem_addr(code_empty + i), kTcDqWarps);
         }
-        for (int i = 0; i < OS; ++i) {
-            mbar_init(smem_addr(op_full + i), 1 + kTcDqWarps);
-            mbar_init(smem_addr(op_empty + i), 1);
+        for (int i = 0; i < XS; ++i) {
+            mbar_init(smem_addr(x_full + i), 1);
+            mbar_init(smem_addr(x_empty + i), 1);
+        }
+        for (int i = 0; i < AS; ++i) {
+            mbar_init(smem_addr(a_full + i), kTcDqWarps);
+            mbar_init(smem_addr(a_empty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(acc_full + i), 1);
@@ -280,10 +310,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kTcWarpProducer) {
-        // ======================= TMA producer =======================
+        // ======================= TMA producer: codes =======================
         if (lane == 0) {
-            int ci = 0, oi = 0;
-            bool dep = false;
+            int ci = 0;
             for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
                 const int64_t row0 = (int64_t)unit * kTcUnitRows;
                 const int tiles = (int)llmin((int64_t)kTcUm, (p.out_dim - row0 + kTcM - 1) / kTcM);
@@ -295,18 +324,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     for (int u = 0; u < tiles; ++u)
                         tma_load_2d(smem_addr(smem + L.code + s * L.code_stage + u * kTcTileBytes), &p.tmap_w,
                                     c * 128, (int)(row0 + u * kTcM), full);
-                    if (!dep) {   // x may be written by the previous kernel of the stream
-                        grid_dep_wait();
-                        dep = true;
-                    }
-                    const int g1 = min(G, (c + 1) * kTcChunkGroups);
-                    for (int g = c * kTcChunkGroups; g < g1; ++g, ++oi) {
-                        const int so = oi % OS;
-                        if (oi >= OS) mbar_wait(smem_addr(op_empty + so), (uint32_t)(oi / OS - 1) & 1u, abort_flag);
-                        const uint32_t of = smem_addr(op_full + so);
-                        mbar_arrive_expect_tx(of, (uint32_t)p.n_pad * 128u);
-                        tma_load_2d(smem_addr(smem + L.op + so * L.op_stage + L.op_x), &p.tmap_x, g * 64, 0, of);
-                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kTcWarpX) {
+        // ======================= TMA producer: x tiles =======================
+        if (lane == 0) {
+            grid_dep_wait();   // x may be written by the previous kernel of the stream
+            int xi = 0;
+            for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+                for (int g = 0; g < G; ++g, ++xi) {
+                    const int sx = xi % XS;
+                    if (xi >= XS) mbar_wait(smem_addr(x_empty + sx), (uint32_t)(xi / XS - 1) & 1u, abort_flag);
+                    const uint32_t xf = smem_addr(x_full + sx);
+                    mbar_arrive_expect_tx(xf, L.x_stage);
+                    tma_load_2d(smem_addr(smem + L.xr + sx * L.x_stage), &p.tmap_x, g * 64, 0, xf);
                 }
             }
         }
@@ -314,28 +347,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     } else if (warp == kTcWarpMma) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
-            int oi = 0, li = 0;
+            int gi = 0, li = 0;
             for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
                 const int buf = li % p.acc_bufs;
                 if (li >= p.acc_bufs)
                     mbar_wait(smem_addr(acc_empty + buf), (uint32_t)(li / p.acc_bufs - 1) & 1u, abort_flag);
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)(buf * kTcUm * p.n_pad);
-                for (int g = 0; g < G; ++g, ++oi) {
-                    const int so = oi % OS;
-                    mbar_wait(smem_addr(op_full + so), (uint32_t)(oi / OS) & 1u, abort_flag);
+                for (int g = 0; g < G; ++g, ++gi) {
+                    const int sx = gi % XS, sa = gi % AS;
+                    mbar_wait(smem_addr(x_full + sx), (uint32_t)(gi / XS) & 1u, abort_flag);
+                    mbar_wait(smem_addr(a_full + sa), (uint32_t)(gi / AS) & 1u, abort_flag);
                     tc_fence_after();
-                    const uint32_t a0 = smem_addr(smem + L.op + so * L.op_stage);
-                    const uint64_t bd = smem_desc(a0 + L.op_x);
+                    const uint64_t bd = smem_desc(smem_addr(smem + L.xr + sx * L.x_stage));
+                    const uint32_t a0 = tmem + p.a_col0 + (uint32_t)(sa * kTcUm * kTcACols);
 #pragma unroll
-                    for (int u = 0; u < kTcUm; ++u) {
-                        const uint64_t ad = smem_desc(a0 + (uint32_t)(u * kTcTileBytes));
+                    for (int u = 0; u < kTcUm; ++u)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)   // K 16 per MMA: +32 bytes along each row
-                            tc_mma(d0 + (uint32_t)(u * p.n_pad), ad + 2u * k, bd + 2u * k, p.idesc,
-                                   (uint32_t)(g | k));
-                    }
-                    tc_commit(smem_addr(op_empty + so));
+                        for (int k = 0; k < 4; ++k)   // K 16 per MMA: 8 TMEM columns of A, 32 bytes of x
+                            tc_mma_ts(d0 + (uint32_t)(u * p.n_pad), a0 + (uint32_t)(u * kTcACols + 8 * k),
+                                      bd + 2u * k, p.idesc, (uint32_t)(g | k));
+                    tc_commit(smem_addr(x_empty + sx));
+                    tc_commit(smem_addr(a_empty + sa));
                 }
                 tc_commit(smem_addr(acc_full + buf));
             }
@@ -396,16 +429,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(acc_empty + buf));
         }
-    } else {
+    } else if (warp < kTcWarpX) {
         // ======================= dequantisation =======================
-        const int r = (warp - kTcWarpDq0) * 32 + lane;    // row within the unit
-        const int u = r / kTcM;
-        const uint32_t rr = (uint32_t)(r % kTcM);
-        const uint32_t rsw = rr & 7u;
-        const uint32_t row_off = (uint32_t)(u * kTcTileBytes) + rr * 128u;   // same in both rings
-        const uint32_t code_base = smem_addr(smem + L.code) + row_off;
-        const uint32_t a_base = smem_addr(smem + L.op) + row_off;
-        int ci = 0, oi = 0, li = 0;
+        const int quarter = warp & 3;                     // TMEM lanes this warp may write
+        const int u = (warp - kTcWarpDq0) / 4;            // tile
+        const int rl = quarter * 32 + lane;               // row within the tile = TMEM lane
+        const int r = u * kTcM + rl;                      // row within the unit
+        const uint32_t rsw = (uint32_t)rl & 7u;
+        const uint32_t code_base = smem_addr(smem + L.code) + (uint32_t)(u * kTcTileBytes) + (uint32_t)rl * 128u;
+        const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 + (uint32_t)(u * kTcACols);
+        int ci = 0, gi = 0, li = 0;
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             const int slot = li & 1;
             mbar_wait(smem_addr(exp_full + slot), (uint32_t)(li >> 1) & 1u, abort_flag);
@@ -428,28 +461,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                 mbar_wait(smem_addr(code_full + cs_), (uint32_t)(ci / CS) & 1u, abort_flag);
                 const uint32_t cb = code_base + (uint32_t)cs_ * L.code_stage;
                 const int ng = min(kTcChunkGroups, G - c * kTcChunkGroups);
-                for (int gi = 0; gi < ng; ++gi, ++oi) {
-                    const int so = oi % OS;
-                    if (oi >= OS) mbar_wait(smem_addr(op_empty + so), (uint32_t)(oi / OS - 1) & 1u, abort_flag);
-                    const uint32_t sb16 = (gi & 1) ? ((gi < 2 ? s_cur.x : s_cur.y) >> 16) : ((gi < 2 ? s_cur.x : s_cur.y) & 0xFFFFu);
-                    const uint32_t bb16 = (gi & 1) ? ((gi < 2 ? b_cur.x : b_cur.y) >> 16) : ((gi < 2 ? b_cur.x : b_cur.y) & 0xFFFFu);
-                    const float sf = bf16_to_f32(sb16) * dq;
-                    const float bfv = bf16_to_f32(bb16) * dq;
+                for (int k = 0; k < ng; ++k, ++gi) {
+                    const int sa = gi % AS;
+                    const uint32_t sp = k < 2 ? s_cur.x : s_cur.y;
+                    const uint32_t bp = k < 2 ? b_cur.x : b_cur.y;
+                    const float sf = bf16_to_f32((k & 1) ? (sp >> 16) : (sp & 0xFFFFu)) * dq;
+                    const float bfv = bf16_to_f32((k & 1) ? (bp >> 16) : (bp & 0xFFFFu)) * dq;
                     const __half2 sc = __floats2half2_rn(sf, sf * 0.0625f);
                     const __half2 bi = __floats2half2_rn(bfv, bfv);
-                    const uint4 q0 = lds_v4(cb + ((((uint32_t)(2 * gi)) ^ rsw) << 4));
-                    const uint4 q1 = lds_v4(cb + ((((uint32_t)(2 * gi + 1)) ^ rsw) << 4));
+                    const uint4 q0 = lds_v4(cb + ((((uint32_t)(2 * k)) ^ rsw) << 4));
+                    const uint4 q1 = lds_v4(cb + ((((uint32_t)(2 * k + 1)) ^ rsw) << 4));
                     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    const uint32_t ab = a_base + (uint32_t)so * L.op_stage;
+                    uint32_t h[32];
 #pragma unroll
                     for (int w8 = 0; w8 < 8; ++w8) {
-                        const uint32_t wd = words[w8];
-                        sts_v4(ab + ((((uint32_t)w8) ^ rsw) << 4), dequant_pair<0>(wd, sc, bi),
-                               dequant_pair<1>(wd, sc, bi), dequant_pair<2>(wd, sc, bi), dequant_pair<3>(wd, sc, bi));
+                        h[4 * w8 + 0] = dequant_pair<0>(words[w8], sc, bi);
+                        h[4 * w8 + 1] = dequant_pair<1>(words[w8], sc, bi);
+                        h[4 * w8 + 2] = dequant_pair<2>(words[w8], sc, bi);
+                        h[4 * w8 + 3] = dequant_pair<3>(words[w8], sc, bi);
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (gi >= AS) mbar_wait(smem_addr(a_empty + sa), (uint32_t)(gi / AS - 1) & 1u, abort_flag);
+                    tc_fence_after();
+                    tc_st32(a_lane + (uint32_t)(sa * kTcUm * kTcACols), h);
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(op_full + so));
+                    if (lane == 0) mbar_arrive(smem_addr(a_full + sa));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(code_empty + cs_));
@@ -492,15 +528,12 @@ struct TcDevice {
 std::mutex g_tc_mu;
 std::map<int, TcDevice> g_tc_dev;
 
-// Layout choice: the deepest rings that fit, operand stages first at small N (the MMA
-// needs no more than double buffering when it is the slower side), code stages first at
-// large N. The smem request never drops below half an SM, so two CTAs never share one SM's
-// TMEM (the allocation can then never wait).
+// Layout choice: the deepest code ring that fits (its depth is the HBM prefetch distance),
+// then the x ring. The smem request never drops below half an SM, so two CTAs never share
+// one SM's TMEM (the allocation can then never wait).
 bool tc_pick_layout(int n_pad, int max_smem, TcLayout& out, uint32_t& smem_bytes) {
-    static const int order_small[4][2] = {{3, 3}, {2, 3}, {3, 2}, {2, 2}};
-    static const int order_large[4][2] = {{3, 3}, {3, 2}, {2, 3}, {2, 2}};
-    const int(*order)[2] = n_pad <= 64 ? order_small : order_large;
-    for (int i = 0; i < 4; ++i) {
+    static const int order[6][2] = {{4, 8}, {4, 6}, {4, 4}, {3, 4}, {3, 3}, {2, 3}};
+    for (int i = 0; i < 6; ++i) {
         const TcLayout L = tc_layout(n_pad, order[i][0], order[i][1]);
         const uint32_t need = L.total + 1024u;
         if ((int)need <= max_smem) {
@@ -549,9 +582,14 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     prm.nb = nb;
     prm.n_pad = n_pad;
     prm.n_units = (int32_t)((out_dim + kTcUnitRows - 1) / kTcUnitRows);
-    prm.acc_bufs = 2 * kTcUm * n_pad <= 512 ? 2 : 1;
+    // TMEM (512 columns): accumulators [acc_bufs][kTcUm][n_pad], then the A stages
+    // [kTcAStages][kTcUm][32]
+    const int a_cols = kTcAStages * kTcUm * kTcACols;
+    prm.acc_bufs = 2 * kTcUm * n_pad + a_cols <= 512 ? 2 : 1;
+    if (prm.acc_bufs * kTcUm * n_pad + a_cols > 512) return Q4A_ERR_UNSUPPORTED;
+    prm.a_col0 = (uint32_t)(prm.acc_bufs * kTcUm * n_pad);
     uint32_t cols = 32;
-    while (cols < (uint32_t)(prm.acc_bufs * kTcUm * n_pad)) cols *= 2;
+    while (cols < prm.a_col0 + (uint32_t)a_cols) cols *= 2;
     prm.tmem_cols = cols;
     prm.idesc = (1u << 4)                          // D: fp32
                 | (0u << 7) | (0u << 10)           // A, B: fp16
@@ -570,9 +608,9 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     cfg.numAttrs = 1;
     static const bool debug = getenv("Q4A_DEBUG") != nullptr;
     if (debug)
-        fprintf(stderr, "q4a dense_tc: out=%lld in=%lld nb=%d n_pad=%d units=%d grid=%u cs=%d os=%d acc_bufs=%d "
+        fprintf(stderr, "q4a dense_tc: out=%lld in=%lld nb=%d n_pad=%d units=%d grid=%u cs=%d xs=%d acc_bufs=%d "
                 "tmem_cols=%u smem=%u\n", (long long)out_dim, (long long)in_dim, nb, n_pad, prm.n_units,
-                cfg.gridDim.x, prm.lay.cs, prm.lay.os, prm.acc_bufs, prm.tmem_cols, smem_bytes);
+                cfg.gridDim.x, prm.lay.cs, prm.lay.xs, prm.acc_bufs, prm.tmem_cols, smem_bytes);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, dense_tc_kernel, prm);
     if (e != cudaSuccess) return cuda_fail(e);
     return Q4A_OK;

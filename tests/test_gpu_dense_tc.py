@@ -1,4 +1,4 @@
-"""GPU parity of the wide-batch dense path of q4a_gemv (NB >= 64: binary16 weight tiles,
+"""GPU parity of the wide-batch dense path of q4a_gemv (NB >= 64: binary16 weights in TMEM,
 tcgen05.mma with TMEM accumulators) against the CPU oracle, through the C ABI.
 
 Bar: every element within the oracle's bound |y - y_ref| <= 2e-3 * sum_i |w_oi x_ri| + 1e-5,
@@ -65,8 +65,8 @@ TC_CASES = [
     (129, 512, 100),     # second tile holds one row
     (513, 1024, 128),    # three units, N 128
     (1000, 4096, 80),    # long K (64 groups, 16 code stages)
-    (256, 1024, 256),    # N 256: one accumulator set
-    (70, 512, 300),      # two launches: 256 rows, then 44
+    (256, 1024, 256),    # two launches of 128 activation rows
+    (70, 512, 300),      # three launches: 128, 128, then 44 rows
     (40000, 512, 64),    # 157 units: CTAs take a second unit
 ]
 
