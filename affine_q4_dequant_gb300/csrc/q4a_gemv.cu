@@ -14,8 +14,9 @@
 //    K-slice of the activations once, as ready-made mma B fragments plus fp32
 //    group sums, and reuses them for all of its rows. Partial sums meet through
 //    distributed shared memory; the reduction order is fixed (deterministic).
-//  * Consumer warp (wr, wg) takes group slots {wg, wg+4} of every 8-group stage
-//    for the tiles of row half wr. Per 16-row tile and group it runs 4 steps of
+//  * Consumer warp wg takes group wg of every 8-group stage, for every 16-row tile
+//    of the row block (several independent tiles per warp hide the mma and
+//    shared-memory latencies). Per 16-row tile and group it runs 4 steps of
 //    mma.sync m16n8k16 (f16 in, f32 accumulate) per 8 activation rows: the A
 //    operand is the raw codes, pulled out of each 32-bit word by masks into
 //    binary16 subnormals (code * 2^-24, exact); the high nibble of a byte lands
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> p) {
     constexpr int NTOK = NT * 8;
     constexpr int MT = tiles_per_block(NT);  // tiles per row block
-    constexpr int TPW = MT / 2;              // tiles per consumer warp (row half)
+    constexpr int TPW = MT;                  // tiles per consumer warp: all of the row block
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -539,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ======================= consumer warps =======================
         const int ctid = threadIdx.x;       // 0 .. 32 * kConsumerWarps - 1
-        const int wr = warp / kGroupSlots;  // row half
-        const int wg = warp % kGroupSlots;  // group slot = group index within each stage
+        const int wg = warp;                // group slot = group index within each stage
         const int g = lane >> 2;
         const int tq = lane & 3;
         grid_dep_wait();   // activations, the row map and y may belong to the previous kernel
@@ -572,13 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lrow = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
         const uint32_t lgran = (uint32_t)(wg & 3) * 2 + (uint32_t)(lane >> 4);
         const uint32_t ldsm_base = smem_addr(ring) + lrow * 128 + ((lgran ^ (lrow & 7)) << 4) +
-                                   (uint32_t)(((wg >> 2) * MT + wr * TPW) * kTileBytes);
+                                   (uint32_t)(((wg >> 2) * MT) * kTileBytes);
         // B fragments of group gl, row tok: xfrag + ((gl*2 + jp)*ntok_max + tok)*64 + tq*16
         const uint32_t xf_jp = (uint32_t)p.ntok_max * 64u;
         const uint32_t xf_base = smem_addr(xfrag) + (uint32_t)wg * 2u * xf_jp + (uint32_t)g * 64u + (uint32_t)tq * 16u;
         const uint32_t xf_stage = (uint32_t)kStageGroups * 2u * xf_jp;
         // scales: [chunk][row][128 B]; this lane's rows g (and g+8) of the warp's first tile
-        const uint32_t s_lane = (uint32_t)(g * 128 + wr * TPW * kTileBytes) + 2u * (uint32_t)wg;
+        const uint32_t s_lane = (uint32_t)(g * 128) + 2u * (uint32_t)wg;
         int staged_seg = -1;
         int rs = 0;            // ring slot and its phase
         uint32_t rph = 0;
@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // groups 16gb..16gb+15 = granules 2*(gb&3), +1 of 64-group chunk gb>>2
                     const uint32_t gran = (uint32_t)(gb & 3) * 2 + (uint32_t)(lane >> 4);
                     const uint32_t boff = smem_addr(sbb) + (uint32_t)((gb >> 2) * MT * kTileBytes) + lrow * 128 +
-                                          ((gran ^ (lrow & 7)) << 4) + (uint32_t)(wr * TPW * kTileBytes);
+                                          ((gran ^ (lrow & 7)) << 4);
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
                         uint32_t a0, a1, a2, a3;
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int R = j.ntile * 16;
 #pragma unroll
             for (int mi = 0; mi < TPW; ++mi) {
-                const int m = wr * TPW + mi;
+                const int m = mi;
                 if (m >= j.ntile) continue;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {

@@ -15,8 +15,8 @@ constexpr int kStageGroups = 8;         // groups per pipeline stage (512 inputs
 constexpr int kBoxBytes = 128;          // TMA box width in bytes (4 groups), 128B swizzle
 constexpr int kTileBytes = 16 * kBoxBytes;      // one 16-row tile of one box column: 2 KB
 constexpr int kNumMaps = 4;                     // box heights 16, 32, 64, 128 rows
-constexpr int kGroupSlots = kStageGroups; // consumer warps per row half: one stage group each
-constexpr int kConsumerWarps = 2 * kGroupSlots;   // 2 row halves x 8 group slots
+constexpr int kGroupSlots = kStageGroups; // one consumer warp per group of a stage
+constexpr int kConsumerWarps = kGroupSlots;       // each owns every tile of the row block
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDenseMaxSeg = 8;         // token chunks of one dense call
 constexpr int kXFragBudget = 64 * 1024; // staged activation fragments per CTA
@@ -54,9 +54,8 @@ struct SmemLayout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-// Row tiles (16 rows) per row block: each of the two row halves of consumer warps holds
-// mt/2 tiles of accumulators: 12-16 fp32 per lane at every NB (the 17 warps of a CTA
-// leave 96 registers per thread).
+// Row tiles (16 rows) per row block. Every consumer warp holds accumulators for all of
+// them: 4 * nt * mt fp32 per lane (24 / 32 / 32 at nt = 1 / 2 / 4).
 __host__ __device__ constexpr int tiles_per_block(int nt) { return nt == 1 ? 6 : (nt == 2 ? 4 : 2); }
 
 // Staged activation fragments: [group][step pair][activation row][lane quad] x 16 bytes,
