@@ -27,8 +27,9 @@
 //   warp 0       TMA producer of the packed codes (128 bytes x 128 rows per box, 4 groups)
 //                into a code ring; it waits only for that ring.
 //   warp 1       allocates TMEM; one thread issues the MMAs: per group, per tile,
-//                4 x (M 128, N NB, K 16) with A from TMEM; commits free the A stage and the
-//                x stage, and signal the accumulator after a unit's last group.
+//                4 x (M 128, N NB, K 16) with A from TMEM; a stage holds two groups, so one
+//                barrier handshake covers 16 MMAs; commits free the A stage and the x stage,
+//                and signal the accumulator after a unit's last group.
 //   warps 2..5   epilogue, one TMEM lane quarter each: exponents of the next unit's rows
 //                (ahead of time), then tcgen05.ld of the accumulators, * 2^e, y stores.
 //   warps 6..13  dequantisation, one weight row per thread (warp w owns TMEM lane quarter
@@ -57,7 +58,8 @@ constexpr int kTcUnitRows = kTcM * kTcUm;   // 256
 constexpr int kTcChunkGroups = 4;           // groups per code stage: 128 bytes of each row
 constexpr int kTcTileBytes = kTcM * 128;    // one 128-row tile of 128-byte rows: 16 KB
 constexpr int kTcACols = 32;                // TMEM columns of one tile's group: 64 fp16
-constexpr int kTcAStages = 4;               // A stages in TMEM
+constexpr int kTcSG = 2;                    // groups per operand stage (one handshake per 128 inputs)
+constexpr int kTcAStages = 2;               // A stages in TMEM: [stage][tile][group][32 columns]
 constexpr int kTcWarpProducer = 0;
 constexpr int kTcWarpMma = 1;
 constexpr int kTcWarpEpi0 = 2;
@@ -74,7 +76,7 @@ static_assert(kTcDqWarps == 4 * kTcUm, "one dequantisation warp per TMEM lane qu
 struct TcLayout {
     uint32_t code;        // code ring: cs stages of kTcUm tiles
     uint32_t code_stage;
-    uint32_t xr;          // x ring: xs stages of [n_pad rows][128 bytes]
+    uint32_t xr;          // x ring: xs stages of [kTcSG groups][n_pad rows][128 bytes]
     uint32_t x_stage;
     uint32_t exps;        // [2][kTcUnitRows] fp32 2^-e of the rows of the next two units
     uint32_t bars;
@@ -91,7 +93,7 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
     L.code = 0;
     L.code_stage = (uint32_t)kTcUm * kTcTileBytes;
     L.xr = L.code + (uint32_t)cs * L.code_stage;
-    L.x_stage = (uint32_t)n_pad * 128u;                     // n_pad % 16 == 0: 2 KB multiples
+    L.x_stage = (uint32_t)kTcSG * n_pad * 128u;             // n_pad % 16 == 0: 2 KB multiples
     L.exps = L.xr + (uint32_t)xs * L.x_stage;
     L.bars = L.exps + 2u * kTcUnitRows * 4u;
     // code_full[cs] code_empty[cs] x_full[xs] x_empty[xs] a_full[A] a_empty[A]
@@ -334,12 +336,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             grid_dep_wait();   // x may be written by the previous kernel of the stream
             int xi = 0;
             for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
-                for (int g = 0; g < G; ++g, ++xi) {
+                for (int g = 0; g < G; g += kTcSG, ++xi) {
                     const int sx = xi % XS;
                     if (xi >= XS) mbar_wait(smem_addr(x_empty + sx), (uint32_t)(xi / XS - 1) & 1u, abort_flag);
                     const uint32_t xf = smem_addr(x_full + sx);
                     mbar_arrive_expect_tx(xf, L.x_stage);
-                    tma_load_2d(smem_addr(smem + L.xr + sx * L.x_stage), &p.tmap_x, g * 64, 0, xf);
+                    for (int gi = 0; gi < kTcSG; ++gi)
+                        tma_load_2d(smem_addr(smem + L.xr + sx * L.x_stage + gi * p.n_pad * 128), &p.tmap_x,
+                                    (g + gi) * 64, 0, xf);
                 }
             }
         }
@@ -354,19 +358,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     mbar_wait(smem_addr(acc_empty + buf), (uint32_t)(li / p.acc_bufs - 1) & 1u, abort_flag);
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)(buf * kTcUm * p.n_pad);
-                for (int g = 0; g < G; ++g, ++gi) {
+                for (int g = 0; g < G; g += kTcSG, ++gi) {
                     const int sx = gi % XS, sa = gi % AS;
                     mbar_wait(smem_addr(x_full + sx), (uint32_t)(gi / XS) & 1u, abort_flag);
                     mbar_wait(smem_addr(a_full + sa), (uint32_t)(gi / AS) & 1u, abort_flag);
                     tc_fence_after();
-                    const uint64_t bd = smem_desc(smem_addr(smem + L.xr + sx * L.x_stage));
-                    const uint32_t a0 = tmem + p.a_col0 + (uint32_t)(sa * kTcUm * kTcACols);
+                    const uint32_t xs0 = smem_addr(smem + L.xr + sx * L.x_stage);
+                    const uint32_t a0 = tmem + p.a_col0 + (uint32_t)(sa * kTcUm * kTcSG * kTcACols);
 #pragma unroll
-                    for (int u = 0; u < kTcUm; ++u)
+                    for (int gg = 0; gg < kTcSG; ++gg) {
+                        const uint64_t bd = smem_desc(xs0 + (uint32_t)(gg * p.n_pad * 128));
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)   // K 16 per MMA: 8 TMEM columns of A, 32 bytes of x
-                            tc_mma_ts(d0 + (uint32_t)(u * p.n_pad), a0 + (uint32_t)(u * kTcACols + 8 * k),
-                                      bd + 2u * k, p.idesc, (uint32_t)(g | k));
+                        for (int u = 0; u < kTcUm; ++u)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)   // K 16 per MMA: 8 TMEM columns of A, 32 bytes of x
+                                tc_mma_ts(d0 + (uint32_t)(u * p.n_pad),
+                                          a0 + (uint32_t)((u * kTcSG + gg) * kTcACols + 8 * k), bd + 2u * k, p.idesc,
+                                          (uint32_t)(g + gg + k));
+                    }
                     tc_commit(smem_addr(x_empty + sx));
                     tc_commit(smem_addr(a_empty + sa));
                 }
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
         const int r = u * kTcM + rl;                      // row within the unit
         const uint32_t rsw = (uint32_t)rl & 7u;
         const uint32_t code_base = smem_addr(smem + L.code) + (uint32_t)(u * kTcTileBytes) + (uint32_t)rl * 128u;
-        const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 + (uint32_t)(u * kTcACols);
+        const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 + (uint32_t)(u * kTcSG * kTcACols);
         int ci = 0, gi = 0, li = 0;
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             const int slot = li & 1;
@@ -461,8 +470,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                 mbar_wait(smem_addr(code_full + cs_), (uint32_t)(ci / CS) & 1u, abort_flag);
                 const uint32_t cb = code_base + (uint32_t)cs_ * L.code_stage;
                 const int ng = min(kTcChunkGroups, G - c * kTcChunkGroups);
-                for (int k = 0; k < ng; ++k, ++gi) {
+                for (int k = 0; k < ng; ++k) {
                     const int sa = gi % AS;
+                    const int gg = k % kTcSG;           // group within the operand stage
                     const uint32_t sp = k < 2 ? s_cur.x : s_cur.y;
                     const uint32_t bp = k < 2 ? b_cur.x : b_cur.y;
                     const float sf = bf16_to_f32((k & 1) ? (sp >> 16) : (sp & 0xFFFFu)) * dq;
@@ -480,12 +490,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                         h[4 * w8 + 2] = dequant_pair<2>(words[w8], sc, bi);
                         h[4 * w8 + 3] = dequant_pair<3>(words[w8], sc, bi);
                     }
-                    if (gi >= AS) mbar_wait(smem_addr(a_empty + sa), (uint32_t)(gi / AS - 1) & 1u, abort_flag);
-                    tc_fence_after();
-                    tc_st32(a_lane + (uint32_t)(sa * kTcUm * kTcACols), h);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_addr(a_full + sa));
+                    if (gg == 0) {
+                        if (gi >= AS) mbar_wait(smem_addr(a_empty + sa), (uint32_t)(gi / AS - 1) & 1u, abort_flag);
+                        tc_fence_after();
+                    }
+                    tc_st32(a_lane + (uint32_t)((sa * kTcUm * kTcSG + gg) * kTcACols), h);
+                    if (gg == kTcSG - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_addr(a_full + sa));
+                        ++gi;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(code_empty + cs_));
@@ -583,8 +598,8 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     prm.n_pad = n_pad;
     prm.n_units = (int32_t)((out_dim + kTcUnitRows - 1) / kTcUnitRows);
     // TMEM (512 columns): accumulators [acc_bufs][kTcUm][n_pad], then the A stages
-    // [kTcAStages][kTcUm][32]
-    const int a_cols = kTcAStages * kTcUm * kTcACols;
+    // [kTcAStages][kTcUm][kTcSG][32]
+    const int a_cols = kTcAStages * kTcUm * kTcSG * kTcACols;
     prm.acc_bufs = 2 * kTcUm * n_pad + a_cols <= 512 ? 2 : 1;
     if (prm.acc_bufs * kTcUm * n_pad + a_cols > 512) return Q4A_ERR_UNSUPPORTED;
     prm.a_col0 = (uint32_t)(prm.acc_bufs * kTcUm * n_pad);
