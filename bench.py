@@ -53,6 +53,24 @@ def layer_bytes(nb):
     return gu, act, dn
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (every rank gets it); x itself outside a process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the bytes every rank moved in one step over the slowest rank's
+    step time (weak scaling: each rank runs the same workload on its own GPU)."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -329,13 +347,8 @@ def run_ours(args, rank, world, local_rank):
         gemv_ms_total += gu_ms + dn_ms
         step_bytes += 2 * (gu_b + act_b + dn_b) * L     # the layer chain + the per-kind chains
     gemv_launches = 2 * n * len(nbs)
-    ms_per_step = elapsed_ms / args.steps
-    if dist is not None:
-        import torch.distributed as dist
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    ms_per_step = max_over_ranks(elapsed_ms / args.steps, dev if dist is not None else None)
+    value = whole_job_gbs(step_bytes, world, ms_per_step)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
