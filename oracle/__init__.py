@@ -57,6 +57,7 @@ def _load():
             "q4o_rmsnorm_f16": (None, [P, P, P, P, D, D, I, I]),
             "q4o_silu_mul_f16": (None, [P, P, I, I]),
             "q4o_route_topk": (None, [P, P, P, I, I, I]),
+            "q4o_moe_combine": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -203,3 +204,28 @@ def route_topk(logits, top_k: int):
     wts = np.empty((n_tok, top_k), np.float64)
     _load().q4o_route_topk(_p(idx), _p(wts), _p(logits), n_tok, n_exp, top_k)
     return idx, wts
+
+
+def moe_combine(y, slot, w, y_shared=None, gate=None, x=None):
+    """Routing-weighted sum of the expert outputs of each token, plus the gated shared
+    expert output. y: float32 [n_slots][hidden]; slot: int32 [n_tok][k]; w: float32
+    [n_tok][k]; y_shared: float32 [n_tok][hidden] or None; gate: bf16 bits [hidden];
+    x: float32 [n_tok][hidden]. Returns (out float64, abs-sum float64 [n_tok][hidden],
+    gate-dot abs-sum float64 [n_tok])."""
+    y = _c(y, np.float32)
+    slot = _c(slot, np.int32)
+    w = _c(w, np.float32)
+    n_slots, hidden = y.shape
+    n_tok, k = slot.shape
+    out = np.empty((n_tok, hidden), np.float64)
+    bound = np.empty((n_tok, hidden), np.float64)
+    gabs = np.empty((n_tok,), np.float64)
+    if y_shared is not None:
+        y_shared = _c(y_shared, np.float32)
+        gate = _c(gate, np.uint16)
+        x = _c(x, np.float32)
+    _load().q4o_moe_combine(_p(out), _p(bound), _p(gabs), _p(y), _p(slot), _p(w),
+                            _p(y_shared) if y_shared is not None else None,
+                            _p(gate) if y_shared is not None else None,
+                            _p(x) if y_shared is not None else None, n_tok, k, n_slots, hidden)
+    return out, bound, gabs

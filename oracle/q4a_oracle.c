@@ -392,3 +392,55 @@ Q4O_EXPORT void q4o_route_topk(int32_t* idx, double* wts, const float* logits,
     free(taken);
     free(p);
 }
+
+/* ---- MoE combine ---------------------------------------------------------- */
+
+/* [BATCH_MSL] experts.metal, fn_moe_combine_b (part 0 and part 1) and
+ * fn_shared_add_rows: the output row of token t is the routing-weighted sum of
+ * the expert outputs of its slots, plus, when a shared expert is present, its
+ * output scaled by sigmoid(gate_vec . x[t]):
+ *     out[t][i] = sum_k w[t][k] * y[slot[t][k]][i]
+ *               + sigmoid(sum_j gate[j] * x[t][j]) * y_shared[t][i].
+ * Double precision, k in order. bound[t][i] = sum_k |w y| + |g y_shared| and
+ * gabs[t] = sum_j |gate[j] x[t][j]| feed the tests' tolerance. A slot id
+ * outside [0, n_slots) makes the row NaN (the library's convention). */
+Q4O_EXPORT void q4o_moe_combine(double* out, double* bound, double* gabs, const float* y,
+                                const int32_t* slot, const float* w, const float* y_shared,
+                                const uint16_t* gate, const float* x, int64_t n_tok,
+                                int64_t top_k, int64_t n_slots, int64_t hidden)
+{
+    for (int64_t t = 0; t < n_tok; t++) {
+        double g = 0.0, ga = 0.0;
+        if (y_shared) {
+            double dot = 0.0;
+            for (int64_t j = 0; j < hidden; j++) {
+                const double term = bf16_value(gate[j]) * (double)x[t * hidden + j];
+                dot += term;
+                ga += fabs(term);
+            }
+            g = 1.0 / (1.0 + exp(-dot));
+        }
+        gabs[t] = ga;
+        int bad = 0;
+        for (int64_t k = 0; k < top_k; k++)
+            if (slot[t * top_k + k] < 0 || slot[t * top_k + k] >= n_slots)
+                bad = 1;
+        for (int64_t i = 0; i < hidden; i++) {
+            double acc = 0.0, a = 0.0;
+            if (!bad)
+                for (int64_t k = 0; k < top_k; k++) {
+                    const double term = (double)w[t * top_k + k] *
+                                        (double)y[(int64_t)slot[t * top_k + k] * hidden + i];
+                    acc += term;
+                    a += fabs(term);
+                }
+            if (y_shared) {
+                const double term = g * (double)y_shared[t * hidden + i];
+                acc += term;
+                a += fabs(term);
+            }
+            out[t * hidden + i] = bad ? NAN : acc;
+            bound[t * hidden + i] = a;
+        }
+    }
+}

@@ -351,3 +351,74 @@ def test_experts_permutation_and_invalid_id():
     y4, _ = oracle.gemv_experts(p, s, b, x, None, np.array([7, 0], np.int32),
                                 np.array([0, 1, 4], np.int32), 4, 6)
     assert np.isnan(y4[0]).all() and np.isfinite(y4[1:]).all()
+
+
+# ---- MoE combine ("BATCH_MSL" page, experts.metal fn_moe_combine_b / fn_shared_add_rows) ----
+
+def test_moe_combine_hand_worked(golden):
+    g = golden("moe_combine_2x2.txt")
+    y = np.array([[float(v) for v in g[f"y{i}"]] for i in range(3)], np.float32)
+    slot = np.array([[int(v) for v in g[f"slot{t}"]] for t in range(2)], np.int32)
+    w = np.array([[float(v) for v in g[f"w{t}"]] for t in range(2)], np.float32)
+    out, bound, _ = oracle.moe_combine(y, slot, w)
+    want = np.array([[float(v) for v in g[f"out{t}"]] for t in range(2)])
+    assert np.array_equal(out, want)
+    assert np.array_equal(bound, want)      # all terms positive
+
+
+def test_moe_combine_identity_routing():
+    rng = np.random.default_rng(21)
+    y = rng.normal(size=(7, 33)).astype(np.float32)
+    perm = rng.permutation(7).astype(np.int32)
+    out, _, _ = oracle.moe_combine(y, perm[:, None], np.ones((7, 1), np.float32))
+    assert np.array_equal(out, y[perm].astype(np.float64))
+
+
+def test_moe_combine_shared_gate_at_zero_is_half():
+    """gate = 0 -> sigmoid(0) = 1/2 exactly."""
+    rng = np.random.default_rng(22)
+    y = rng.integers(-8, 8, size=(4, 16)).astype(np.float32)
+    ysh = rng.integers(-8, 8, size=(2, 16)).astype(np.float32)
+    slot = np.array([[0, 3], [2, 1]], np.int32)
+    w = np.array([[0.5, 0.5], [0.25, 0.75]], np.float32)
+    x = rng.normal(size=(2, 16)).astype(np.float32)
+    out, _, gabs = oracle.moe_combine(y, slot, w, ysh, np.zeros(16, np.uint16), x)
+    plain, _, _ = oracle.moe_combine(y, slot, w)
+    assert np.array_equal(out, plain + 0.5 * ysh)
+    assert np.all(gabs == 0.0)
+
+
+def test_moe_combine_sigmoid_symmetry():
+    """sigmoid(-d) = 1 - sigmoid(d): the shared parts for gate and -gate add up to y_shared."""
+    rng = np.random.default_rng(23)
+    y = rng.normal(size=(5, 24)).astype(np.float32)
+    ysh = rng.normal(size=(3, 24)).astype(np.float32)
+    slot = rng.integers(0, 5, size=(3, 2)).astype(np.int32)
+    w = rng.random((3, 2)).astype(np.float32)
+    x = rng.normal(size=(3, 24)).astype(np.float32)
+    gate = wl.f32_to_bf16_bits(rng.normal(0, 0.2, 24).astype(np.float32))
+    plain, _, _ = oracle.moe_combine(y, slot, w)
+    a, _, _ = oracle.moe_combine(y, slot, w, ysh, gate, x)
+    b, _, _ = oracle.moe_combine(y, slot, w, ysh, gate ^ np.uint16(0x8000), x)
+    assert np.allclose((a - plain) + (b - plain), ysh, rtol=0, atol=1e-12)
+
+
+def test_moe_combine_saturated_gate_and_linearity():
+    rng = np.random.default_rng(24)
+    y = rng.normal(size=(6, 8)).astype(np.float32)
+    ysh = rng.normal(size=(2, 8)).astype(np.float32)
+    slot = np.array([[0, 5, 2], [4, 4, 1]], np.int32)
+    w = rng.random((2, 3)).astype(np.float32)
+    x = np.full((2, 8), 8.0, np.float32)
+    gate = wl.f32_to_bf16_bits(np.full(8, 1.0, np.float32))     # dot = 64: sigmoid = 1 - 1.6e-28
+    plain, _, _ = oracle.moe_combine(y, slot, w)
+    out, _, gabs = oracle.moe_combine(y, slot, w, ysh, gate, x)
+    assert np.allclose(out - plain, ysh, rtol=0, atol=1e-15) and np.all(gabs == 64.0)
+    out2, _, _ = oracle.moe_combine(y, slot, 2 * w)               # exact: doubling a float32
+    assert np.array_equal(out2, 2 * plain)
+
+
+def test_moe_combine_invalid_slot_gives_nan_row():
+    y = np.ones((3, 4), np.float32)
+    out, _, _ = oracle.moe_combine(y, np.array([[0, 3], [1, 2]], np.int32), np.ones((2, 2), np.float32))
+    assert np.isnan(out[0]).all() and np.array_equal(out[1], np.full(4, 2.0))
