@@ -26,7 +26,7 @@ from . import _build
 
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_experts", "gemv_rmsnorm",
-    "silu_mul_xsum", "check_device_error", "STATUS", "MAX_SEGMENTS",
+    "silu_mul_xsum", "moe_combine", "check_device_error", "STATUS", "MAX_SEGMENTS",
 ]
 
 MAX_SEGMENTS = 512
@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_silu_mul_xsum": (I32, [P, P, P, I64, I64, P]),
+        "q4a_moe_combine": (I32, [P, P, P, P, I32, I32, I64, I64, P, P, P, P]),
         "q4a_check_device_error": (I32, [P]),
     }
     for name, (res, args) in sigs.items():
@@ -177,6 +178,26 @@ def silu_mul_xsum(gate_up: torch.Tensor, h: torch.Tensor | None = None,
     _check("q4a_silu_mul_xsum", _lib.q4a_silu_mul_xsum(
         _dev(h, "h", _F16), hp, _dev(gate_up, "gate_up", _F32), rows, inter, _stream(stream)))
     return h, hsum
+
+
+def moe_combine(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, y_shared: torch.Tensor | None = None,
+                gate: torch.Tensor | None = None, x: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[t] = sum_k w[t][k] * y[slot[t][k]] (+ sigmoid(gate . x[t]) * y_shared[t]).
+    y fp32 [n_slots][hidden]; slot int32 [n_tok][k]; w fp32 [n_tok][k]; y_shared fp32
+    [n_tok][hidden] or None; gate bf16 [hidden]; x fp32 [n_tok][hidden]."""
+    n_slots, hidden = y.shape
+    n_tok, top_k = slot.shape
+    if out is None:
+        out = torch.empty((n_tok, hidden), dtype=torch.float32, device=y.device)
+    null = ctypes.c_void_p(0)
+    _check("q4a_moe_combine", _lib.q4a_moe_combine(
+        _dev(out, "out", _F32), _dev(y, "y", _F32), _dev(slot, "slot", _I32), _dev(w, "w", _F32),
+        int(n_tok), int(top_k), int(n_slots), int(hidden),
+        null if y_shared is None else _dev(y_shared, "y_shared", _F32),
+        null if y_shared is None else _dev(gate, "gate", _BF16),
+        null if y_shared is None else _dev(x, "x", _F32), _stream(stream)))
+    return out
 
 
 def check_device_error(stream=None) -> None:

@@ -203,6 +203,21 @@ q4a_status q4a_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int
     return launch_silu_mul_xsum(h, hsum, gate_up, rows, inter, (cudaStream_t)stream);
 }
 
+q4a_status q4a_moe_combine(float* out, const float* y, const int32_t* slot, const float* w, int n_tok,
+                           int top_k, int64_t n_slots, int64_t hidden, const float* y_shared,
+                           const uint16_t* gate, const float* x, q4a_stream_t stream) {
+    if (!out || !y || !slot || !w) return Q4A_ERR_NULL;
+    if (y_shared && (!gate || !x)) return Q4A_ERR_NULL;
+    if (n_tok < 1 || top_k < 1 || n_slots < 1 || hidden < 4 || hidden % 4 != 0) return Q4A_ERR_SHAPE;
+    if (top_k > kCombineMaxK || n_slots > ((int64_t)1 << 31) - 1) return Q4A_ERR_UNSUPPORTED;
+    if ((int64_t)n_tok * ((hidden + 1023) / 1024) > ((int64_t)1 << 31) - 1) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(out, 16) || !aligned(y, 16) || !aligned(slot, 4) || !aligned(w, 4) ||
+        (y_shared && (!aligned(y_shared, 16) || !aligned(x, 16) || !aligned(gate, 2))))
+        return Q4A_ERR_ALIGN;
+    return launch_moe_combine(out, y, slot, w, n_tok, top_k, n_slots, hidden, y_shared, y_shared ? gate : nullptr,
+                              y_shared ? x : nullptr, (cudaStream_t)stream);
+}
+
 q4a_status q4a_check_device_error(q4a_stream_t stream) {
     uint32_t word = 0;
     q4a_status st = read_and_clear_device_error((cudaStream_t)stream, &word);

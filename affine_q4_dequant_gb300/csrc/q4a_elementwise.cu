@@ -2,9 +2,10 @@
 //   q4a_pack           (A1) codes -> 4-bit rows
 //   q4a_xsum           (A2) per-64-group sums of fp16 activations
 //   q4a_silu_mul_xsum  (A7) h = fp16(silu(gate) * up) plus group sums of h
+//   q4a_moe_combine    routing-weighted sum of expert rows plus the gated shared expert
 //   a NaN fill for routed-expert segments with an out-of-range expert id.
-// All are grid-stride kernels over 16-byte vectors, sized to a multiple of the SM
-// count, with no shared memory and no waits.
+// The elementwise ones are grid-stride kernels over 16-byte vectors, sized to a multiple
+// of the SM count, with no shared memory and no waits.
 #include <cuda_fp16.h>
 
 #include "q4a_internal.h"
@@ -124,6 +125,79 @@ __global__ void fill_nan_kernel(float* __restrict__ y, int64_t n) {
         y[i] = __int_as_float(0x7fc00000);
 }
 
+// Routed-expert combine ("BATCH_MSL" page, experts.metal fn_moe_combine_b and
+// fn_shared_add_rows):
+//     out[t][i] = sum_k w[t][k] * y[slot[t][k]][i]  (+ sigmoid(gate . x[t]) * y_shared[t][i]).
+// One CTA per (token, kCombineChunk outputs), 4 outputs per thread. The k terms are added
+// in k order and the gate dot reduces in a fixed tree, so the result is deterministic; like
+// the pages, every CTA of a token recomputes the gate dot. A slot outside [0, n_slots)
+// makes the token's row NaN.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineChunk = 4 * kCombineThreads;
+
+__global__ void __launch_bounds__(kCombineThreads)
+    moe_combine_kernel(float* __restrict__ out, const float* __restrict__ y, const int32_t* __restrict__ slot,
+                       const float* __restrict__ w, int top_k, int64_t n_slots, int64_t hidden, int nchunk,
+                       const float* __restrict__ y_shared, const uint16_t* __restrict__ gate,
+                       const float* __restrict__ x) {
+    __shared__ int32_t s_slot[kCombineMaxK];
+    __shared__ float s_w[kCombineMaxK];
+    __shared__ float s_red[kCombineThreads / 32];
+    __shared__ int s_bad;
+    grid_dep_wait();
+    const int64_t t = blockIdx.x / nchunk;
+    const int c = (int)(blockIdx.x % nchunk);
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    if ((int)threadIdx.x < top_k) {
+        const int32_t sl = slot[t * top_k + threadIdx.x];
+        s_slot[threadIdx.x] = sl;
+        s_w[threadIdx.x] = w[t * top_k + threadIdx.x];
+        if (sl < 0 || (int64_t)sl >= n_slots) atomicOr(&s_bad, 1);
+    }
+    if (y_shared) {
+        const float* xr = x + t * hidden;
+        float part = 0.f;
+        for (int64_t j = threadIdx.x; j < hidden; j += kCombineThreads)
+            part = fmaf(__uint_as_float((uint32_t)gate[j] << 16), xr[j], part);
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
+    }
+    __syncthreads();
+    float g = 0.f;
+    if (y_shared) {
+        float dot = 0.f;
+        for (int i = 0; i < kCombineThreads / 32; ++i) dot += s_red[i];
+        g = 1.f / (1.f + expf(-dot));
+    }
+    const int64_t i0 = (int64_t)c * kCombineChunk + 4 * (int64_t)threadIdx.x;
+    if (i0 < hidden) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s_bad) {
+            const float nan = __int_as_float(0x7fc00000);
+            acc = make_float4(nan, nan, nan, nan);
+        } else {
+            for (int k = 0; k < top_k; ++k) {
+                const float4 v = *reinterpret_cast<const float4*>(y + (int64_t)s_slot[k] * hidden + i0);
+                const float wk = s_w[k];
+                acc.x = fmaf(wk, v.x, acc.x);
+                acc.y = fmaf(wk, v.y, acc.y);
+                acc.z = fmaf(wk, v.z, acc.z);
+                acc.w = fmaf(wk, v.w, acc.w);
+            }
+            if (y_shared) {
+                const float4 v = *reinterpret_cast<const float4*>(y_shared + t * hidden + i0);
+                acc.x = fmaf(g, v.x, acc.x);
+                acc.y = fmaf(g, v.y, acc.y);
+                acc.z = fmaf(g, v.z, acc.z);
+                acc.w = fmaf(g, v.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4*>(out + t * hidden + i0) = acc;
+    }
+    grid_dep_launch();
+}
+
 template <typename... KArgs, typename... Args>
 q4a_status launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -171,6 +245,14 @@ q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, 
                                 int64_t inter, cudaStream_t stream) {
     const int64_t n = rows * inter / 8;
     return launch_pdl(silu_mul_kernel, grid_for(n, 256), 256, stream, h, hsum, gate_up, rows, inter);
+}
+
+q4a_status launch_moe_combine(float* out, const float* y, const int32_t* slot, const float* w, int n_tok,
+                              int top_k, int64_t n_slots, int64_t hidden, const float* y_shared,
+                              const uint16_t* gate, const float* x, cudaStream_t stream) {
+    const int nchunk = (int)((hidden + kCombineChunk - 1) / kCombineChunk);
+    return launch_pdl(moe_combine_kernel, n_tok * nchunk, kCombineThreads, stream, out, y, slot, w, top_k,
+                      n_slots, hidden, nchunk, y_shared, gate, x);
 }
 
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim, cudaStream_t stream) {

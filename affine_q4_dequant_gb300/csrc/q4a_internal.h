@@ -23,6 +23,7 @@ constexpr int kXFragBudget = 64 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path
+constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
 
 // How the producer fetches a row block's scales and biases into shared memory. Both modes
 // write the same layout: [64-group chunk][row][128 bytes], 16-byte granule u of row r
@@ -155,6 +156,9 @@ q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, 
                                 int64_t inter, cudaStream_t stream);
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim,
                            cudaStream_t stream);
+q4a_status launch_moe_combine(float* out, const float* y, const int32_t* slot, const float* w, int n_tok,
+                              int top_k, int64_t n_slots, int64_t hidden, const float* y_shared,
+                              const uint16_t* gate, const float* x, cudaStream_t stream);
 q4a_status read_and_clear_device_error(cudaStream_t stream, uint32_t* word);
 
 // Dense path for wide batches (q4a_dense_tc.cu): dequantise to binary16 tiles, tcgen05.mma.

@@ -505,7 +505,8 @@ def graph_us(torch, fn, n, trials=5):
 def run_moe_mode(args):
     """One routed MoE layer on the 64-expert bank (hidden 2048, inter 640, 16 tokens,
     top-8 by N(0,1) logits): q4a_gemv_experts on gate|up with the token map, the
-    SiLU*up activation, q4a_gemv_experts on down. Bank replicas total > 3 x L2."""
+    SiLU*up activation, q4a_gemv_experts on down, and q4a_moe_combine back to one row per
+    token (no shared expert in this workload). Bank replicas total > 3 x L2."""
     import torch
 
     import affine_q4_dequant_gb300 as q4a
@@ -531,6 +532,10 @@ def run_moe_mode(args):
     h = torch.empty(slots, I, dtype=torch.float16, device=dev)
     hs = torch.empty(slots, I // 64, device=dev)
     y_dn = torch.empty(slots, H, device=dev)
+    slot_np, w_np = wl.moe_combine_inputs(r)
+    c_slot = torch.from_numpy(slot_np).to(dev)
+    c_w = torch.from_numpy(w_np).to(dev)
+    out = torch.empty(T, H, device=dev)
 
     def gate_up(i):
         w, s_, b_ = banks[i % copies][0]
@@ -543,10 +548,14 @@ def run_moe_mode(args):
         w, s_, b_ = banks[i % copies][1]
         q4a.gemv_experts(w, s_, b_, h, None, r.expert_ids, r.token_offsets, E, H, out=y_dn)
 
+    def combine(i):
+        q4a.moe_combine(y_dn, c_slot, c_w, out=out)
+
     def layer(i):
         gate_up(i)
         act(i)
         down(i)
+        combine(i)
 
     for i in range(3):
         layer(i)
@@ -560,18 +569,20 @@ def run_moe_mode(args):
         return
     n = copies * max(1, args.reps // copies)
     us = {k: graph_us(torch, fn, n) for k, fn in (("gate_up", gate_up), ("act", act), ("down", down),
-                                                   ("layer", layer))}
+                                                   ("combine", combine), ("layer", layer))}
     q4a.check_device_error()
     gu_b = U * 2 * I * H * BYTES_PER_WEIGHT + T * H * 2 + slots * 2 * I * 4
     act_b = slots * 2 * I * 4 + slots * I * 2 + slots * (I // 64) * 4
     dn_b = U * H * I * BYTES_PER_WEIGHT + slots * I * 2 + slots * H * 4
+    cb_b = slots * H * 4 + T * H * 4 + slots * 8
     peak, kind = load_peaks()
     print(json.dumps({
         "kernel": "moe_layer", "experts": E, "union_experts": U, "slots": slots,
         "touched_weight_bytes": U * per_expert, "us_per_moe_layer": us["layer"],
         "gate_up_us": us["gate_up"], "gate_up_gbs": gu_b / us["gate_up"] / 1e3,
         "act_us": us["act"], "down_us": us["down"], "down_gbs": dn_b / us["down"] / 1e3,
-        "layer_gbs": (gu_b + act_b + dn_b) / us["layer"] / 1e3,
+        "combine_us": us["combine"], "combine_gbs": cb_b / us["combine"] / 1e3,
+        "layer_gbs": (gu_b + act_b + dn_b + cb_b) / us["layer"] / 1e3,
         "frac_of_peak_gate_up": gu_b / us["gate_up"] / 1e3 / peak,
         "frac_of_peak_down": dn_b / us["down"] / 1e3 / peak, "peak": peak, "peak_kind": kind,
         "launches_timed": n, "bank_copies": copies}), flush=True)

@@ -160,6 +160,31 @@ Q4A_API q4a_status q4a_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate
                              int64_t inter, q4a_stream_t stream);
 
 /*
+ * q4a_moe_combine -- the step after the routed-expert down projection: each token's
+ * output row is the routing-weighted sum of its experts' rows, plus the shared expert's
+ * row scaled by a sigmoid gate ("BATCH_MSL", experts.metal fn_moe_combine_b parts 0
+ * and 1, fn_scatter_add_rows, fn_shared_add_rows):
+ *     out[t][i] = sum_{k < top_k} w[t][k] * y[slot[t][k]][i]
+ *               + sigmoid( sum_j gate[j] * x[t][j] ) * y_shared[t][i]   (if y_shared)
+ *   out       out  fp32 [n_tok][hidden], fully overwritten
+ *   y         in   fp32 [n_slots][hidden] expert output rows (q4a_gemv_experts' y)
+ *   slot      in   int32 [n_tok][top_k] device array: row of y for token t's k-th expert
+ *   w         in   fp32 [n_tok][top_k] device array: routing weights
+ *   y_shared  in   fp32 [n_tok][hidden] shared-expert output, or NULL (no shared term;
+ *                  gate and x are then ignored)
+ *   gate      in   bf16 [hidden] shared-expert gate vector
+ *   x         in   fp32 [n_tok][hidden] the input the gate reads
+ *   The k terms are added in k order (deterministic). A slot outside [0, n_slots)
+ *   makes that token's row NaN (a loud failure, never an out-of-bounds read).
+ *   Requires n_tok >= 1, 1 <= top_k <= 64, hidden % 4 == 0; out, y, y_shared, x
+ *   16-byte aligned, slot and w 4-byte aligned, gate 2-byte aligned.
+ */
+Q4A_API q4a_status q4a_moe_combine(float* out, const float* y, const int32_t* slot, const float* w,
+                           int n_tok, int top_k, int64_t n_slots, int64_t hidden,
+                           const float* y_shared, const uint16_t* gate, const float* x,
+                           q4a_stream_t stream);
+
+/*
  * q4a_check_device_error -- synchronise `stream`, then report and clear the
  * device error word: Q4A_ERR_TIMEOUT if a kernel of this library gave up a
  * bounded wait since the last check (its outputs are then garbage),

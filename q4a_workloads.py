@@ -34,6 +34,7 @@ LM_HEAD = 4           # 4096 -> 151936, NB in {1, 8, 32, 64, 128}
 # Tensor identifiers (the tensor_id component of every seed).
 T_CODES, T_SCALE, T_BIAS, T_X, T_NORM_W, T_A, T_B, T_LOGITS = range(8)
 T_CODES_DOWN, T_SCALE_DOWN, T_BIAS_DOWN = 8, 9, 10
+T_COMBINE = 11
 
 
 def rng(config_id: int, tensor_id: int, seed: int = 0) -> np.random.Generator:
@@ -183,6 +184,21 @@ def dense_x(case: DenseCase, nb: int, seed: int = 0) -> np.ndarray:
 
 def moe_logits(seed: int = 0) -> np.ndarray:
     return normal_f32(MOE_BANK, T_LOGITS, (MOE_TOKENS, MOE_EXPERTS), seed=seed)
+
+
+def moe_combine_inputs(routing: Routing, seed: int = 0):
+    """For the combine step: slot[t][k] = the slot (row of the expert outputs) of token
+    t's k-th chosen expert, and routing weights w[t][k] > 0 summing to 1 per token
+    (uniform draws, normalised; the combine reads them as given)."""
+    n_tok, k = routing.chosen.shape
+    where = {}
+    for a, e in enumerate(routing.expert_ids):
+        for s_ in range(int(routing.token_offsets[a]), int(routing.token_offsets[a + 1])):
+            where[(int(e), int(routing.x_rows[s_]))] = s_
+    slot = np.array([[where[(int(e), t)] for e in routing.chosen[t]] for t in range(n_tok)], np.int32)
+    u = rng(MOE_BANK, T_COMBINE, seed).random((n_tok, k)) + 0.05
+    w = (u / u.sum(axis=1, keepdims=True)).astype(np.float32)
+    return slot, w
 
 
 def moe_banks(seed: int = 0, n_experts: int = MOE_EXPERTS):

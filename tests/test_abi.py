@@ -34,6 +34,7 @@ def lib():
     lib.q4a_gemv_experts.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]
     lib.q4a_gemv_rmsnorm.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
     lib.q4a_silu_mul_xsum.argtypes = [P, P, P, I64, I64, P]
+    lib.q4a_moe_combine.argtypes = [P, P, P, P, I32, I32, I64, I64, P, P, P, P]
     return lib
 
 
@@ -132,3 +133,18 @@ def test_silu_rejections(lib):
     assert s(A, A, A, 0, 64, None) == SHAPE
     assert s(A + 2, A, A, 1, 64, None) == ALIGN
     assert s(A, A + 2, A, 1, 64, None) == ALIGN
+
+
+def test_moe_combine_rejections(lib):
+    A = 0x1000    # a 16-byte aligned stand-in address; nothing is dereferenced on rejection
+    f = lib.q4a_moe_combine
+    assert f(None, A, A, A, 2, 8, 16, 2048, None, None, None, None) == NULL
+    assert f(A, A, A, A, 2, 8, 16, 2048, A, None, A, None) == NULL          # shared term without gate
+    assert f(A, A, A, A, 0, 8, 16, 2048, None, None, None, None) == SHAPE
+    assert f(A, A, A, A, 2, 0, 16, 2048, None, None, None, None) == SHAPE
+    assert f(A, A, A, A, 2, 8, 16, 2050, None, None, None, None) == SHAPE   # hidden % 4
+    assert f(A, A, A, A, 2, 65, 16, 2048, None, None, None, None) == UNSUP  # top_k > 64
+    assert f(A + 4, A, A, A, 2, 8, 16, 2048, None, None, None, None) == ALIGN
+    assert f(A, A, A + 2, A, 2, 8, 16, 2048, None, None, None, None) == ALIGN
+    assert f(A, A, A, A, 2, 8, 16, 2048, A + 8, A, A, None) == ALIGN        # y_shared
+
