@@ -58,6 +58,7 @@ def _load():
             "q4o_silu_mul_f16": (None, [P, P, I, I]),
             "q4o_route_topk": (None, [P, P, P, I, I, I]),
             "q4o_moe_combine": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
+            "q4o_gemv_silu": (None, [P, P, P, P, P, P, P, D, I, I, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -229,3 +230,18 @@ def moe_combine(y, slot, w, y_shared=None, gate=None, x=None):
                             _p(gate) if y_shared is not None else None,
                             _p(x) if y_shared is not None else None, n_tok, k, n_slots, hidden)
     return out, bound, gabs
+
+
+def gemv_silu(packed, s, b, x_bits, div: float):
+    """silu(y / div) of the plain product. Returns (out, y, bound) in float64; bound is the
+    product's acceptance bound (the epilogue's own tolerance follows from it)."""
+    packed, s, b, x_bits = (_c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16),
+                            _c(x_bits, np.uint16))
+    nb, in_dim = x_bits.shape
+    out_dim = packed.shape[0]
+    out = np.empty((nb, out_dim), np.float64)
+    y = np.empty((nb, out_dim), np.float64)
+    bound = np.empty((nb, out_dim), np.float64)
+    _load().q4o_gemv_silu(_p(out), _p(y), _p(bound), _p(packed), _p(s), _p(b), _p(x_bits), float(div),
+                          nb, out_dim, in_dim)
+    return out, y, bound

@@ -444,3 +444,20 @@ Q4O_EXPORT void q4o_moe_combine(double* out, double* bound, double* gabs, const 
         }
     }
 }
+
+/* ---- GEMV with a SiLU epilogue -------------------------------------------- */
+
+/* [BATCH_MSL] hyperconnection.metal, fn_qmv_silu_b: the Q4 matvec whose outputs go
+ * through silu(y / div) (the gated-residual bottleneck):
+ *     out[r][o] = v / (1 + e^-v),  v = y[r][o] / div,  y = the plain product above.
+ * Double precision; y and its acceptance bound come from q4o_gemv. */
+Q4O_EXPORT void q4o_gemv_silu(double* out, double* y, double* bound, const uint8_t* packed,
+                              const uint16_t* s, const uint16_t* b, const uint16_t* x, double div,
+                              int64_t nb, int64_t out_dim, int64_t in_dim)
+{
+    q4o_gemv(y, bound, packed, s, b, x, nb, out_dim, in_dim);
+    for (int64_t i = 0; i < nb * out_dim; i++) {
+        const double v = y[i] / div;
+        out[i] = v / (1.0 + exp(-v));
+    }
+}

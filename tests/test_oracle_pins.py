@@ -422,3 +422,41 @@ def test_moe_combine_invalid_slot_gives_nan_row():
     y = np.ones((3, 4), np.float32)
     out, _, _ = oracle.moe_combine(y, np.array([[0, 3], [1, 2]], np.int32), np.ones((2, 2), np.float32))
     assert np.isnan(out[0]).all() and np.array_equal(out[1], np.full(4, 2.0))
+
+
+# ---- GEMV with the SiLU epilogue ("BATCH_MSL" page, hyperconnection.metal fn_qmv_silu_b) ----
+
+def _silu_case(seed, out_dim=9, in_dim=128, nb=2):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(out_dim, in_dim), dtype=np.uint8)
+    s = wl.f32_to_bf16_bits(np.abs(rng.normal(0, 0.02, (out_dim, in_dim // 64))).astype(np.float32))
+    b = wl.f32_to_bf16_bits((-8 * rng.normal(0, 0.01, (out_dim, in_dim // 64))).astype(np.float32))
+    x = wl.f16_bits(rng.normal(0, 1, (nb, in_dim)))
+    return oracle.pack(codes), s, b, x
+
+
+def test_gemv_silu_zero_weights_give_zero():
+    """q = 0, b = 0 -> y = 0 -> silu(0) = 0 exactly."""
+    _, s, _, x = _silu_case(41)
+    packed = oracle.pack(np.zeros((9, 128), np.uint8))
+    out, y, _ = oracle.gemv_silu(packed, s, np.zeros_like(s), x, 3.0)
+    assert np.all(y == 0.0) and np.all(out == 0.0)
+
+
+def test_gemv_silu_odd_part_identity():
+    """silu(v) - silu(-v) = v: the outputs for div and -div differ by y / div."""
+    packed, s, b, x = _silu_case(42)
+    a, y, _ = oracle.gemv_silu(packed, s, b, x, 0.75)
+    c, _, _ = oracle.gemv_silu(packed, s, b, x, -0.75)
+    assert np.allclose(a - c, y / 0.75, rtol=1e-13, atol=1e-15)
+
+
+def test_gemv_silu_matches_the_plain_product_and_limits():
+    packed, s, b, x = _silu_case(43)
+    out, y, bound = oracle.gemv_silu(packed, s, b, x, 1.0)
+    y2, bound2 = oracle.gemv(packed, s, b, x)
+    assert np.array_equal(y, y2) and np.array_equal(bound, bound2)
+    big, _, _ = oracle.gemv_silu(packed, s, b, x, 1e-4)           # |v| large: silu -> max(v, 0)
+    v = y / 1e-4
+    pos = v > 50
+    assert np.allclose(big[pos], v[pos], rtol=1e-15) and np.all(np.abs(big[v < -50]) < 1e-15)
