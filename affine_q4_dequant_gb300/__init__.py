@@ -25,7 +25,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_experts", "gemv_rmsnorm",
+    "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
     "silu_mul_xsum", "moe_combine", "check_device_error", "STATUS", "MAX_SEGMENTS",
 ]
 
@@ -58,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "q4a_pack": (I32, [P, P, I64, I64, P]),
         "q4a_xsum": (I32, [P, P, I32, I64, P]),
         "q4a_gemv": (I32, [P, P, P, P, P, I32, I64, I64, P]),
+        "q4a_gemv_silu": (I32, [P, P, P, P, P, F, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_silu_mul_xsum": (I32, [P, P, P, I64, I64, P]),
@@ -143,6 +144,19 @@ def gemv_rmsnorm(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
         _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
         _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift), nb,
         out_dim, in_dim, _stream(stream)))
+    return out
+
+
+def gemv_silu(w: torch.Tensor, s: torch.Tensor, b: torch.Tensor, x: torch.Tensor, div: float,
+              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = silu((W.x) / div) elementwise; otherwise as gemv()."""
+    nb, in_dim = x.shape
+    out_dim = w.shape[0]
+    if out is None:
+        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
+    _check("q4a_gemv_silu", _lib.q4a_gemv_silu(
+        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
+        _dev(x, "x", _F16), float(div), nb, out_dim, in_dim, _stream(stream)))
     return out
 
 

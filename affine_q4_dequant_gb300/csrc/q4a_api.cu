@@ -79,8 +79,13 @@ q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_dim, q4a_
     return launch_xsum(xsum, x, nb, in_dim, (cudaStream_t)stream);
 }
 
-q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
-                    const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+}  // extern "C"
+
+namespace q4a {
+namespace {
+
+q4a_status gemv_common(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                       int nb, int64_t out_dim, int64_t in_dim, bool silu, float silu_div, cudaStream_t stream) {
     if (!y || !w || !s || !b || !x) return Q4A_ERR_NULL;
     if (nb < 1) return Q4A_ERR_SHAPE;
     q4a_status st = check_matrix_shape(out_dim, in_dim);
@@ -88,7 +93,7 @@ q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
         return Q4A_ERR_ALIGN;
     if (dense_tc_eligible(s, b, nb, in_dim))
-        return launch_dense_tc(w, s, b, x, y, nb, out_dim, in_dim, (cudaStream_t)stream);
+        return launch_dense_tc(w, s, b, x, y, nb, out_dim, in_dim, silu, silu_div, stream);
     std::vector<Segment> segs;
     push_segments(segs, 0, 0, nb);
     if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
@@ -104,7 +109,26 @@ q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_
     L.nseg = (int)segs.size();
     L.seg = segs.data();
     L.max_ntok = nb < 32 ? nb : 32;
-    return launch_gemv(L, (cudaStream_t)stream);
+    L.silu = silu;
+    L.silu_div = silu_div;
+    return launch_gemv(L, stream);
+}
+
+}  // namespace
+}  // namespace q4a
+
+extern "C" {
+
+q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                    const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+    return gemv_common(y, w, s, b, x, nb, out_dim, in_dim, false, 1.0f, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_silu(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                         const uint16_t* x, float div, int nb, int64_t out_dim, int64_t in_dim,
+                         q4a_stream_t stream) {
+    if (!(div == div) || div == 0.0f || !(div - div == 0.0f)) return Q4A_ERR_SHAPE;   // finite, nonzero
+    return gemv_common(y, w, s, b, x, nb, out_dim, in_dim, true, div, (cudaStream_t)stream);
 }
 
 q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,

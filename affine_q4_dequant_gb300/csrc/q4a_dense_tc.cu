@@ -119,6 +119,8 @@ struct TcParams {
     uint32_t a_col0;      // first TMEM column of the A stages (after the accumulators)
     uint32_t tmem_cols;
     uint32_t idesc;       // tcgen05 instruction descriptor (f16 x f16 -> f32, M 128, N n_pad)
+    float silu_div;       // output epilogue silu(y / silu_div) when silu
+    int32_t silu;
     TcLayout lay;
 };
 
@@ -430,7 +432,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     if (row < p.out_dim) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = v[j] * esc[u];
+                            if (c0 + j < p.nb) {
+                                float o = v[j] * esc[u];
+                                if (p.silu) {
+                                    const float t = o / p.silu_div;
+                                    o = t / (1.0f + expf(-t));
+                                }
+                                p.y[(int64_t)(c0 + j) * p.out_dim + row] = o;
+                            }
                     }
                 }
             }
@@ -561,8 +570,8 @@ bool tc_pick_layout(int n_pad, int max_smem, TcLayout& out, uint32_t& smem_bytes
 }
 
 q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s, const uint16_t* b,
-                        const uint16_t* x, float* y, int nb, int64_t out_dim, int64_t in_dim,
-                        cudaStream_t stream) {
+                        const uint16_t* x, float* y, int nb, int64_t out_dim, int64_t in_dim, bool silu,
+                        float silu_div, cudaStream_t stream) {
     EncodeTiledFn enc = tc_encode_fn();
     if (!enc) return Q4A_ERR_UNSUPPORTED;
     TcParams prm;
@@ -596,6 +605,8 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     prm.groups = (int32_t)(in_dim / kGroup);
     prm.nb = nb;
     prm.n_pad = n_pad;
+    prm.silu = silu ? 1 : 0;
+    prm.silu_div = silu ? silu_div : 1.0f;
     prm.n_units = (int32_t)((out_dim + kTcUnitRows - 1) / kTcUnitRows);
     // TMEM (512 columns): accumulators [acc_bufs][kTcUm][n_pad], then the A stages
     // [kTcAStages][kTcUm][kTcSG][32]
@@ -639,7 +650,8 @@ bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_
 }
 
 q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
-                           int nb, int64_t out_dim, int64_t in_dim, cudaStream_t stream) {
+                           int nb, int64_t out_dim, int64_t in_dim, bool silu, float silu_div,
+                           cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -660,7 +672,7 @@ q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* 
     for (int t0 = 0; t0 < nb; t0 += kTcMaxN) {
         const int n = nb - t0 < kTcMaxN ? nb - t0 : kTcMaxN;
         const q4a_status st = launch_chunk(d, w, s, b, x + (int64_t)t0 * in_dim, y + (int64_t)t0 * out_dim, n,
-                                           out_dim, in_dim, stream);
+                                           out_dim, in_dim, silu, silu_div, stream);
         if (st != Q4A_OK) return st;
     }
     return Q4A_OK;

@@ -754,7 +754,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         v = cp[row * NTOK + tok];
                     }
-                    p.y[(int64_t)(sg.tok0 + tok) * p.out_dim + lrow0 + row] = v * 16777216.0f;
+                    float out = v * 16777216.0f;
+                    if (p.post_silu) {   // silu(y / div): the gated-residual bottleneck epilogue
+                        const float t = out / p.post_div;
+                        out = t / (1.0f + expf(-t));
+                    }
+                    p.y[(int64_t)(sg.tok0 + tok) * p.out_dim + lrow0 + row] = out;
                 }
             }
             ++blk;
@@ -1010,6 +1015,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.y = L.y;
     prm.eps = L.eps;
     prm.shift = L.shift;
+    prm.post_silu = L.silu ? 1 : 0;
+    prm.post_div = L.silu ? L.silu_div : 1.0f;
     prm.out_dim = L.out_dim;
     prm.in_dim = L.in_dim;
     prm.groups = G;

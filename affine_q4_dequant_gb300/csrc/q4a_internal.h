@@ -111,6 +111,8 @@ struct GemvParams {
     const uint16_t* norm_w;   // bf16 [in_dim] (RMSNorm variant)
     float* y;                 // fp32 [slots][out_dim]
     float eps, shift;
+    float post_div;           // output epilogue silu(y / post_div) when post_silu
+    int32_t post_silu;
     int64_t out_dim;          // rows per segment matrix
     int64_t in_dim;
     int32_t groups;           // in_dim / 64
@@ -141,6 +143,8 @@ struct GemvLaunch {
     float eps, shift;
     int64_t out_dim, in_dim;
     bool rmsnorm;
+    bool silu;                // output epilogue y -> silu(y / silu_div)
+    float silu_div;
     bool experts;
     int nseg;
     const Segment* seg;
@@ -165,7 +169,8 @@ q4a_status read_and_clear_device_error(cudaStream_t stream, uint32_t* word);
 // Eligible when nb >= kDenseTcMinRows, in_dim % 512 == 0 and s, b are 16-byte aligned.
 bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_dim);
 q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
-                           int nb, int64_t out_dim, int64_t in_dim, cudaStream_t stream);
+                           int nb, int64_t out_dim, int64_t in_dim, bool silu, float silu_div,
+                           cudaStream_t stream);
 q4a_status read_and_clear_dense_tc_error(uint32_t* word);   // after a stream synchronisation
 
 // Records a CUDA error for q4a_last_cuda_error and returns Q4A_ERR_CUDA.

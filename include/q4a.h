@@ -107,6 +107,17 @@ Q4A_API q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const
                     q4a_stream_t stream);
 
 /*
+ * q4a_gemv_silu -- q4a_gemv whose outputs go through silu(y / div) on the way out
+ * ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b: the gated-residual bottleneck):
+ *     y[r][o] = v / (1 + e^-v),  v = (W.x)[r][o] / div
+ *   div  finite and nonzero (else Q4A_ERR_SHAPE); all other arguments, layouts, kernel
+ *   choice (NB >= 64 takes the tensor-core path) and errors as q4a_gemv.
+ */
+Q4A_API q4a_status q4a_gemv_silu(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                         const uint16_t* x, float div, int nb, int64_t out_dim, int64_t in_dim,
+                         q4a_stream_t stream);
+
+/*
  * q4a_gemv_experts -- A6: the GEMV over a routed-expert bank.
  *   y              out   fp32 [n_rows][out_dim]; row r = W_e . x[x_rows ? x_rows[r] : r]
  *                        for the segment a with token_offsets[a] <= r < token_offsets[a+1]

@@ -35,6 +35,7 @@ def lib():
     lib.q4a_gemv_rmsnorm.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
     lib.q4a_silu_mul_xsum.argtypes = [P, P, P, I64, I64, P]
     lib.q4a_moe_combine.argtypes = [P, P, P, P, I32, I32, I64, I64, P, P, P, P]
+    lib.q4a_gemv_silu.argtypes = [P, P, P, P, P, F, I32, I64, I64, P]
     return lib
 
 
@@ -147,4 +148,15 @@ def test_moe_combine_rejections(lib):
     assert f(A + 4, A, A, A, 2, 8, 16, 2048, None, None, None, None) == ALIGN
     assert f(A, A, A + 2, A, 2, 8, 16, 2048, None, None, None, None) == ALIGN
     assert f(A, A, A, A, 2, 8, 16, 2048, A + 8, A, A, None) == ALIGN        # y_shared
+
+
+def test_gemv_silu_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_gemv_silu
+    assert f(A, A, A, A, A, 0.0, 1, 64, 64, None) == SHAPE              # div = 0
+    assert f(A, A, A, A, A, float("inf"), 1, 64, 64, None) == SHAPE
+    assert f(A, A, A, A, A, float("nan"), 1, 64, 64, None) == SHAPE
+    assert f(None, A, A, A, A, 2.0, 1, 64, 64, None) == NULL
+    assert f(A, A, A, A, A, 2.0, 1, 64, 96, None) == SHAPE              # in_dim % 64
+    assert f(A, A + 1, A, A, A, 2.0, 1, 64, 64, None) == ALIGN
 
