@@ -59,6 +59,7 @@ def _load():
             "q4o_route_topk": (None, [P, P, P, I, I, I]),
             "q4o_moe_combine": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
             "q4o_gemv_silu": (None, [P, P, P, P, P, P, P, D, I, I, I]),
+            "q4o_rmsnorm_groups_f16": (None, [P, P, P, P, D, D, I, I, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -245,3 +246,15 @@ def gemv_silu(packed, s, b, x_bits, div: float):
     _load().q4o_gemv_silu(_p(out), _p(y), _p(bound), _p(packed), _p(s), _p(b), _p(x_bits), float(div),
                           nb, out_dim, in_dim)
     return out, y, bound
+
+
+def rmsnorm_groups_f16(x_raw, norm_w, groups: int, eps: float = 1e-6, shift: float = 0.0):
+    """Grouped RMSNorm: each of `groups` equal segments of a row normalised on its own.
+    Returns (xn fp16 bits [nb][in_dim], inv_rms [nb][groups])."""
+    x_raw, norm_w = _c(x_raw, np.float32), _c(norm_w, np.uint16)
+    nb, n = x_raw.shape
+    xn = np.empty((nb, n), np.uint16)
+    inv = np.empty((nb, groups), np.float64)
+    _load().q4o_rmsnorm_groups_f16(_p(xn), _p(inv), _p(x_raw), _p(norm_w), float(eps), float(shift), nb, n,
+                                   int(groups))
+    return xn, inv

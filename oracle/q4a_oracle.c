@@ -461,3 +461,29 @@ Q4O_EXPORT void q4o_gemv_silu(double* out, double* y, double* bound, const uint8
         out[i] = v / (1.0 + exp(-v));
     }
 }
+
+/* ---- grouped RMSNorm prologue ----------------------------------------------- */
+
+/* [BATCH_MSL] hyperconnection.metal fn_group_norm_b with `groups` streams per row: the
+ * row splits into groups equal segments of width n = in_dim / groups, each normalised
+ * with its own mean of squares; the weight is indexed by the position in the whole row:
+ *   xn[r][g*n + i] = x[r][g*n + i] / sqrt(mean_i x[r][g*n + i]^2 + eps) * (w[g*n + i] + shift),
+ * evaluated in double and rounded once to binary16. inv_rms [nb][groups] may be NULL. */
+Q4O_EXPORT void q4o_rmsnorm_groups_f16(uint16_t* xn, double* inv_rms, const float* x,
+                                       const uint16_t* w, double eps, double shift,
+                                       int64_t nb, int64_t in_dim, int64_t groups)
+{
+    const int64_t n = in_dim / groups;
+    for (int64_t r = 0; r < nb; r++)
+        for (int64_t g = 0; g < groups; g++) {
+            const float* xs = x + r * in_dim + g * n;
+            double ss = 0.0;
+            for (int64_t i = 0; i < n; i++)
+                ss += (double)xs[i] * (double)xs[i];
+            const double inv = 1.0 / sqrt(ss / (double)n + eps);
+            if (inv_rms)
+                inv_rms[r * groups + g] = inv;
+            for (int64_t i = 0; i < n; i++)
+                xn[r * in_dim + g * n + i] = half_round((double)xs[i] * inv * (bf16_value(w[g * n + i]) + shift));
+        }
+}

@@ -460,3 +460,36 @@ def test_gemv_silu_matches_the_plain_product_and_limits():
     v = y / 1e-4
     pos = v > 50
     assert np.allclose(big[pos], v[pos], rtol=1e-15) and np.all(np.abs(big[v < -50]) < 1e-15)
+
+
+# ---- grouped RMSNorm ("BATCH_MSL" page, hyperconnection.metal fn_group_norm_b, groups > 1) ----
+
+def test_rmsnorm_groups_one_group_is_the_row_norm():
+    rng = np.random.default_rng(51)
+    x = rng.normal(0, 2, (3, 256)).astype(np.float32)
+    w = wl.norm_weight(0, 0, 256)
+    a, ia = oracle.rmsnorm_groups_f16(x, w, 1, eps=1e-6, shift=0.25)
+    b, ib = oracle.rmsnorm_f16(x, w, eps=1e-6, shift=0.25)
+    assert np.array_equal(a, b) and np.array_equal(ia[:, 0], ib)
+
+
+def test_rmsnorm_groups_are_independent_segments():
+    """Each segment equals the one-group norm of that segment alone (weight slice g*n..)."""
+    rng = np.random.default_rng(52)
+    x = rng.normal(0, 1, (2, 512)).astype(np.float32)
+    x[:, 128:256] *= 40.0                  # one loud segment: the others must not notice
+    w = wl.norm_weight(0, 1, 512)
+    xn, inv = oracle.rmsnorm_groups_f16(x, w, 4)
+    for g in range(4):
+        seg, iseg = oracle.rmsnorm_f16(x[:, 128 * g:128 * (g + 1)], w[128 * g:128 * (g + 1)])
+        assert np.array_equal(xn[:, 128 * g:128 * (g + 1)], seg) and np.array_equal(inv[:, g], iseg)
+
+
+def test_rmsnorm_groups_unit_rms_per_segment():
+    """w = 1, shift = 0, eps = 0: every segment of the output has RMS 1 (up to fp16 rounding)."""
+    rng = np.random.default_rng(53)
+    x = rng.normal(0, 1, (2, 384)).astype(np.float32) * np.repeat([0.01, 1.0, 100.0], 128)
+    w = wl.f32_to_bf16_bits(np.ones(384, np.float32))
+    xn, _ = oracle.rmsnorm_groups_f16(x, w, 3, eps=0.0)
+    v = xn.view(np.float16).astype(np.float64).reshape(2, 3, 128)
+    assert np.allclose(np.sqrt((v ** 2).mean(axis=2)), 1.0, rtol=2e-3)
