@@ -26,6 +26,7 @@ from . import _build
 
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
+    "gemv_rmsnorm_grouped",
     "silu_mul_xsum", "moe_combine", "check_device_error", "STATUS", "MAX_SEGMENTS",
 ]
 
@@ -61,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "q4a_gemv_silu": (I32, [P, P, P, P, P, F, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
+        "q4a_gemv_rmsnorm_grouped": (I32, [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
         "q4a_silu_mul_xsum": (I32, [P, P, P, I64, I64, P]),
         "q4a_moe_combine": (I32, [P, P, P, P, I32, I32, I64, I64, P, P, P, P]),
         "q4a_check_device_error": (I32, [P]),
@@ -177,6 +179,20 @@ def gemv_experts(w_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n
         ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
         int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim), int(in_dim),
         _stream(stream)))
+    return out
+
+
+def gemv_rmsnorm_grouped(w, s, b, x_raw, norm_w, norm_groups: int, eps: float = 1e-6, shift: float = 0.0,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gemv_rmsnorm with norm_groups equal segments per row, each normalised on its own."""
+    nb, in_dim = x_raw.shape
+    out_dim = w.shape[0]
+    if out is None:
+        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x_raw.device)
+    _check("q4a_gemv_rmsnorm_grouped", _lib.q4a_gemv_rmsnorm_grouped(
+        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
+        _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift),
+        int(norm_groups), nb, out_dim, in_dim, _stream(stream)))
     return out
 
 

@@ -131,14 +131,16 @@ q4a_status q4a_gemv_silu(float* y, const uint8_t* w, const uint16_t* s, const ui
     return gemv_common(y, w, s, b, x, nb, out_dim, in_dim, true, div, (cudaStream_t)stream);
 }
 
-q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
-                            const float* x_raw, const uint16_t* norm_w, float eps, float shift,
-                            int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+q4a_status q4a_gemv_rmsnorm_grouped(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                                    const float* x_raw, const uint16_t* norm_w, float eps, float shift,
+                                    int norm_groups, int nb, int64_t out_dim, int64_t in_dim,
+                                    q4a_stream_t stream) {
     if (!y || !w || !s || !b || !x_raw || !norm_w) return Q4A_ERR_NULL;
-    if (nb < 1 || !(eps >= 0.0f)) return Q4A_ERR_SHAPE;
+    if (nb < 1 || !(eps >= 0.0f) || norm_groups < 1) return Q4A_ERR_SHAPE;
     q4a_status st = check_matrix_shape(out_dim, in_dim);
     if (st != Q4A_OK) return st;
-    if (nb > 32) return Q4A_ERR_UNSUPPORTED;
+    if (in_dim % ((int64_t)kGroup * norm_groups) != 0) return Q4A_ERR_SHAPE;
+    if (nb > 32 || norm_groups > kMaxNormGroups) return Q4A_ERR_UNSUPPORTED;
     if (!aligned(w, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(s, 2) ||
         !aligned(b, 2) || !aligned(y, 4))
         return Q4A_ERR_ALIGN;
@@ -157,10 +159,17 @@ q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const
     L.out_dim = out_dim;
     L.in_dim = in_dim;
     L.rmsnorm = true;
+    L.norm_groups = norm_groups;
     L.nseg = (int)segs.size();
     L.seg = segs.data();
     L.max_ntok = nb;
     return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                            const float* x_raw, const uint16_t* norm_w, float eps, float shift,
+                            int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+    return q4a_gemv_rmsnorm_grouped(y, w, s, b, x_raw, norm_w, eps, shift, 1, nb, out_dim, in_dim, stream);
 }
 
 q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_bank,

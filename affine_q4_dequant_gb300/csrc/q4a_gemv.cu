@@ -195,7 +195,9 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
                 v[0] = ld[k][0].x; v[1] = ld[k][0].y; v[2] = ld[k][0].z; v[3] = ld[k][0].w;
                 u[0] = ld[k][1].x; u[1] = ld[k][1].y; u[2] = ld[k][1].z; u[3] = ld[k][1].w;
             } else {
-                const float inv = live ? inv_s[tok] : 0.f;
+                // the item's 16 inputs lie in one 64-group, hence in one normalisation segment
+                const int seg = (int)(((int64_t)(kg0 + gl) * kGroup) / p.norm_width);
+                const float inv = live ? inv_s[tok * p.norm_groups + seg] : 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint4 f0 = ld[k][2 * half], f1 = ld[k][2 * half + 1], wv = ld[k][4 + half];
@@ -279,7 +281,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Sum of squares of this CTA's K-slice of every activation row (the RMSNorm prologue).
+// Sum of squares of this CTA's K-slice of every activation row (the RMSNorm prologue), per
+// normalisation segment of the row (ssq_s[tok * G + seg]; segments outside the slice get 0).
 // Warp w owns rows w, w+8, ...; each lane issues up to 16 independent 16-byte loads per
 // round before accumulating.
 template <int NT, class P>
@@ -287,26 +290,33 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
                             int lane) {
     constexpr int NTOK = NT * 8;
     constexpr int U = 16;
-    const int chunks = gsz * (kGroup / 4);     // float4 chunks per row slice
+    const int G = p.norm_groups;
+    const int64_t k_lo = (int64_t)kg0 * kGroup, k_hi = k_lo + (int64_t)gsz * kGroup;
     for (int tok = warp; tok < NTOK; tok += kConsumerWarps) {
-        float acc = 0.f;
-        if (tok < sg.ntok) {
-            const float4* xr = reinterpret_cast<const float4*>(
-                static_cast<const float*>(p.x) + (int64_t)(sg.tok0 + tok) * p.in_dim + (int64_t)kg0 * kGroup);
-            for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
-                float4 f[U];
+        for (int seg = 0; seg < G; ++seg) {
+            const int64_t s_lo = llmax(k_lo, (int64_t)seg * p.norm_width);
+            const int64_t s_hi = llmin(k_hi, (int64_t)(seg + 1) * p.norm_width);
+            float acc = 0.f;
+            if (tok < sg.ntok && s_lo < s_hi) {
+                const float4* xr = reinterpret_cast<const float4*>(
+                    static_cast<const float*>(p.x) + (int64_t)(sg.tok0 + tok) * p.in_dim + s_lo);
+                const int chunks = (int)((s_hi - s_lo) / 4);   // float4 chunks of this segment's part
+                for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
+                    float4 f[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * 32 + lane;
-                    f[u] = c < chunks ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + u * 32 + lane;
+                        f[u] = c < chunks ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        acc += f[u].x * f[u].x + f[u].y * f[u].y + f[u].z * f[u].z + f[u].w * f[u].w;
                 }
-#pragma unroll
-                for (int u = 0; u < U; ++u) acc += f[u].x * f[u].x + f[u].y * f[u].y + f[u].z * f[u].z + f[u].w * f[u].w;
             }
-        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) ssq_s[tok] = acc;
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) ssq_s[tok * G + seg] = acc;
+        }
     }
 }
 
@@ -555,11 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 consumer_sync();
             }
-            if (ctid < NTOK) {
+            const int ng = NTOK * p.norm_groups;
+            for (int e = ctid; e < ng; e += kConsumerWarps * 32) {
                 float tot = 0.f;
                 for (int c = 0; c < C; ++c)
-                    tot += C > 1 ? ld_peer_f32(map_peer(smem_addr(ssq_s + ctid), c)) : ssq_s[ctid];
-                ssq_s[NTOK + ctid] = rsqrtf(tot / (float)p.in_dim + p.eps);
+                    tot += C > 1 ? ld_peer_f32(map_peer(smem_addr(ssq_s + e), c)) : ssq_s[e];
+                ssq_s[NTOK * kMaxNormGroups + e] = rsqrtf(tot / (float)p.norm_width + p.eps);
             }
             consumer_sync();
         }
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = p.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK, ctid);
+                stage_x<NT, RMS>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
                 consumer_sync();
@@ -1015,6 +1026,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.y = L.y;
     prm.eps = L.eps;
     prm.shift = L.shift;
+    prm.norm_groups = L.norm_groups > 0 ? L.norm_groups : 1;
+    prm.norm_width = L.in_dim / prm.norm_groups;
     prm.post_silu = L.silu ? 1 : 0;
     prm.post_div = L.silu ? L.silu_div : 1.0f;
     prm.out_dim = L.out_dim;

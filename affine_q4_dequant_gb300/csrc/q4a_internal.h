@@ -24,6 +24,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path
 constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
+constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation segments per row
 
 // How the producer fetches a row block's scales and biases into shared memory. Both modes
 // write the same layout: [64-group chunk][row][128 bytes], 16-byte granule u of row r
@@ -87,7 +88,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     L.wpart = L.sb + L.n_sb * L.sb_buf;
     L.cpart = L.wpart + (uint32_t)kGroupSlots * rows * ntok * 4u;
     L.ssq = L.cpart + 2u * rows * ntok * 4u;
-    L.raw = align_up(L.ssq + 2u * ntok * 4u, 128);
+    L.raw = align_up(L.ssq + 2u * ntok * (uint32_t)kMaxNormGroups * 4u, 128);   // sums, then factors
     // a row block's elements plus up to 7 in front (the box start is rounded down to 16 bytes)
     L.raw_elems = sb_mode == kSbRaw ? align_up(rows * (uint32_t)gs + 7u, (uint32_t)kRawBox) : 0u;
     L.bars = align_up(L.raw + 2u * 2u * L.raw_elems * 2u, 8);
@@ -113,6 +114,8 @@ struct GemvParams {
     float eps, shift;
     float post_div;           // output epilogue silu(y / post_div) when post_silu
     int32_t post_silu;
+    int32_t norm_groups;      // RMSNorm variant: segments per row, each normalised on its own
+    int64_t norm_width;       // in_dim / norm_groups
     int64_t out_dim;          // rows per segment matrix
     int64_t in_dim;
     int32_t groups;           // in_dim / 64
@@ -145,6 +148,7 @@ struct GemvLaunch {
     bool rmsnorm;
     bool silu;                // output epilogue y -> silu(y / silu_div)
     float silu_div;
+    int norm_groups;          // RMSNorm variant: normalisation segments per row (>= 1)
     bool experts;
     int nseg;
     const Segment* seg;

@@ -159,6 +159,20 @@ Q4A_API q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* 
                             int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream);
 
 /*
+ * q4a_gemv_rmsnorm_grouped -- q4a_gemv_rmsnorm with norm_groups normalisation segments
+ * per row ("BATCH_MSL", hyperconnection.metal fn_group_norm_b with groups > 1, the
+ * multi-stream form of fn_norm_prep_b): with n = in_dim / norm_groups,
+ *     xn[r][g*n + i] = fp16( x_raw[r][g*n + i] * rsqrt(mean_i x_raw[r][g*n + i]^2 + eps)
+ *                            * (norm_w[g*n + i] + shift) ),   then y = W.xn.
+ *   Requires 1 <= norm_groups <= 8 and in_dim % (64 * norm_groups) == 0; otherwise as
+ *   q4a_gemv_rmsnorm (which is this call with norm_groups = 1).
+ */
+Q4A_API q4a_status q4a_gemv_rmsnorm_grouped(float* y, const uint8_t* w, const uint16_t* s,
+                                    const uint16_t* b, const float* x_raw, const uint16_t* norm_w,
+                                    float eps, float shift, int norm_groups, int nb, int64_t out_dim,
+                                    int64_t in_dim, q4a_stream_t stream);
+
+/*
  * q4a_silu_mul_xsum -- A7: the step between the two routed-expert GEMVs.
  *   h        out  fp16 [rows][inter];  h[r][j] = fp16( silu(gate) * up ),
  *                 silu(v) = v / (1 + e^-v), gate = gate_up[r][j], up = gate_up[r][inter + j]

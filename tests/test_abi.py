@@ -36,6 +36,7 @@ def lib():
     lib.q4a_silu_mul_xsum.argtypes = [P, P, P, I64, I64, P]
     lib.q4a_moe_combine.argtypes = [P, P, P, P, I32, I32, I64, I64, P, P, P, P]
     lib.q4a_gemv_silu.argtypes = [P, P, P, P, P, F, I32, I64, I64, P]
+    lib.q4a_gemv_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     return lib
 
 
@@ -159,4 +160,15 @@ def test_gemv_silu_rejections(lib):
     assert f(None, A, A, A, A, 2.0, 1, 64, 64, None) == NULL
     assert f(A, A, A, A, A, 2.0, 1, 64, 96, None) == SHAPE              # in_dim % 64
     assert f(A, A + 1, A, A, A, 2.0, 1, 64, 64, None) == ALIGN
+
+
+def test_rmsnorm_grouped_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_gemv_rmsnorm_grouped
+    assert f(A, A, A, A, A, A, 1e-6, 0.0, 0, 1, 64, 512, None) == SHAPE      # groups < 1
+    assert f(A, A, A, A, A, A, 1e-6, 0.0, 3, 1, 64, 512, None) == SHAPE      # 512 % (64*3)
+    assert f(A, A, A, A, A, A, 1e-6, 0.0, 16, 1, 64, 1024, None) == UNSUP    # groups > 8
+    assert f(A, A, A, A, A, A, 1e-6, 0.0, 2, 33, 64, 512, None) == UNSUP     # nb > 32
+    assert f(A, A, A, A, A, A, -1.0, 0.0, 2, 1, 64, 512, None) == SHAPE      # eps < 0
+    assert f(A, A, A, A, A + 4, A, 1e-6, 0.0, 2, 1, 64, 512, None) == ALIGN  # x_raw
 

@@ -192,6 +192,26 @@ def test_gemv_rmsnorm_matches_oracle(out_dim, in_dim, nb, shift):
     assert_within_bound(host(y), y_ref, bound, f"gemv_rmsnorm {out_dim}x{in_dim} nb={nb}")
 
 
+@pytest.mark.parametrize("out_dim,in_dim,nb,groups", [(300, 1024, 4, 2), (77, 4096, 16, 4), (40, 512, 1, 8),
+                                                      (33, 12288, 3, 3), (129, 2048, 9, 1)])
+def test_gemv_rmsnorm_grouped_matches_oracle(out_dim, in_dim, nb, groups):
+    """Each of `groups` segments of a row normalised on its own (one loud segment), on both
+    the single-CTA and the cluster K-split layouts."""
+    codes, s, b, _ = ragged_case(out_dim, in_dim, nb, 12)
+    a = wl.normal_f32(78, 0, (nb, in_dim)) * 3.0
+    n = in_dim // groups
+    a[:, :n] *= 50.0
+    nw = wl.norm_weight(78, 1, in_dim)
+    packed = oracle.pack(codes)
+    y = torch.full((nb, out_dim), float("nan"), dtype=torch.float32, device=DEV)
+    q4a.gemv_rmsnorm_grouped(dev(packed), dev(s), dev(b), dev(a), dev(nw), groups, eps=1e-6, out=y)
+    torch.cuda.synchronize()
+    q4a.check_device_error()
+    xn, _ = oracle.rmsnorm_groups_f16(a, nw, groups, eps=1e-6)
+    y_ref, bound = oracle.gemv(packed, s, b, xn)
+    assert_within_bound(host(y), y_ref, bound, f"gemv_rmsnorm_grouped {out_dim}x{in_dim} nb={nb} groups={groups}")
+
+
 # ---- A7 --------------------------------------------------------------------------------
 
 def ulp16(v: np.ndarray) -> np.ndarray:
