@@ -58,9 +58,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait: after kWaitLimitNs the thread records the failure in the device error
 // word and in the CTA's abort flag, then carries on. Control flow never depends on
 // shared-memory data, so a give-up can only produce garbage values, never a hang, a
-// skipped barrier or an out-of-range address.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return;
+// skipped barrier or an out-of-range address. The retry loop is out of line: every launch
+// starts with a cold instruction cache, and inlining it at each wait site costs more
+// fetch time than the call costs a thread that is waiting anyway.
+__device__ __noinline__ void mbar_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return;
@@ -73,6 +74,11 @@ __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return;
+    mbar_wait_slow(bar, parity, abort_flag);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,

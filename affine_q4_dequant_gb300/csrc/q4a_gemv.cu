@@ -954,7 +954,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     const int G = (int)(L.in_dim / kGroup);
 
     // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
-    // ring of at least 4 stages. Among them: the smallest that gives every cluster >= 3 row
+    // ring of at least 3 stages (a deeper ring matters less than avoiding the split: each
+    // split row block pays a cluster-wide barrier and a DSMEM reduction). Among them: the smallest that gives every cluster >= 3 row
     // tiles (a row block worth a few TMA boxes) while its co-resident clusters still cover
     // >= 90% of the SMs (clusters must fit inside a GPC, which can strand SMs).
     const int ntm = L.max_ntok;
@@ -987,10 +988,10 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     };
     int C = 0;
     for (int c = 1; c <= 8; c *= 2) {
-        if (!fits(c, 4)) continue;
+        if (!fits(c, 3)) continue;
         if (C == 0) C = c;                       // smallest that fits at all
         const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
-                                       smem_layout(nt, mt, 4, slice(c), ntm, sbmode(c), sbufs(c)).total + 1024);
+                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c)).total + 1024);
         if (q <= 0) continue;
         if (n_tiles >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
             C = c;

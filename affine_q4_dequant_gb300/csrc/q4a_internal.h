@@ -19,7 +19,7 @@ constexpr int kGroupSlots = kStageGroups; // one consumer warp per group of a st
 constexpr int kConsumerWarps = kGroupSlots;       // each owns every tile of the row block
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDenseMaxSeg = 8;         // token chunks of one dense call
-constexpr int kXFragBudget = 64 * 1024; // staged activation fragments per CTA
+constexpr int kXFragBudget = 128 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path
