@@ -60,6 +60,10 @@ def _load():
             "q4o_moe_combine": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
             "q4o_gemv_silu": (None, [P, P, P, P, P, P, P, D, I, I, I]),
             "q4o_rmsnorm_groups_f16": (None, [P, P, P, P, D, D, I, I, I]),
+            "q4o_lowbit_pack2": (None, [P, P, I, I]),
+            "q4o_lowbit_pack3lo": (None, [P, P, I, I]),
+            "q4o_lowbit_codes": (None, [P, P, P, I, I]),
+            "q4o_gemv_lowbit": (None, [P, P, P, P, P, P, P, I, I, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -258,3 +262,47 @@ def rmsnorm_groups_f16(x_raw, norm_w, groups: int, eps: float = 1e-6, shift: flo
     _load().q4o_rmsnorm_groups_f16(_p(xn), _p(inv), _p(x_raw), _p(norm_w), float(eps), float(shift), nb, n,
                                    int(groups))
     return xn, inv
+
+
+# ---- derived low-bit codes ([BATCH_MSL] fn_q2_rows_h, fn_q3_rows_h) ------------------------
+
+
+def lowbit_pack2(codes):
+    """4-bit codes [rows][in] (one per byte) -> 2-bit packed rows [rows][in/4] of q4 >> 2."""
+    codes = _c(codes, np.uint8)
+    rows, in_dim = codes.shape
+    out = np.empty((rows, in_dim // 4), np.uint8)
+    _load().q4o_lowbit_pack2(_p(out), _p(codes), rows, in_dim)
+    return out
+
+
+def lowbit_pack3lo(codes):
+    """4-bit codes [rows][in] -> the lowest-bit plane [rows][in/8] of the 3-bit codes q4 >> 1."""
+    codes = _c(codes, np.uint8)
+    rows, in_dim = codes.shape
+    out = np.empty((rows, in_dim // 8), np.uint8)
+    _load().q4o_lowbit_pack3lo(_p(out), _p(codes), rows, in_dim)
+    return out
+
+
+def lowbit_codes(w2, wlo=None):
+    """The derived codes read back from the packed layout: q2 (wlo None) or q3."""
+    w2 = _c(w2, np.uint8)
+    rows, in_dim = w2.shape[0], w2.shape[1] * 4
+    wlo = None if wlo is None else _c(wlo, np.uint8)
+    out = np.empty((rows, in_dim), np.uint8)
+    _load().q4o_lowbit_codes(_p(out), _p(w2), _p(wlo), rows, in_dim)
+    return out
+
+
+def gemv_lowbit(w2, wlo, s, b, x_bits):
+    """y = W x with W from derived 2-bit (wlo None) or 3-bit codes. Returns (y, bound)."""
+    w2, s, b, x_bits = _c(w2, np.uint8), _c(s, np.uint16), _c(b, np.uint16), _c(x_bits, np.uint16)
+    wlo = None if wlo is None else _c(wlo, np.uint8)
+    nb, in_dim = x_bits.shape
+    out_dim = w2.shape[0]
+    y = np.empty((nb, out_dim), np.float64)
+    bound = np.empty((nb, out_dim), np.float64)
+    _load().q4o_gemv_lowbit(_p(y), _p(bound), _p(w2), _p(wlo), _p(s), _p(b), _p(x_bits), nb, out_dim, in_dim)
+    return y, bound
+

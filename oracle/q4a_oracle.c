@@ -487,3 +487,122 @@ Q4O_EXPORT void q4o_rmsnorm_groups_f16(uint16_t* xn, double* inv_rms, const floa
                 xn[r * in_dim + g * n + i] = half_round((double)xs[i] * inv * (bf16_value(w[g * n + i]) + shift));
         }
 }
+
+/* ---- derived low-bit codes (2-bit and 3-bit) ------------------------------------ */
+
+/* [BATCH_MSL] quantized_rows.metal fn_q2_rows_h and fn_q3_rows_h. The low-bit codes are
+ * derived from the 4-bit ones: q2 = q4 >> 2 with the quad midpoint w = (4 q2 + 1.5) s + b,
+ * and q3 = q4 >> 1 with w = (2 q3 + 0.5) s + b. The 2-bit row is a run of 32-code chunks,
+ * two little-endian 32-bit words each; byte b of word t of chunk c holds four 2-bit fields
+ * (the masked casts of the kernel pair them with the even / odd activation streams):
+ *     field 0 (bits 1:0)  element 32c + 2(8t + b)
+ *     field 1 (bits 3:2)  element 32c + 2(8t + 4 + b)
+ *     field 2 (bits 5:4)  element 32c + 2(8t + b) + 1
+ *     field 3 (bits 7:6)  element 32c + 2(8t + 4 + b) + 1
+ * A 3-bit code is 2 * upper + lowest: the upper two bits (= q2) in the 2-bit layout, and one
+ * 32-bit word per chunk of lowest bits, the bit of the element in field j of byte b of upper
+ * word t sitting at bit 4t + j of byte b. The pages interleave the three words of a chunk;
+ * this library keeps the lowest-bit words as a plane of their own ([rows][in/32] words). */
+
+/* element index (within its 32-code chunk) of field j, byte b, word t */
+static int lowbit_element(int t, int b, int j)
+{
+    const int even_slot = 8 * t + ((j & 1) ? 4 : 0) + b;   /* index in the even / odd stream */
+    return 2 * even_slot + ((j & 2) ? 1 : 0);
+}
+
+/* codes[rows][in_dim] (4-bit codes, one per byte) -> the 2-bit packed rows [rows][in_dim/4]. */
+Q4O_EXPORT void q4o_lowbit_pack2(uint8_t* w2, const uint8_t* codes, int64_t rows, int64_t in_dim)
+{
+    for (int64_t o = 0; o < rows; o++)
+        for (int64_t c = 0; c < in_dim / 32; c++)
+            for (int t = 0; t < 2; t++)
+                for (int b = 0; b < 4; b++) {
+                    int v = 0;
+                    for (int j = 0; j < 4; j++) {
+                        const int q4 = codes[o * in_dim + 32 * c + lowbit_element(t, b, j)] & 0x0F;
+                        v |= (q4 >> 2) << (2 * j);
+                    }
+                    w2[o * (in_dim / 4) + 8 * c + 4 * t + b] = (uint8_t)v;
+                }
+}
+
+/* codes[rows][in_dim] -> the lowest-bit plane of the 3-bit codes [rows][in_dim/8] bytes. */
+Q4O_EXPORT void q4o_lowbit_pack3lo(uint8_t* wlo, const uint8_t* codes, int64_t rows, int64_t in_dim)
+{
+    for (int64_t o = 0; o < rows; o++)
+        for (int64_t c = 0; c < in_dim / 32; c++)
+            for (int b = 0; b < 4; b++) {
+                int v = 0;
+                for (int t = 0; t < 2; t++)
+                    for (int j = 0; j < 4; j++) {
+                        const int q4 = codes[o * in_dim + 32 * c + lowbit_element(t, b, j)] & 0x0F;
+                        v |= ((q4 >> 1) & 1) << (4 * t + j);
+                    }
+                wlo[o * (in_dim / 8) + 4 * c + b] = (uint8_t)v;
+            }
+}
+
+/* The code of element i of a row, read back from the packed layout: q2 (wlo NULL) or q3. */
+static int lowbit_code_at(const uint8_t* w2row, const uint8_t* wlorow, int64_t i)
+{
+    const int64_t c = i / 32;
+    const int e = (int)(i % 32);
+    const int odd = e & 1;
+    const int slot = e >> 1;                 /* 0..15 in the even / odd stream */
+    const int t = slot / 8;
+    const int hi4 = (slot % 8) >= 4;
+    const int b = slot % 4;
+    const int j = (hi4 ? 1 : 0) + (odd ? 2 : 0);
+    const int up = (w2row[8 * c + 4 * t + b] >> (2 * j)) & 3;
+    if (!wlorow)
+        return up;
+    const int lo = (wlorow[4 * c + b] >> (4 * t + j)) & 1;
+    return 2 * up + lo;
+}
+
+/* codes[rows][in_dim] = the derived codes read back from the packed layout. */
+Q4O_EXPORT void q4o_lowbit_codes(uint8_t* codes, const uint8_t* w2, const uint8_t* wlo,
+                                 int64_t rows, int64_t in_dim)
+{
+    for (int64_t o = 0; o < rows; o++)
+        for (int64_t i = 0; i < in_dim; i++)
+            codes[o * in_dim + i] = (uint8_t)lowbit_code_at(w2 + o * (in_dim / 4),
+                                                            wlo ? wlo + o * (in_dim / 8) : NULL, i);
+}
+
+/* y[r][o] = sum_i w[o][i] x[r][i] with w = (4 q2 + 1.5) s + b (wlo NULL: 2-bit) or
+ * w = (2 q3 + 0.5) s + b (3-bit), dequantised explicitly in double; bound as q4o_gemv. */
+Q4O_EXPORT void q4o_gemv_lowbit(double* y, double* bound, const uint8_t* w2, const uint8_t* wlo,
+                                const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                                int64_t nb, int64_t out_dim, int64_t in_dim)
+{
+    const int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    double* xv = (double*)malloc((size_t)(nb * in_dim) * sizeof(double));
+    for (int64_t i = 0; i < nb * in_dim; i++)
+        xv[i] = half_value(x[i]);
+    for (int64_t o = 0; o < out_dim; o++) {
+        const uint8_t* w2row = w2 + o * (in_dim / 4);
+        const uint8_t* wlorow = wlo ? wlo + o * (in_dim / 8) : NULL;
+        for (int64_t i = 0; i < in_dim; i++) {
+            const double sv = bf16_value(s[o * groups + i / 64]);
+            const double bv = bf16_value(b[o * groups + i / 64]);
+            const double q = (double)lowbit_code_at(w2row, wlorow, i);
+            w[i] = wlorow ? sv * (2.0 * q + 0.5) + bv : sv * (4.0 * q + 1.5) + bv;
+        }
+        for (int64_t r = 0; r < nb; r++) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < in_dim; i++) {
+                const double p = w[i] * xv[r * in_dim + i];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[r * out_dim + o] = acc;
+            if (bound)
+                bound[r * out_dim + o] = 2e-3 * mag + 1e-5;
+        }
+    }
+    free(xv);
+    free(w);
+}

@@ -493,3 +493,84 @@ def test_rmsnorm_groups_unit_rms_per_segment():
     xn, _ = oracle.rmsnorm_groups_f16(x, w, 3, eps=0.0)
     v = xn.view(np.float16).astype(np.float64).reshape(2, 3, 128)
     assert np.allclose(np.sqrt((v ** 2).mean(axis=2)), 1.0, rtol=2e-3)
+
+
+# ---- derived low-bit codes ([BATCH_MSL] fn_q2_rows_h, fn_q3_rows_h) ----------------------
+
+
+def _golden_lowbit_row(golden):
+    g = golden("lowbit_layout.txt")
+    codes = np.zeros((1, 64), np.uint8)
+    for item in g["codes"]:
+        e, v = item.split("=")
+        codes[0, int(e)] = int(v)
+    w2 = np.array([int(v, 16) for v in g["w2_words"]], np.uint32)
+    lo = np.array([int(v, 16) for v in g["lo_words"]], np.uint32)
+    return codes, w2, lo
+
+
+def test_lowbit_layout_hand_worked(golden):
+    codes, w2_words, lo_words = _golden_lowbit_row(golden)
+    w2 = oracle.lowbit_pack2(codes)
+    lo = oracle.lowbit_pack3lo(codes)
+    assert np.array_equal(w2.view("<u4").ravel(), w2_words)
+    assert np.array_equal(lo.view("<u4").ravel(), lo_words)
+    assert np.array_equal(oracle.lowbit_codes(w2), codes >> 2)
+    assert np.array_equal(oracle.lowbit_codes(w2, lo), codes >> 1)
+
+
+def test_lowbit_codes_are_the_shifted_4bit_codes():
+    rng = np.random.default_rng(41)
+    codes = rng.integers(0, 16, (7, 192), dtype=np.uint8)
+    w2, lo = oracle.lowbit_pack2(codes), oracle.lowbit_pack3lo(codes)
+    assert np.array_equal(oracle.lowbit_codes(w2), codes >> 2)
+    assert np.array_equal(oracle.lowbit_codes(w2, lo), codes >> 1)
+    # every code lands in exactly one field: packing a single nonzero code sets one field
+    one = np.zeros((1, 64), np.uint8)
+    for e in range(64):
+        one[:] = 0
+        one[0, e] = 12
+        bits = np.unpackbits(oracle.lowbit_pack2(one)).sum()
+        assert bits == 2 and np.unpackbits(oracle.lowbit_pack3lo(one)).sum() == 0
+
+
+def _lowbit_case(seed, rows, in_dim, nb):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, (rows, in_dim), dtype=np.uint8)
+    s = wl.f32_to_bf16_bits(np.abs(rng.normal(0, 0.02, (rows, in_dim // 64))).astype(np.float32))
+    b = wl.f32_to_bf16_bits((-8 * rng.normal(0, 0.01, (rows, in_dim // 64))).astype(np.float32))
+    x = wl.f16_bits(rng.normal(0, 1, (nb, in_dim)))
+    return codes, s, b, x
+
+
+def test_lowbit_gemv_is_the_quad_midpoint_of_the_4bit_product():
+    """w2 = (4 q2 + 1.5) s + b is the mean of the four 4-bit weights s q4 + b sharing q2,
+    and w3 = (2 q3 + 0.5) s + b the mean of the two sharing q3: the low-bit products are the
+    means of 4-bit products (the pinned 4-bit oracle) over the codes of each quad / pair."""
+    codes, s, b, x = _lowbit_case(42, 9, 128, 3)
+    y2, _ = oracle.gemv_lowbit(oracle.lowbit_pack2(codes), None, s, b, x)
+    quads = [oracle.gemv(oracle.pack(((codes >> 2) << 2) + k), s, b, x)[0] for k in range(4)]
+    np.testing.assert_allclose(y2, sum(quads) / 4, rtol=1e-12, atol=1e-12)
+    y3, _ = oracle.gemv_lowbit(oracle.lowbit_pack2(codes), oracle.lowbit_pack3lo(codes), s, b, x)
+    pairs = [oracle.gemv(oracle.pack(((codes >> 1) << 1) + k), s, b, x)[0] for k in range(2)]
+    np.testing.assert_allclose(y3, sum(pairs) / 2, rtol=1e-12, atol=1e-12)
+
+
+def test_lowbit_gemv_brute_force_tiny():
+    codes, s, b, x = _lowbit_case(43, 3, 64, 2)
+    sf, bf = wl.bf16_bits_to_f32(s).astype(float), wl.bf16_bits_to_f32(b).astype(float)
+    xf = x.view(np.float16).astype(float)
+    for bits in (2, 3):
+        w2 = oracle.lowbit_pack2(codes)
+        lo = oracle.lowbit_pack3lo(codes) if bits == 3 else None
+        y, bound = oracle.gemv_lowbit(w2, lo, s, b, x)
+        for r in range(2):
+            for o in range(3):
+                acc = 0.0
+                for i in range(64):
+                    q = int(codes[o, i])
+                    w = (4 * (q >> 2) + 1.5) * sf[o, 0] + bf[o, 0] if bits == 2 else \
+                        (2 * (q >> 1) + 0.5) * sf[o, 0] + bf[o, 0]
+                    acc += w * xf[r, i]
+                assert abs(y[r, o] - acc) <= 1e-12 * (1 + abs(acc))
+        assert np.all(bound > 0)
