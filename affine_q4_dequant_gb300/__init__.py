@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
         "q4a_xsum": (I32, [P, P, I32, I64, P]),
         "q4a_gemv": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_silu": (I32, [P, P, P, P, P, F, I32, I64, I64, P]),
+        "q4a_lowbit_pack": (I32, [P, P, P, I64, I64, P]),
+        "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_grouped": (I32, [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
@@ -113,6 +115,32 @@ def pack(codes: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> t
         out = torch.empty((rows, in_dim // 2), dtype=torch.uint8, device=codes.device)
     _check("q4a_pack", _lib.q4a_pack(_dev(out, "out", _U8), _dev(codes, "codes", _U8), rows, in_dim,
                                      _stream(stream)))
+    return out
+
+
+def lowbit_pack(w_packed: torch.Tensor, with_lowest: bool = True, stream=None):
+    """Derived low-bit codes of a packed 4-bit matrix: (w_up [rows][in/4], w_lo [rows][in/8]
+    or None). w_up alone is the 2-bit matrix; w_up with w_lo the 3-bit one."""
+    rows, half = w_packed.shape
+    in_dim = 2 * half
+    w_up = torch.empty((rows, in_dim // 4), dtype=torch.uint8, device=w_packed.device)
+    w_lo = torch.empty((rows, in_dim // 8), dtype=torch.uint8, device=w_packed.device) if with_lowest else None
+    _check("q4a_lowbit_pack", _lib.q4a_lowbit_pack(
+        _dev(w_up, "w_up", _U8), ctypes.c_void_p(0) if w_lo is None else _dev(w_lo, "w_lo", _U8),
+        _dev(w_packed, "w_packed", _U8), rows, in_dim, _stream(stream)))
+    return w_up, w_lo
+
+
+def gemv_lowbit(bits: int, w_up, w_lo, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = W.x with W from derived 2-bit (bits=2, w_lo unused) or 3-bit codes."""
+    out_dim = w_up.shape[0]
+    nb, in_dim = x.shape
+    if out is None:
+        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
+    lo = ctypes.c_void_p(0) if (w_lo is None or bits == 2) else _dev(w_lo, "w_lo", _U8)
+    _check("q4a_gemv_lowbit", _lib.q4a_gemv_lowbit(
+        _dev(out, "y", _F32), int(bits), _dev(w_up, "w_up", _U8), lo, _dev(s, "s", _BF16),
+        _dev(b, "b", _BF16), _dev(x, "x", _F16), nb, out_dim, in_dim, _stream(stream)))
     return out
 
 

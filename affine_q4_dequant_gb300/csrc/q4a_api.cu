@@ -72,6 +72,14 @@ q4a_status q4a_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64
     return launch_pack(w_packed, codes, rows, in_dim, (cudaStream_t)stream);
 }
 
+q4a_status q4a_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_packed, int64_t rows, int64_t in_dim,
+                           q4a_stream_t stream) {
+    if (!w_up || !w_packed) return Q4A_ERR_NULL;
+    if (rows < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (!aligned(w_packed, 16) || !aligned(w_up, 16) || (w_lo && !aligned(w_lo, 16))) return Q4A_ERR_ALIGN;
+    return launch_lowbit_pack(w_up, w_lo, w_packed, rows, in_dim, (cudaStream_t)stream);
+}
+
 q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_dim, q4a_stream_t stream) {
     if (!xsum || !x) return Q4A_ERR_NULL;
     if (nb < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
@@ -122,6 +130,38 @@ extern "C" {
 q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
                     const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
     return gemv_common(y, w, s, b, x, nb, out_dim, in_dim, false, 1.0f, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_lowbit(float* y, int bits, const uint8_t* w_up, const uint8_t* w_lo, const uint16_t* s,
+                           const uint16_t* b, const uint16_t* x, int nb, int64_t out_dim, int64_t in_dim,
+                           q4a_stream_t stream) {
+    if (bits != 2 && bits != 3) return Q4A_ERR_UNSUPPORTED;
+    if (!y || !w_up || !s || !b || !x || (bits == 3 && !w_lo)) return Q4A_ERR_NULL;
+    if (nb < 1) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if (bits == 3 && in_dim % 128 != 0) return Q4A_ERR_SHAPE;   // lowest-bit rows: 16-byte multiples
+    if (!aligned(w_up, 16) || (w_lo && !aligned(w_lo, 16)) || !aligned(x, 16) || !aligned(s, 2) ||
+        !aligned(b, 2) || !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
+    GemvLaunch L = {};
+    L.w = w_up;
+    L.w_lo = bits == 3 ? w_lo : nullptr;
+    L.code_bits = bits;
+    L.tensor_rows = out_dim;
+    L.s = s;
+    L.b = b;
+    L.x = x;
+    L.y = y;
+    L.out_dim = out_dim;
+    L.in_dim = in_dim;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb < 32 ? nb : 32;
+    return launch_gemv(L, (cudaStream_t)stream);
 }
 
 q4a_status q4a_gemv_silu(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,

@@ -54,6 +54,37 @@ __global__ void pack_kernel(uint4* __restrict__ out, const uint4* __restrict__ i
     grid_dep_launch();
 }
 
+// Derived low-bit codes, one thread per 32-code chunk: 16 bytes of nibbles in, the chunk's
+// two words of 2-bit codes q4 >> 2 out, and (when wlo is set) its word of lowest bits of the
+// 3-bit codes q4 >> 1. Byte b of word t holds in bit field j the code of element
+// 2 * (8t + 4 * (j & 1) + b) + (j >> 1); the lowest bit of that element is bit 4t + j of
+// byte b of the lowest-bit word.
+__global__ void lowbit_pack_kernel(uint2* __restrict__ w2, uint32_t* __restrict__ wlo,
+                                   const uint4* __restrict__ in, int64_t n_chunks) {
+    grid_dep_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_chunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 a = ld_nc_16(in + i);
+        const uint32_t src[4] = {a.x, a.y, a.z, a.w};   // byte k: element 2k (low), 2k + 1 (high)
+        uint32_t up[2] = {0u, 0u}, lo = 0u;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = 2 * (8 * t + 4 * (j & 1) + b) + (j >> 1);
+                    const uint32_t q = (src[e >> 3] >> (8 * ((e >> 1) & 3) + 4 * (e & 1))) & 15u;
+                    up[t] |= (q >> 2) << (8 * b + 2 * j);
+                    lo |= ((q >> 1) & 1u) << (8 * b + 4 * t + j);
+                }
+        w2[i] = make_uint2(up[0], up[1]);
+        if (wlo) wlo[i] = lo;
+    }
+    __threadfence();
+    grid_dep_launch();
+}
+
 // One thread per (row, group): 8 vectors of 8 halves summed in fp32 in index order.
 __global__ void xsum_kernel(float* __restrict__ xsum, const __half* __restrict__ x, int64_t n_groups_total) {
     grid_dep_wait();
@@ -234,6 +265,13 @@ q4a_status launch_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, in
     const int64_t n_out_vec = rows * in_dim / 32;
     return launch_pdl(pack_kernel, grid_for(n_out_vec, 256), 256, stream, reinterpret_cast<uint4*>(w_packed),
                       reinterpret_cast<const uint4*>(codes), n_out_vec);
+}
+
+q4a_status launch_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_packed, int64_t rows,
+                              int64_t in_dim, cudaStream_t stream) {
+    const int64_t n = rows * in_dim / 32;
+    return launch_pdl(lowbit_pack_kernel, grid_for(n, 256), 256, stream, reinterpret_cast<uint2*>(w_up),
+                      reinterpret_cast<uint32_t*>(w_lo), reinterpret_cast<const uint4*>(w_packed), n);
 }
 
 q4a_status launch_xsum(float* xsum, const uint16_t* x, int64_t nb, int64_t in_dim, cudaStream_t stream) {

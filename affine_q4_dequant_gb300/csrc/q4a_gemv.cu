@@ -48,6 +48,12 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -141,9 +147,16 @@ __device__ __forceinline__ bool next_job(const P& p, int& t, int t_end, Job& j) 
 // 32+8t..32+8t+7 of group gl for activation row tok; the four t of an item sit in one
 // lane quad, which sums its group. Each batch issues all of its global loads before
 // any arithmetic, so the staging costs about one memory latency per batch.
-template <int NT, bool RMS, class P>
+//
+// Derived low-bit codes (CB = 2 or 3) pair lane quad t with the 16 consecutive inputs
+// 16t..16t+15 of a group (the 2-bit word t of the group's 16 bytes holds exactly those), and
+// step j with the inputs whose codes sit in bit field j of the word's bytes: the even inputs
+// 16t + {0,2,4,6} (j = 0) and 16t + {8,10,12,14} (j = 1), the odd ones after them (j = 2, 3);
+// field j is read in place (value 4^j * code), so step j's activations are scaled by 4^-j.
+template <int NT, bool RMS, int CB, class P>
 __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                         float* xsum_s, const float* inv_s, int ctid) {
+    static_assert(CB == 4 || !RMS, "the RMSNorm prologue is built for 4-bit codes only");
     constexpr int NTOK = NT * 8;
     constexpr int BATCH = RMS ? 2 : 4;
     constexpr int NTH = kConsumerWarps * 32;
@@ -165,11 +178,11 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
             if (on) {
                 const int slot = sg.tok0 + tok;
                 const int64_t src = p.x_rows ? (int64_t)p.x_rows[slot] : (int64_t)slot;
-                const int64_t col = (int64_t)(kg0 + gl) * kGroup + 8 * (i & 3);
+                const int64_t col = (int64_t)(kg0 + gl) * kGroup + (CB == 4 ? 8 : 16) * (i & 3);
                 if constexpr (!RMS) {
                     const __half* xr = static_cast<const __half*>(p.x) + src * p.in_dim + col;
                     ld[k][0] = ld_nc_16(xr);
-                    ld[k][1] = ld_nc_16(xr + 32);
+                    ld[k][1] = ld_nc_16(xr + (CB == 4 ? 32 : 8));
                 } else {
                     const float* xr = static_cast<const float*>(p.x) + src * p.in_dim + col;
                     ld[k][0] = ld_nc_16(xr);
@@ -217,6 +230,29 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
             float part = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) part += half2_sum(v[q]) + half2_sum(u[q]);
+            if constexpr (CB != 4) {
+                // v: inputs 16t + 0..7, u: 16t + 8..15 (pairs). Step j, fragment b0 = k-low
+                // (code bytes 0 and 2), b1 = k-high (bytes 1 and 3).
+                const uint32_t sc1 = 0x34003400u, sc2 = 0x2C002C00u, sc3 = 0x24002400u;   // 4^-1, 4^-2, 4^-3
+                uint32_t bfr[8];
+                bfr[0] = __byte_perm(v[0], v[2], 0x5410);                     // j0: x0, x4
+                bfr[1] = __byte_perm(v[1], v[3], 0x5410);                     //     x2, x6
+                bfr[2] = hmul2_u32(__byte_perm(u[0], u[2], 0x5410), sc1);     // j1: x8, x12
+                bfr[3] = hmul2_u32(__byte_perm(u[1], u[3], 0x5410), sc1);     //     x10, x14
+                bfr[4] = hmul2_u32(__byte_perm(v[0], v[2], 0x7632), sc2);     // j2: x1, x5
+                bfr[5] = hmul2_u32(__byte_perm(v[1], v[3], 0x7632), sc2);     //     x3, x7
+                bfr[6] = hmul2_u32(__byte_perm(u[0], u[2], 0x7632), sc3);     // j3: x9, x13
+                bfr[7] = hmul2_u32(__byte_perm(u[1], u[3], 0x7632), sc3);     //     x11, x15
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                if (live) {
+                    uint8_t* f = xfrag + ((size_t)(gl * 2) * ntm + tok) * 64 + t * 16;
+                    *reinterpret_cast<uint4*>(f) = make_uint4(bfr[0], bfr[1], bfr[2], bfr[3]);
+                    *reinterpret_cast<uint4*>(f + (size_t)ntm * 64) = make_uint4(bfr[4], bfr[5], bfr[6], bfr[7]);
+                    if (t == 0) xsum_s[gl * NTOK + tok] = part * 5.9604644775390625e-08f;
+                }
+                continue;
+            }
             // B fragments for the 4 mma steps: step j pairs element j with j+4 (v: word t,
             // u: word t+4). Odd steps come from the high nibbles (16x) -> scale by 1/16.
             uint32_t b01[4], b23[4];
@@ -322,7 +358,9 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
 
 // ---- the kernel --------------------------------------------------------------------------
 
-template <int NT, bool RMS, int MAXSEG>
+// CB: code bits. 4: packed nibbles. 2: derived 2-bit codes q4 >> 2, w = (4 q + 1.5) s + b.
+// 3: derived 3-bit codes q4 >> 1 = 2 * (2-bit upper part) + lowest bit, w = (2 q + 0.5) s + b.
+template <int NT, bool RMS, int MAXSEG, int CB = 4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> p) {
     constexpr int NTOK = NT * 8;
@@ -522,18 +560,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = ring + (size_t)s * L.stage_bytes;
                 const int g0 = kg0 + ks * kStageGroups;
                 const int ng = min(kStageGroups, kg1 - g0);
-                const int nbox = (ng + 3) / 4;
+                // box columns of 128 bytes: 4 groups of nibbles, 8 groups of 2-bit codes
+                const int nbox = CB == 4 ? (ng + 3) / 4 : 1;
                 if (lane == 0) {
                     // One tall box per box column for each power-of-two run of tiles: the
                     // TMA engine pays per box, so few large boxes keep HBM streaming.
-                    mbar_arrive_expect_tx(full, (uint32_t)(j.ntile * nbox * kTileBytes));
+                    mbar_arrive_expect_tx(full, (uint32_t)(j.ntile * (nbox * kTileBytes + (CB == 3 ? kLoTileBytes : 0))));
                     int m0 = 0;
                     for (int lg = kNumMaps - 1; lg >= 0; --lg) {
                         const int h = 1 << lg;
                         if (j.ntile - m0 < h) continue;
                         for (int c = 0; c < nbox; ++c)
                             tma_load_2d(smem_addr(st + (c * MT + m0) * kTileBytes), &p.tmap_w[lg],
-                                        (g0 + 4 * c) * 32, (int)(trow0 + 16 * m0), full);
+                                        CB == 4 ? (g0 + 4 * c) * 32 : g0 * 16, (int)(trow0 + 16 * m0), full);
+                        if constexpr (CB == 3)   // lowest bits: 8 bytes per group and row
+                            tma_load_2d(smem_addr(st + MT * kTileBytes + m0 * kLoTileBytes), &p.tmap_lo[lg], g0 * 8,
+                                        (int)(trow0 + 16 * m0), full);
                         m0 += h;
                     }
                 }
@@ -581,9 +623,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ldmatrix: rows 0-7 / 8-15 of a tile, 16-byte granules 2*(wg&3) and 2*(wg&3)+1 of
         // its box column; 128-byte swizzle granule ^= row & 7.
         const uint32_t lrow = (uint32_t)((lane & 7) + ((lane >> 3) & 1) * 8);
-        const uint32_t lgran = (uint32_t)(wg & 3) * 2 + (uint32_t)(lane >> 4);
+        // 4-bit: lanes 16-31 address the group's second granule; low-bit: the next tile
+        const uint32_t lgran = CB == 4 ? (uint32_t)(wg & 3) * 2 + (uint32_t)(lane >> 4) : (uint32_t)wg;
         const uint32_t ldsm_base = smem_addr(ring) + lrow * 128 + ((lgran ^ (lrow & 7)) << 4) +
-                                   (uint32_t)(((wg >> 2) * MT) * kTileBytes);
+                                   (CB == 4 ? (uint32_t)(((wg >> 2) * MT) * kTileBytes)
+                                            : (uint32_t)(lane >> 4) * (uint32_t)kTileBytes);
+        // 3-bit: this lane's lowest-bit word (chunk tq/2 of group wg, row g), shifted so that
+        // the bits of its half (word tq & 1 of the upper codes) sit at bits j of each byte
+        const uint32_t lo_base = smem_addr(ring) + (uint32_t)(MT * kTileBytes) + (uint32_t)g * 64u +
+                                 (uint32_t)wg * 8u + (uint32_t)(tq >> 1) * 4u;
+        const uint32_t lo_shift = 4u * (uint32_t)(tq & 1);
         // B fragments of group gl, row tok: xfrag + ((gl*2 + jp)*ntok_max + tok)*64 + tq*16
         const uint32_t xf_jp = (uint32_t)p.ntok_max * 64u;
         const uint32_t xf_base = smem_addr(xfrag) + (uint32_t)wg * 2u * xf_jp + (uint32_t)g * 64u + (uint32_t)tq * 16u;
@@ -599,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = p.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid);
+                stage_x<NT, RMS, CB>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
                 consumer_sync();
@@ -625,11 +674,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(smem_addr(full_b + rs), rph, abort_flag);
                 if (wg < min(kStageGroups, gsz - ks * kStageGroups)) {
                     // Slots beyond the row block read stale stage data and are never stored.
-                    uint32_t w[TPW][4];
+                    // 4-bit: w[mi][0..3] = rows g, g+8 of granule 0, then of granule 1 (8 nibbles each).
+                    // Low-bit: w[mi][0], w[mi][1] = rows g, g+8 (16 codes each), two tiles per ldmatrix.
+                    uint32_t w[TPW][CB == 4 ? 4 : 2];
                     const uint32_t st = ldsm_base + (uint32_t)rs * L.stage_bytes;
+                    if constexpr (CB == 4) {
 #pragma unroll
-                    for (int mi = 0; mi < TPW; ++mi)
-                        ldsm_x4(st + (uint32_t)(mi * kTileBytes), w[mi][0], w[mi][1], w[mi][2], w[mi][3]);
+                        for (int mi = 0; mi < TPW; ++mi)
+                            ldsm_x4(st + (uint32_t)(mi * kTileBytes), w[mi][0], w[mi][1], w[mi][2], w[mi][3]);
+                    } else {
+#pragma unroll
+                        for (int mi = 0; mi < TPW; mi += 2)
+                            ldsm_x4(st + (uint32_t)(mi * kTileBytes), w[mi][0], w[mi][1], w[mi + 1][0], w[mi + 1][1]);
+                    }
+                    uint32_t lw[TPW][2];   // 3-bit: the lowest-bit words of rows g, g+8
+                    if constexpr (CB == 3) {
+                        const uint32_t lb = lo_base + (uint32_t)rs * L.stage_bytes;
+#pragma unroll
+                        for (int mi = 0; mi < TPW; ++mi) {
+                            lw[mi][0] = lds_u32(lb + (uint32_t)(mi * kLoTileBytes)) >> lo_shift;
+                            lw[mi][1] = lds_u32(lb + (uint32_t)(mi * kLoTileBytes + 8 * 64)) >> lo_shift;
+                        }
+                    }
                     uint32_t bf[NT][8];
                     const uint32_t xf = xf_base + (uint32_t)ks * xf_stage;
 #pragma unroll
@@ -650,16 +716,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int mi = 0; mi < TPW; ++mi) {
                         // The mma partial sums are sum(q x) * 2^-24; s multiplies them as is and
                         // the result is multiplied by 2^24 once at the end (no scale overflows).
-                        const float s0 = bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes)));
-                        const float s1 = bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes + 1024)));
+                        // Low-bit codes: the steps compute sum(q x) / (4 or 2); the scale restores it.
+                        constexpr float kq = CB == 4 ? 1.0f : (CB == 2 ? 4.0f : 2.0f);
+                        const float s0 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes)));
+                        const float s1 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes + 1024)));
+                        // h[a][jj]: mma step jj's A register a (a0/a2: row g, a1/a3: row g+8)
                         uint32_t h[4][4];
+                        if constexpr (CB == 4) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t v8 = w[mi][k] >> 8;
-                            h[k][0] = w[mi][k] & 0x000F000Fu;
-                            h[k][1] = w[mi][k] & 0x00F000F0u;
-                            h[k][2] = v8 & 0x000F000Fu;
-                            h[k][3] = v8 & 0x00F000F0u;
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t v8 = w[mi][k] >> 8;
+                                h[k][0] = w[mi][k] & 0x000F000Fu;
+                                h[k][1] = w[mi][k] & 0x00F000F0u;
+                                h[k][2] = v8 & 0x000F000Fu;
+                                h[k][3] = v8 & 0x00F000F0u;
+                            }
+                        } else if constexpr (CB == 2) {
+                            // field jj of bytes 0, 2 (k-low) and of bytes 1, 3 (k-high), in place
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const uint32_t v8 = w[mi][r] >> 8;
+#pragma unroll
+                                for (int jj = 0; jj < 4; ++jj) {
+                                    h[r][jj] = w[mi][r] & (0x00030003u << (2 * jj));
+                                    h[2 + r][jj] = v8 & (0x00030003u << (2 * jj));
+                                }
+                            }
+                        } else {
+                            // code = 2 * upper + lowest, assembled in bits 2jj .. 2jj+2 of each half:
+                            // the upper field moved up one bit, the lowest bit (bit jj of the byte
+                            // once the lane's word half is shifted down) moved to bit 2jj
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const uint32_t u1 = w[mi][r] << 1, u7 = w[mi][r] >> 7;
+                                const uint32_t l = lw[mi][r];
+#pragma unroll
+                                for (int jj = 0; jj < 4; ++jj) {
+                                    const uint32_t mu = 0x00060006u << (2 * jj), ml = 0x00010001u << (2 * jj);
+                                    h[r][jj] = (u1 & mu) | ((l << jj) & ml);
+                                    h[2 + r][jj] = (u7 & mu) | ((l >> (8 - jj)) & ml);
+                                }
+                            }
                         }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -710,6 +807,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int nt = 0; nt < NT; ++nt) {
                             mma_bf16(acc[mi][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
                             mma_bf16(acc[mi][nt], a0, a1, a2, a3, bx[nt][2], bx[nt][3]);
+                        }
+                        if constexpr (CB != 4) {
+                            // the reconstruction offset: + (1.5 or 0.5) * sum_g s[o][g] * xsum[r][g]
+                            constexpr float koff = CB == 2 ? 1.5f : 0.5f;
+                            ldsm_x4(boff - (uint32_t)L.sb_pitch + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                float d2[4] = {0.f, 0.f, 0.f, 0.f};
+                                mma_bf16(d2, a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                                mma_bf16(d2, a0, a1, a2, a3, bx[nt][2], bx[nt][3]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) acc[mi][nt][e] = fmaf(koff, d2[e], acc[mi][nt][e]);
+                            }
                         }
                     }
                 }
@@ -848,9 +958,9 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG>
+template <int NT, bool RMS, int MAXSEG, int CB = 4>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -889,8 +999,18 @@ int occupancy_clusters(int cluster, uint32_t smem_bytes) {
 }
 
 template <int MAXSEG>
-int cluster_capacity_t(int nt, bool rms, int cluster, uint32_t smem_bytes) {
+int cluster_capacity_t(int nt, bool rms, int cluster, uint32_t smem_bytes, int cb) {
     if constexpr (MAXSEG == kDenseMaxSeg) {
+        if (cb == 2) {
+            if (nt == 1) return occupancy_clusters<1, false, MAXSEG, 2>(cluster, smem_bytes);
+            if (nt == 2) return occupancy_clusters<2, false, MAXSEG, 2>(cluster, smem_bytes);
+            return occupancy_clusters<4, false, MAXSEG, 2>(cluster, smem_bytes);
+        }
+        if (cb == 3) {
+            if (nt == 1) return occupancy_clusters<1, false, MAXSEG, 3>(cluster, smem_bytes);
+            if (nt == 2) return occupancy_clusters<2, false, MAXSEG, 3>(cluster, smem_bytes);
+            return occupancy_clusters<4, false, MAXSEG, 3>(cluster, smem_bytes);
+        }
         if (rms) {
             if (nt == 1) return occupancy_clusters<1, true, MAXSEG>(cluster, smem_bytes);
             if (nt == 2) return occupancy_clusters<2, true, MAXSEG>(cluster, smem_bytes);
@@ -902,14 +1022,14 @@ int cluster_capacity_t(int nt, bool rms, int cluster, uint32_t smem_bytes) {
     return occupancy_clusters<4, false, MAXSEG>(cluster, smem_bytes);
 }
 
-int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_bytes) {
-    return experts ? cluster_capacity_t<Q4A_MAX_SEGMENTS>(nt, rms, cluster, smem_bytes)
-                   : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes);
+int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_bytes, int cb) {
+    return experts ? cluster_capacity_t<Q4A_MAX_SEGMENTS>(nt, rms, cluster, smem_bytes, 4)
+                   : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG>
+template <int NT, bool RMS, int MAXSEG, int CB = 4>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -923,7 +1043,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.n_tiles ? max_clusters : prm.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
@@ -951,6 +1071,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
 
     const int nt = L.max_ntok <= 8 ? 1 : (L.max_ntok <= 16 ? 2 : 4);
     const int mt = tiles_per_block(nt);
+    const int cb = L.code_bits;
+    if (cb != 4 && (L.experts || L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
     const int G = (int)(L.in_dim / kGroup);
 
     // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
@@ -984,14 +1106,14 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         if (c > 1 && sbm_full != kSbTma) return false;
         if (c > 1 && (int64_t)g * (c - 1) >= G) return false;
         if (xfrag_bytes(g, ntm) > (uint32_t)kXFragBudget) return false;
-        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c)).total + 1024) <= di.max_smem_optin;
+        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c), cb).total + 1024) <= di.max_smem_optin;
     };
     int C = 0;
     for (int c = 1; c <= 8; c *= 2) {
         if (!fits(c, 3)) continue;
         if (C == 0) C = c;                       // smallest that fits at all
         const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
-                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c)).total + 1024);
+                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb).total + 1024, cb);
         if (q <= 0) continue;
         if (n_tiles >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
             C = c;
@@ -1004,12 +1126,15 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     int stages = 8;
     while (stages > 2 && !fits(C, stages)) --stages;
     if (!fits(C, stages)) return Q4A_ERR_UNSUPPORTED;
-    const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C));
+    const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C), cb);
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
     memset(&prm, 0, sizeof(prm));
-    const cuuint64_t dims[2] = {(cuuint64_t)(L.in_dim / 2), (cuuint64_t)L.tensor_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)(L.in_dim / 2)};
+    // packed codes: in_dim/2 bytes per row (nibbles) or in_dim/4 (2-bit codes; the 3-bit
+    // codes' upper two bits); the 3-bit lowest-bit plane: in_dim/8 bytes per row
+    const int64_t wrow = cb == 4 ? L.in_dim / 2 : L.in_dim / 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)wrow, (cuuint64_t)L.tensor_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)wrow};
     const cuuint32_t estr[2] = {1u, 1u};
     for (int i = 0; i < kNumMaps; ++i) {
         const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)(16 << i)};
@@ -1017,6 +1142,15 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        if (cb == 3) {
+            const cuuint64_t ldims[2] = {(cuuint64_t)(L.in_dim / 8), (cuuint64_t)L.tensor_rows};
+            const cuuint64_t lstrides[1] = {(cuuint64_t)(L.in_dim / 8)};
+            const cuuint32_t lbox[2] = {64u, (cuuint32_t)(16 << i)};
+            r = enc(&prm.tmap_lo[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w_lo), ldims, lstrides,
+                    lbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        }
     }
 
     prm.s = L.s;
@@ -1074,6 +1208,16 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
 
     const uint32_t smem_bytes = lay.total + 1024;
     if constexpr (MAXSEG == kDenseMaxSeg) {
+        if (cb == 2) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 2>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 2>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 2>(prm, smem_bytes, stream);
+        }
+        if (cb == 3) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 3>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 3>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 3>(prm, smem_bytes, stream);
+        }
         if (L.rmsnorm) {
             if (nt == 1) return launch_variant<1, true, MAXSEG>(prm, smem_bytes, stream);
             if (nt == 2) return launch_variant<2, true, MAXSEG>(prm, smem_bytes, stream);

@@ -48,7 +48,9 @@ struct Segment {
 
 // Shared-memory carve-up, identical on host and device.
 struct SmemLayout {
-    uint32_t stage_bytes;   // one ring stage: mt tiles x 2 box columns x 2 KB of packed weights
+    uint32_t stage_bytes;   // one ring stage of packed codes: 4-bit: mt tiles x 2 box columns
+                            // x 2 KB; 2-bit: one box column; 3-bit: one box column (upper
+                            // two bits), then mt x 1 KB of lowest-bit words ([tile][row][64 B])
     uint32_t ring, xfrag, xsum, xbias, sb, sb_pitch, sb_buf, n_sb, wpart, cpart, ssq, raw, raw_elems, bars, total;
     // raw, raw_elems: the raw mode's staging buffers [2 buffers][scales | biases][raw_elems] bf16
     // sb_pitch: bytes of one row block's scales (the biases follow); sb_buf: both
@@ -72,11 +74,16 @@ __host__ __device__ inline uint32_t sb_bytes(int /*sb_mode*/, int gs, int rows) 
     return (uint32_t)((gs + 63) / 64) * rows * 128u;
 }
 
+// Bytes of the lowest-bit words of one 16-row tile in a ring stage (3-bit codes): 8 groups x
+// 8 bytes per row.
+constexpr uint32_t kLoTileBytes = 16u * 64u;
+
 __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, int gs, int ntok_max,
-                                                  int sb_mode, int sb_bufs) {
+                                                  int sb_mode, int sb_bufs, int code_bits = 4) {
     SmemLayout L;
     const uint32_t ntok = 8u * nt, rows = 16u * mt;
-    L.stage_bytes = (uint32_t)mt * 2u * kTileBytes;        // [box column][rows][128 B]
+    L.stage_bytes = (uint32_t)mt * (code_bits == 4 ? 2u : 1u) * kTileBytes +   // [box column][rows][128 B]
+                    (code_bits == 3 ? (uint32_t)mt * kLoTileBytes : 0u);
     L.ring = 0;                                             // relative to a 1024-aligned base
     L.xfrag = L.ring + (uint32_t)stages * L.stage_bytes;
     L.xsum = L.xfrag + align_up(xfrag_bytes(gs, ntok_max), 16);
@@ -105,6 +112,8 @@ struct GemvParams {
     CUtensorMap tmap_b[kNumMaps];  // box 64 groups x (16 << i) rows, 128-byte swizzle
     CUtensorMap tmap_s1;           // raw mode: 1D bf16 views of s and b (rows * groups
     CUtensorMap tmap_b1;           // elements), box kRawBox elements
+    CUtensorMap tmap_lo[kNumMaps]; // 3-bit codes: lowest-bit plane, dim0 = in_dim/8 bytes,
+                                   // box 64 bytes x (16 << i) rows, no swizzle
     const uint16_t* s;        // bf16 [rows][G]
     const uint16_t* b;
     const void* x;            // fp16 [*][in_dim] (or fp32 x_raw for the RMSNorm variant)
@@ -149,6 +158,8 @@ struct GemvLaunch {
     bool silu;                // output epilogue y -> silu(y / silu_div)
     float silu_div;
     int norm_groups;          // RMSNorm variant: normalisation segments per row (>= 1)
+    int code_bits = 4;        // 4 (w: packed nibbles), 2 or 3 (w: 2-bit codes [rows][in/4],
+    const uint8_t* w_lo = nullptr;  // w_lo: the 3-bit codes' lowest-bit plane [rows][in/8])
     bool experts;
     int nseg;
     const Segment* seg;
@@ -160,6 +171,8 @@ q4a_status launch_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, in
                        cudaStream_t stream);
 q4a_status launch_xsum(float* xsum, const uint16_t* x, int64_t nb, int64_t in_dim,
                        cudaStream_t stream);
+q4a_status launch_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_packed, int64_t rows,
+                              int64_t in_dim, cudaStream_t stream);
 q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,
                                 int64_t inter, cudaStream_t stream);
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim,

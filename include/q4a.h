@@ -107,6 +107,37 @@ Q4A_API q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const
                     q4a_stream_t stream);
 
 /*
+ * q4a_lowbit_pack -- derived low-bit codes of a packed 4-bit matrix ("BATCH_MSL",
+ * quantized_rows.metal fn_q2_rows_h and fn_q3_rows_h: codes q4 >> 2 and q4 >> 1).
+ *   w_up      out  uint8 [rows][in_dim/4]: the 2-bit codes q4 >> 2 (also the upper two bits of
+ *                  the 3-bit codes). Per 32-code chunk two little-endian 32-bit words; byte b
+ *                  of word t holds in bits 2j+1:2j the code of element 2(8t + 4(j&1) + b) + (j>>1)
+ *                  of the chunk (the layout the 2-bit kernel's masked casts read).
+ *   w_lo      out  uint8 [rows][in_dim/8] or NULL: the lowest bits of the 3-bit codes,
+ *                  (q4 >> 1) & 1, one word per chunk, the bit of the element in field j of byte
+ *                  b of word t at bit 4t + j of byte b. (The pages interleave the three words
+ *                  of a chunk; this library keeps the lowest-bit words as their own plane.)
+ *   w_packed  in   uint8 [rows][in_dim/2], packed as q4a_pack writes it
+ *   Requires rows >= 1, in_dim % 64 == 0, every pointer 16-byte aligned. The caller owns all
+ *   buffers; nothing is allocated.
+ */
+Q4A_API q4a_status q4a_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_packed, int64_t rows,
+                                   int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_gemv_lowbit -- y = W.x with W from derived low-bit codes ("BATCH_MSL", quantized_rows.metal
+ * fn_q2_rows_h, fn_q3_rows_h): the quad midpoint w = (4 q2 + 1.5) s + b for bits = 2, and
+ * w = (2 q3 + 0.5) s + b with q3 = 2 * upper + lowest for bits = 3.
+ *   bits       2 or 3 (else Q4A_ERR_UNSUPPORTED)
+ *   w_up, w_lo as q4a_lowbit_pack writes them (w_lo ignored for bits = 2, required for 3)
+ *   y, s, b, x, nb, out_dim, in_dim as q4a_gemv; bits = 3 also needs in_dim % 128 == 0.
+ *   Any nb >= 1 up to 256 runs on the GEMV kernel (no tensor-core path for low-bit codes).
+ */
+Q4A_API q4a_status q4a_gemv_lowbit(float* y, int bits, const uint8_t* w_up, const uint8_t* w_lo,
+                                   const uint16_t* s, const uint16_t* b, const uint16_t* x, int nb,
+                                   int64_t out_dim, int64_t in_dim, q4a_stream_t stream);
+
+/*
  * q4a_gemv_silu -- q4a_gemv whose outputs go through silu(y / div) on the way out
  * ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b: the gated-residual bottleneck):
  *     y[r][o] = v / (1 + e^-v),  v = (W.x)[r][o] / div

@@ -37,6 +37,8 @@ def lib():
     lib.q4a_moe_combine.argtypes = [P, P, P, P, I32, I32, I64, I64, P, P, P, P]
     lib.q4a_gemv_silu.argtypes = [P, P, P, P, P, F, I32, I64, I64, P]
     lib.q4a_gemv_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
+    lib.q4a_lowbit_pack.argtypes = [P, P, P, I64, I64, P]
+    lib.q4a_gemv_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, I64, I64, P]
     return lib
 
 
@@ -171,4 +173,21 @@ def test_rmsnorm_grouped_rejections(lib):
     assert f(A, A, A, A, A, A, 1e-6, 0.0, 2, 33, 64, 512, None) == UNSUP     # nb > 32
     assert f(A, A, A, A, A, A, -1.0, 0.0, 2, 1, 64, 512, None) == SHAPE      # eps < 0
     assert f(A, A, A, A, A + 4, A, 1e-6, 0.0, 2, 1, 64, 512, None) == ALIGN  # x_raw
+
+
+def test_lowbit_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_lowbit_pack
+    assert f(None, None, A, 4, 64, None) == NULL
+    assert f(A, None, A, 0, 64, None) == SHAPE
+    assert f(A, None, A, 4, 96, None) == SHAPE
+    assert f(A + 8, None, A, 4, 64, None) == ALIGN
+    assert f(A, A + 4, A, 4, 64, None) == ALIGN
+    g = lib.q4a_gemv_lowbit
+    assert g(A, 4, A, A, A, A, A, 1, 64, 512, None) == UNSUP    # bits
+    assert g(A, 3, A, None, A, A, A, 1, 64, 512, None) == NULL  # 3-bit needs the lowest bits
+    assert g(A, 2, A, None, A, A, A, 0, 64, 512, None) == SHAPE
+    assert g(A, 3, A, A, A, A, A, 1, 64, 576, None) == SHAPE    # 3-bit: in_dim % 128
+    assert g(A, 2, A, None, A, A, A, 257, 64, 512, None) == UNSUP
+    assert g(A, 2, A + 4, None, A, A, A, 1, 64, 512, None) == ALIGN
 
