@@ -42,8 +42,11 @@ BYTES_PER_WEIGHT = 0.5 + 4.0 / 64.0                # codes + bf16 scale and bias
 METRIC = "achieved HBM GB/s (and % of roofline) per q4a_gemv call vs NB; us/decode-layer"
 
 
-def gemv_bytes(out_dim, in_dim, nb, x_bytes_per_el):
-    return out_dim * in_dim * BYTES_PER_WEIGHT + nb * in_dim * x_bytes_per_el + nb * out_dim * 4
+def gemv_bytes(out_dim, in_dim, nb, x_bytes_per_el, bits=4):
+    """Algorithmic bytes of one product: codes (bits / 8 per weight) plus a bf16 scale and
+    bias per 64 weights, the activations and the fp32 outputs."""
+    per_weight = bits / 8.0 + 4.0 / 64.0
+    return out_dim * in_dim * per_weight + nb * in_dim * x_bytes_per_el + nb * out_dim * 4
 
 
 def layer_bytes(nb):
@@ -432,21 +435,30 @@ def run_kernel_mode(args):
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
-    wbytes = out_dim * in_dim * BYTES_PER_WEIGHT
+    wbytes = out_dim * in_dim * (args.bits / 8.0 + 4.0 / 64.0)
     copies = max(2, int(3 * 130e6 // wbytes) + 1)
     ws = []
+    bits = args.bits
     for _ in range(copies):
         codes = torch.randint(0, 16, (out_dim, in_dim), dtype=torch.uint8, device=dev, generator=g)
-        ws.append((q4a.pack(codes), (torch.rand(out_dim, in_dim // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
-                   (torch.randn(out_dim, in_dim // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
+        w4 = q4a.pack(codes)
         del codes
+        # derived low-bit codes (q4 >> 2, q4 >> 1) replace the nibbles when bits < 4
+        wc = (w4, None) if bits == 4 else q4a.lowbit_pack(w4, with_lowest=bits == 3)
+        if bits != 4:
+            del w4
+        ws.append((wc, (torch.rand(out_dim, in_dim // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
+                   (torch.randn(out_dim, in_dim // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
     for nb in [int(v) for v in args.nbs.split(",")]:
         x = torch.randn(nb, in_dim, device=dev, generator=g).half()
         y = torch.empty(nb, out_dim, device=dev)
 
         def call(i):
-            w, s_, b_ = ws[i % copies]
-            q4a.gemv(w, s_, b_, x, out=y)
+            (w, w_lo), s_, b_ = ws[i % copies]
+            if bits == 4:
+                q4a.gemv(w, s_, b_, x, out=y)
+            else:
+                q4a.gemv_lowbit(bits, w, w_lo, s_, b_, x, out=y)
 
         for i in range(3):
             call(i)
@@ -456,8 +468,8 @@ def run_kernel_mode(args):
             for i in range(args.reps):
                 call(3 + i)
             torch.cuda.synchronize()
-            print(json.dumps({"kernel": "q4a_gemv", "shape": f"{in_dim}->{out_dim}", "nb": nb,
-                              "profile_launches": args.reps + 3}), flush=True)
+            print(json.dumps({"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
+                              "shape": f"{in_dim}->{out_dim}", "nb": nb, "profile_launches": args.reps + 3}), flush=True)
             continue
         n = copies * max(1, args.reps // copies)
         graph = torch.cuda.CUDAGraph()
@@ -475,9 +487,10 @@ def run_kernel_mode(args):
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1) / n * 1e3)
         us = statistics.median(times)
-        nbytes = gemv_bytes(out_dim, in_dim, nb, 2)
+        nbytes = gemv_bytes(out_dim, in_dim, nb, 2, bits)
         peak, kind = load_peaks()
-        print(json.dumps({"kernel": "q4a_gemv", "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us,
+        print(json.dumps({"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
+                          "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us,
                           "gbs": nbytes / us / 1e3, "frac_of_peak": nbytes / us / 1e3 / peak, "peak": peak,
                           "peak_kind": kind, "weights_per_s": out_dim * in_dim / (us * 1e-6),
                           "launches_timed": n, "weight_copies": copies}), flush=True)
@@ -644,6 +657,8 @@ def main():
     ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe"], default=None,
                     help="time one GEMV shape per launch instead of the decode-layer step")
     ap.add_argument("--reps", type=int, default=60)
+    ap.add_argument("--bits", type=int, choices=[4, 3, 2], default=4,
+                    help="with --kernel: code width (3 and 2: derived low-bit codes, q4a_gemv_lowbit)")
     ap.add_argument("--profile", action="store_true",
                     help="with --kernel: eager launches only (a target for ncu), no timing")
     args = ap.parse_args()
