@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "q4a_gemv": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_silu": (I32, [P, P, P, P, P, F, I32, I64, I64, P]),
         "q4a_lowbit_pack": (I32, [P, P, P, I64, I64, P]),
+        "q4a_gemv_gate_up_silu": (I32, [P, P, P, P, P, I32, I64, I64, P]),
+        "q4a_gemv_rmsnorm_gate_up_silu": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
@@ -115,6 +117,32 @@ def pack(codes: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> t
         out = torch.empty((rows, in_dim // 2), dtype=torch.uint8, device=codes.device)
     _check("q4a_pack", _lib.q4a_pack(_dev(out, "out", _U8), _dev(codes, "codes", _U8), rows, in_dim,
                                      _stream(stream)))
+    return out
+
+
+def gemv_gate_up_silu(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h = fp16(silu(W_gate x) * (W_up x)); w holds the gate rows, then the up rows."""
+    nb, in_dim = x.shape
+    inter = w.shape[0] // 2
+    if out is None:
+        out = torch.empty((nb, inter), dtype=torch.float16, device=x.device)
+    _check("q4a_gemv_gate_up_silu", _lib.q4a_gemv_gate_up_silu(
+        _dev(out, "h", _F16), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
+        _dev(x, "x", _F16), nb, inter, in_dim, _stream(stream)))
+    return out
+
+
+def gemv_rmsnorm_gate_up_silu(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gemv_gate_up_silu on RMS-normalised fp32 activations (one normalisation group)."""
+    nb, in_dim = x_raw.shape
+    inter = w.shape[0] // 2
+    if out is None:
+        out = torch.empty((nb, inter), dtype=torch.float16, device=x_raw.device)
+    _check("q4a_gemv_rmsnorm_gate_up_silu", _lib.q4a_gemv_rmsnorm_gate_up_silu(
+        _dev(out, "h", _F16), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
+        _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift), nb, inter,
+        in_dim, _stream(stream)))
     return out
 
 

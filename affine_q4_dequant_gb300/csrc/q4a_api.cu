@@ -206,6 +206,67 @@ q4a_status q4a_gemv_rmsnorm_grouped(float* y, const uint8_t* w, const uint16_t* 
     return launch_gemv(L, (cudaStream_t)stream);
 }
 
+q4a_status q4a_gemv_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                                 const uint16_t* x, int nb, int64_t inter, int64_t in_dim, q4a_stream_t stream) {
+    if (!h || !w || !s || !b || !x) return Q4A_ERR_NULL;
+    if (nb < 1 || inter < 1 || inter % 16 != 0) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(2 * inter, in_dim);
+    if (st != Q4A_OK) return st;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(h, 2))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
+    GemvLaunch L = {};
+    L.w = w;
+    L.tensor_rows = 2 * inter;
+    L.s = s;
+    L.b = b;
+    L.x = x;
+    L.h = h;
+    L.fused_gate_up = true;
+    L.out_dim = inter;
+    L.in_dim = in_dim;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb < 32 ? nb : 32;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                                         const float* x_raw, const uint16_t* norm_w, float eps, float shift,
+                                         int nb, int64_t inter, int64_t in_dim, q4a_stream_t stream) {
+    if (!h || !w || !s || !b || !x_raw || !norm_w) return Q4A_ERR_NULL;
+    if (nb < 1 || !(eps >= 0.0f) || inter < 1 || inter % 16 != 0) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(2 * inter, in_dim);
+    if (st != Q4A_OK) return st;
+    if (nb > 32) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(s, 2) ||
+        !aligned(b, 2) || !aligned(h, 2))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    GemvLaunch L = {};
+    L.w = w;
+    L.tensor_rows = 2 * inter;
+    L.s = s;
+    L.b = b;
+    L.x = x_raw;
+    L.norm_w = norm_w;
+    L.eps = eps;
+    L.shift = shift;
+    L.h = h;
+    L.fused_gate_up = true;
+    L.out_dim = inter;
+    L.in_dim = in_dim;
+    L.rmsnorm = true;
+    L.norm_groups = 1;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
 q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
                             const float* x_raw, const uint16_t* norm_w, float eps, float shift,
                             int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {

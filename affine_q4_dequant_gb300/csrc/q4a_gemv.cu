@@ -360,7 +360,11 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
 
 // CB: code bits. 4: packed nibbles. 2: derived 2-bit codes q4 >> 2, w = (4 q + 1.5) s + b.
 // 3: derived 3-bit codes q4 >> 1 = 2 * (2-bit upper part) + lowest bit, w = (2 q + 0.5) s + b.
-template <int NT, bool RMS, int MAXSEG, int CB = 4>
+// FG: fused gate|up. The matrix holds the gate rows [0, out_dim) and then the up rows; a
+// "tile" of the schedule is a unit of 16 gate rows and the 16 up rows with the same index,
+// kept in shared-memory tiles u and MT/2 + u of the row block, and the epilogue writes
+// h = fp16(silu(gate) * up) instead of y ("BATCH_MSL" experts.metal fn_moe_act_b).
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> p) {
     constexpr int NTOK = NT * 8;
@@ -487,18 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.sb_mode == kSbTma) {
                     if (lane == 0) {
                         const int nchunk = (gsz + 63) / 64;
-                        mbar_arrive_expect_tx(bar, (uint32_t)(2 * nchunk * j.ntile * kTileBytes));
-                        int m0 = 0;
-                        for (int lg = kNumMaps - 1; lg >= 0; --lg) {
-                            const int h = 1 << lg;
-                            if (j.ntile - m0 < h) continue;
-                            for (int c = 0; c < nchunk; ++c) {
-                                const uint32_t o = (uint32_t)((c * MT + m0) * kTileBytes);
-                                tma_load_2d(smem_addr(sdst + o), &p.tmap_s[lg], kg0 + 64 * c, (int)(trow0 + 16 * m0), bar);
-                                tma_load_2d(smem_addr(sdst + L.sb_pitch + o), &p.tmap_b[lg], kg0 + 64 * c,
-                                            (int)(trow0 + 16 * m0), bar);
+                        mbar_arrive_expect_tx(bar, (uint32_t)((FG ? 4 : 2) * nchunk * j.ntile * kTileBytes));
+                        for (int part = 0; part < (FG ? 2 : 1); ++part) {   // fused: gate rows, up rows
+                            const int64_t prow = trow0 + (part ? p.out_dim : 0);
+                            const int mbase = part * (MT / 2);
+                            int m0 = 0;
+                            for (int lg = kNumMaps - 1; lg >= 0; --lg) {
+                                const int h = 1 << lg;
+                                if (j.ntile - m0 < h) continue;
+                                for (int c = 0; c < nchunk; ++c) {
+                                    const uint32_t o = (uint32_t)((c * MT + mbase + m0) * kTileBytes);
+                                    tma_load_2d(smem_addr(sdst + o), &p.tmap_s[lg], kg0 + 64 * c, (int)(prow + 16 * m0), bar);
+                                    tma_load_2d(smem_addr(sdst + L.sb_pitch + o), &p.tmap_b[lg], kg0 + 64 * c,
+                                                (int)(prow + 16 * m0), bar);
+                                }
+                                m0 += h;
                             }
-                            m0 += h;
                         }
                     }
                 } else if (p.sb_mode == kSbRaw) {
@@ -565,18 +573,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     // One tall box per box column for each power-of-two run of tiles: the
                     // TMA engine pays per box, so few large boxes keep HBM streaming.
-                    mbar_arrive_expect_tx(full, (uint32_t)(j.ntile * (nbox * kTileBytes + (CB == 3 ? kLoTileBytes : 0))));
-                    int m0 = 0;
-                    for (int lg = kNumMaps - 1; lg >= 0; --lg) {
-                        const int h = 1 << lg;
-                        if (j.ntile - m0 < h) continue;
-                        for (int c = 0; c < nbox; ++c)
-                            tma_load_2d(smem_addr(st + (c * MT + m0) * kTileBytes), &p.tmap_w[lg],
-                                        CB == 4 ? (g0 + 4 * c) * 32 : g0 * 16, (int)(trow0 + 16 * m0), full);
-                        if constexpr (CB == 3)   // lowest bits: 8 bytes per group and row
-                            tma_load_2d(smem_addr(st + MT * kTileBytes + m0 * kLoTileBytes), &p.tmap_lo[lg], g0 * 8,
-                                        (int)(trow0 + 16 * m0), full);
-                        m0 += h;
+                    mbar_arrive_expect_tx(full, (uint32_t)((FG ? 2 : 1) * j.ntile *
+                                                           (nbox * kTileBytes + (CB == 3 ? kLoTileBytes : 0))));
+                    for (int part = 0; part < (FG ? 2 : 1); ++part) {   // fused: gate rows, up rows
+                        const int64_t prow = trow0 + (part ? p.out_dim : 0);
+                        const int mbase = part * (MT / 2);
+                        int m0 = 0;
+                        for (int lg = kNumMaps - 1; lg >= 0; --lg) {
+                            const int h = 1 << lg;
+                            if (j.ntile - m0 < h) continue;
+                            for (int c = 0; c < nbox; ++c)
+                                tma_load_2d(smem_addr(st + (c * MT + mbase + m0) * kTileBytes), &p.tmap_w[lg],
+                                            CB == 4 ? (g0 + 4 * c) * 32 : g0 * 16, (int)(prow + 16 * m0), full);
+                            if constexpr (CB == 3)   // lowest bits: 8 bytes per group and row
+                                tma_load_2d(smem_addr(st + MT * kTileBytes + (mbase + m0) * kLoTileBytes), &p.tmap_lo[lg],
+                                            g0 * 8, (int)(prow + 16 * m0), full);
+                            m0 += h;
+                        }
                     }
                 }
                 __syncwarp();
@@ -832,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int mi = 0; mi < TPW; ++mi) {
                 const int m = mi;
-                if (m >= j.ntile) continue;
+                if ((FG ? m % (MT / 2) : m) >= j.ntile) continue;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float* w0 = wpart + ((size_t)wg * (16 * MT) + m * 16 + g) * NTOK + nt * 8 + 2 * tq;
@@ -842,7 +855,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             consumer_sync();
             float* cp = cpart + (size_t)(blk & 1) * (16 * MT) * NTOK;
-            for (int e = ctid; e < R * NTOK; e += kConsumerWarps * 32) {
+            // fused: the gate rows [0, R) and the up rows [8 MT, 8 MT + R) of the row block
+            for (int e0 = ctid; e0 < (FG ? 2 : 1) * R * NTOK; e0 += kConsumerWarps * 32) {
+                const int e = (FG && e0 >= R * NTOK) ? e0 - R * NTOK + 8 * MT * NTOK : e0;
                 const size_t stride = (size_t)(16 * MT) * NTOK;
                 float v = wpart[e];
 #pragma unroll
@@ -874,6 +889,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < C; ++c) v += ld_peer_f32(map_peer(cp_addr + off, (uint32_t)c));
                     } else {
                         v = cp[row * NTOK + tok];
+                    }
+                    if constexpr (FG) {
+                        float u;
+                        if (C > 1) {
+                            const uint32_t off = (uint32_t)(((8 * MT + row) * NTOK + tok) * 4);
+                            u = 0.f;
+                            for (int c = 0; c < C; ++c) u += ld_peer_f32(map_peer(cp_addr + off, (uint32_t)c));
+                        } else {
+                            u = cp[(8 * MT + row) * NTOK + tok];
+                        }
+                        const float gt = v * 16777216.0f;
+                        const float hv = gt / (1.0f + expf(-gt)) * (u * 16777216.0f);
+                        p.h[(int64_t)(sg.tok0 + tok) * p.out_dim + lrow0 + row] = __half_as_ushort(__float2half_rn(hv));
+                        continue;
                     }
                     float out = v * 16777216.0f;
                     if (p.post_silu) {   // silu(y / div): the gated-residual bottleneck epilogue
@@ -958,9 +987,9 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1022,14 +1051,24 @@ int cluster_capacity_t(int nt, bool rms, int cluster, uint32_t smem_bytes, int c
     return occupancy_clusters<4, false, MAXSEG>(cluster, smem_bytes);
 }
 
-int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_bytes, int cb) {
+int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_bytes, int cb, bool fg) {
+    if (fg) {
+        if (rms) {
+            if (nt == 1) return occupancy_clusters<1, true, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+            if (nt == 2) return occupancy_clusters<2, true, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+            return occupancy_clusters<4, true, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+        }
+        if (nt == 1) return occupancy_clusters<1, false, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+        if (nt == 2) return occupancy_clusters<2, false, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+        return occupancy_clusters<4, false, kDenseMaxSeg, 4, true>(cluster, smem_bytes);
+    }
     return experts ? cluster_capacity_t<Q4A_MAX_SEGMENTS>(nt, rms, cluster, smem_bytes, 4)
                    : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1043,7 +1082,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.n_tiles ? max_clusters : prm.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
@@ -1073,6 +1112,10 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     const int mt = tiles_per_block(nt);
     const int cb = L.code_bits;
     if (cb != 4 && (L.experts || L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
+    const bool fg = L.fused_gate_up;
+    if (fg && (L.experts || cb != 4 || L.silu || L.out_dim % 16 != 0 || !L.h)) return Q4A_ERR_UNSUPPORTED;
+    // schedule units per row block: tiles, or (fused) gate|up tile pairs
+    const int mt_units = fg ? mt / 2 : mt;
     const int G = (int)(L.in_dim / kGroup);
 
     // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
@@ -1087,6 +1130,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         return g;
     };
     const int64_t n_tiles = (int64_t)((L.out_dim + 15) / 16) * L.nseg;
+    const int64_t tile_work = fg ? 2 * n_tiles : n_tiles;   // 16-row tiles to stream (fused: 2 per unit)
     const bool al16 = (reinterpret_cast<uintptr_t>(L.s) % 16 == 0) && (reinterpret_cast<uintptr_t>(L.b) % 16 == 0);
     // Scales/biases of a full-K row block: 2D TMA when rows are 16-byte multiples, else 1D
     // TMA of the contiguous block when it fits the raw staging budget, else element copies.
@@ -1099,7 +1143,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     auto sbmode = [&](int c) { return c == 1 ? sbm_full : kSbTma; };
     auto sbufs = [&](int c) {
         const int64_t clusters = di.sm_count / c;
-        return (n_tiles + clusters - 1) / clusters <= mt && L.nseg == 1 ? 1 : 2;
+        return (n_tiles + clusters - 1) / clusters <= mt_units && L.nseg == 1 ? 1 : 2;
     };
     auto fits = [&](int c, int stages) {
         const int g = slice(c);
@@ -1113,13 +1157,13 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         if (!fits(c, 3)) continue;
         if (C == 0) C = c;                       // smallest that fits at all
         const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
-                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb).total + 1024, cb);
+                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb).total + 1024, cb, fg);
         if (q <= 0) continue;
-        if (n_tiles >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
+        if (tile_work >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
             C = c;
             break;
         }
-        if (c == C && n_tiles >= 3 * (int64_t)q) break;
+        if (c == C && tile_work >= 3 * (int64_t)q) break;
     }
     if (C == 0) return Q4A_ERR_UNSUPPORTED;
     const int gs = slice(C);
@@ -1159,6 +1203,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.x_rows = L.x_rows;
     prm.norm_w = L.norm_w;
     prm.y = L.y;
+    prm.h = L.h;
     prm.eps = L.eps;
     prm.shift = L.shift;
     prm.norm_groups = L.norm_groups > 0 ? L.norm_groups : 1;
@@ -1173,7 +1218,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.tiles_per_seg = (int)((L.out_dim + 15) / 16);
     prm.nseg = L.nseg;
     prm.n_tiles = prm.tiles_per_seg * L.nseg;
-    prm.mt = mt;
+    prm.mt = mt_units;
     prm.ntok_max = ntm;
     prm.stages = stages;
     prm.sb_mode = sbmode(C);
@@ -1208,6 +1253,16 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
 
     const uint32_t smem_bytes = lay.total + 1024;
     if constexpr (MAXSEG == kDenseMaxSeg) {
+        if (fg) {
+            if (L.rmsnorm) {
+                if (nt == 1) return launch_variant<1, true, MAXSEG, 4, true>(prm, smem_bytes, stream);
+                if (nt == 2) return launch_variant<2, true, MAXSEG, 4, true>(prm, smem_bytes, stream);
+                return launch_variant<4, true, MAXSEG, 4, true>(prm, smem_bytes, stream);
+            }
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+        }
         if (cb == 2) {
             if (nt == 1) return launch_variant<1, false, MAXSEG, 2>(prm, smem_bytes, stream);
             if (nt == 2) return launch_variant<2, false, MAXSEG, 2>(prm, smem_bytes, stream);

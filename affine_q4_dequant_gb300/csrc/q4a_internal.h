@@ -120,6 +120,7 @@ struct GemvParams {
     const int32_t* x_rows;    // may be null
     const uint16_t* norm_w;   // bf16 [in_dim] (RMSNorm variant)
     float* y;                 // fp32 [slots][out_dim]
+    uint16_t* h;              // fused gate|up: fp16 silu(gate) * up [slots][out_dim]
     float eps, shift;
     float post_div;           // output epilogue silu(y / post_div) when post_silu
     int32_t post_silu;
@@ -158,6 +159,8 @@ struct GemvLaunch {
     bool silu;                // output epilogue y -> silu(y / silu_div)
     float silu_div;
     int norm_groups;          // RMSNorm variant: normalisation segments per row (>= 1)
+    bool fused_gate_up = false;   // w holds gate rows [0, out_dim) then up rows [out_dim, 2 out_dim);
+    uint16_t* h = nullptr;        // the output is h = fp16(silu(gate) * up) [slots][out_dim]
     int code_bits = 4;        // 4 (w: packed nibbles), 2 or 3 (w: 2-bit codes [rows][in/4],
     const uint8_t* w_lo = nullptr;  // w_lo: the 3-bit codes' lowest-bit plane [rows][in/8])
     bool experts;

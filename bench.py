@@ -4,10 +4,11 @@
 One step = for every NB in the sweep (default 1, 2, 4, 8, 16), one decode-layer
 MLP on each of L weight sets (default 8, so the 453 MB of weights are larger
 than three L2 caches and every layer streams from HBM):
-    q4a_gemv_rmsnorm  4096 -> 12288 fused gate|up with the RMSNorm prologue
-    q4a_silu_mul_xsum silu(gate) * up on the 6144-wide halves
-    q4a_gemv          12288 -> 4096 down projection (its own synthetic input
-                      x = fp16(silu(a) * b), built once per NB by the same kernel)
+    q4a_gemv_rmsnorm_gate_up_silu  4096 -> 2 x 6144 gate|up with the RMSNorm prologue
+                                   and h = fp16(silu(gate) * up) in the epilogue
+    q4a_gemv                       12288 -> 4096 down projection (its own synthetic input
+                                   x = fp16(silu(a) * b), built once per NB by
+                                   q4a_silu_mul_xsum)
 The headline value is achieved HBM GB/s over the step: algorithmic bytes of every
 launch (packed codes at 0.5 B per weight, bf16 scale + bias per 64 weights,
 activations, outputs) divided by the device time of the step.
@@ -50,10 +51,11 @@ def gemv_bytes(out_dim, in_dim, nb, x_bytes_per_el, bits=4):
 
 
 def layer_bytes(nb):
-    gu = gemv_bytes(INTER2, HIDDEN, nb, 4) + HIDDEN * 2           # fp32 x_raw + bf16 norm weight
-    act = nb * INTER2 * 4 + nb * INTER * 2 + nb * (INTER // 64) * 4
+    """(fused gate|up, down) algorithmic bytes of one decode layer at NB rows: the gate|up
+    reads fp32 x_raw and the bf16 norm weight and writes h in fp16 (no fp32 gate|up output)."""
+    gu = INTER2 * HIDDEN * BYTES_PER_WEIGHT + nb * HIDDEN * 4 + HIDDEN * 2 + nb * INTER * 2
     dn = gemv_bytes(DOWN_OUT, DOWN_IN, nb, 2)
-    return gu, act, dn
+    return gu, dn
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -244,9 +246,7 @@ def run_ours(args, rank, world, local_rank):
             x_dn, _ = q4a.silu_mul_xsum(gate_up_dn, want_hsum=False)
             acts[nb] = {
                 "a": a, "x_dn": x_dn,
-                "y_gu": torch.empty((nb, INTER2), dtype=torch.float32, device=dev),
                 "h": torch.empty((nb, INTER), dtype=torch.float16, device=dev),
-                "hsum": torch.empty((nb, INTER // 64), dtype=torch.float32, device=dev),
                 "y_dn": torch.empty((nb, DOWN_OUT), dtype=torch.float32, device=dev),
             }
     torch.cuda.synchronize()
@@ -254,11 +254,7 @@ def run_ours(args, rank, world, local_rank):
     def gate_up_call(nb, l):
         ly, ac = layers[l], acts[nb]
         w, s_, b_ = ly["gu"]
-        q4a.gemv_rmsnorm(w, s_, b_, ac["a"], ly["norm_w"], eps=1e-6, out=ac["y_gu"], stream=stream)
-
-    def act_call(nb, l):
-        ac = acts[nb]
-        q4a.silu_mul_xsum(ac["y_gu"], h=ac["h"], hsum=ac["hsum"], stream=stream)
+        q4a.gemv_rmsnorm_gate_up_silu(w, s_, b_, ac["a"], ly["norm_w"], eps=1e-6, out=ac["h"], stream=stream)
 
     def down_call(nb, l):
         ly, ac = layers[l], acts[nb]
@@ -267,7 +263,6 @@ def run_ours(args, rank, world, local_rank):
 
     def layer_call(nb, l):
         gate_up_call(nb, l)
-        act_call(nb, l)
         down_call(nb, l)
 
     # eager warm-up: first calls fill the library's per-device caches before capture
@@ -278,9 +273,9 @@ def run_ours(args, rank, world, local_rank):
 
     # Graphs per NB (no event nodes inside, so programmatic dependent launch overlaps
     # consecutive kernels): the decode layer over the L weight sets, and one chain per
-    # kernel kind (L gate|up launches, L SiLU*up launches, L down launches) whose replay
-    # time gives the per-launch kernel duration.
-    kinds = {"layer": layer_call, "gate_up": gate_up_call, "act": act_call, "down": down_call}
+    # kernel kind (L fused gate|up launches, L down launches) whose replay time gives the
+    # per-launch kernel duration.
+    kinds = {"layer": layer_call, "gate_up": gate_up_call, "down": down_call}
     graphs = {}
     for nb in nbs:
         for kind, fn in kinds.items():
@@ -338,17 +333,16 @@ def run_ours(args, rank, world, local_rank):
     gemv_bytes_total, gemv_ms_total, step_bytes = 0.0, 0.0, 0.0
     n = args.steps * L
     for nb in nbs:
-        gu_b, act_b, dn_b = layer_bytes(nb)
-        gu_ms, act_ms, dn_ms, lay_ms = (kind_ms(k, nb) for k in ("gate_up", "act", "down", "layer"))
+        gu_b, dn_b = layer_bytes(nb)
+        gu_ms, dn_ms, lay_ms = (kind_ms(k, nb) for k in ("gate_up", "down", "layer"))
         per_nb[str(nb)] = {
             "layer_us": lay_ms / n * 1e3,
             "gate_up_us": gu_ms / n * 1e3, "gate_up_gbs": gu_b / (gu_ms / n * 1e-3) / 1e9,
-            "act_us": act_ms / n * 1e3,
             "down_us": dn_ms / n * 1e3, "down_gbs": dn_b / (dn_ms / n * 1e-3) / 1e9,
         }
         gemv_bytes_total += (gu_b + dn_b) * n
         gemv_ms_total += gu_ms + dn_ms
-        step_bytes += 2 * (gu_b + act_b + dn_b) * L     # the layer chain + the per-kind chains
+        step_bytes += 2 * (gu_b + dn_b) * L     # the layer chain + the per-kind chains
     gemv_launches = 2 * n * len(nbs)
     ms_per_step = max_over_ranks(elapsed_ms / args.steps, dev if dist is not None else None)
     value = whole_job_gbs(step_bytes, world, ms_per_step)
@@ -364,7 +358,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = gemv_bytes_total / (gemv_ms_total * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_kind": peak_kind,
-                    "kernel": "gemv_kernel: every q4a_gemv / q4a_gemv_rmsnorm launch of the step",
+                    "kernel": "gemv_kernel: every q4a_gemv_rmsnorm_gate_up_silu / q4a_gemv launch of the step",
                     "kernel_source_sha256_16": kernel_source_hash(),
                     "launches": gemv_launches, "traffic": load_traffic(),
                     "timing": "CUDA events around graph replays of back-to-back launches of one kind, "
@@ -376,10 +370,10 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xu4->f32", "data": "synthetic",
-        "config": {"workload": "dense decode-layer MLP: 4096->12288 gate|up (fused RMSNorm) + "
-                               "silu*up (6144) + 12288->4096 down; affine-Q4 group 64",
+        "config": {"workload": "dense decode-layer MLP: 4096->2x6144 gate|up (RMSNorm prologue, "
+                               "silu(gate)*up epilogue) + 12288->4096 down; affine-Q4 group 64",
                    "step": "per NB: the decode layer on each of the weight sets, then the same "
-                           "gate|up, silu*up and down launches as one back-to-back chain per kind",
+                           "gate|up and down launches as one back-to-back chain per kind",
                    "nbs": nbs, "layers_cycled": L,
                    "l2": f"weights cycled over {L} layers ({L * 2 * 28.3:.0f} MB > 3 x L2); no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -387,7 +381,7 @@ def run_ours(args, rank, world, local_rank):
         "us_per_decode_layer": {k: v["layer_us"] for k, v in per_nb.items()},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * len(nbs) * L * 6,
+        "gpu_launches": args.steps * len(nbs) * L * 4,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -624,8 +618,7 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
                 a = host_in[nb][0].to(dev, non_blocking=True)
                 gu_dn = host_in[nb][1].to(dev, non_blocking=True)
                 w, s, b = ly["gu"]
-                y = q4a.gemv_rmsnorm(w, s, b, a, ly["norm_w"], eps=1e-6, stream=stream)
-                q4a.silu_mul_xsum(y, stream=stream)
+                q4a.gemv_rmsnorm_gate_up_silu(w, s, b, a, ly["norm_w"], eps=1e-6, stream=stream)
                 x_dn, _ = q4a.silu_mul_xsum(gu_dn, want_hsum=False, stream=stream)
                 w, s, b = ly["dn"]
                 y_dn = q4a.gemv(w, s, b, x_dn, stream=stream)

@@ -107,6 +107,33 @@ Q4A_API q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const
                     q4a_stream_t stream);
 
 /*
+ * q4a_gemv_gate_up_silu -- the gate and up projections of a gated MLP in one pass, with the
+ * activation in the output epilogue ("BATCH_MSL", experts.metal fn_moe_gate_up_b followed by
+ * fn_moe_act_b):  h[r][o] = fp16( silu(g) * u ),  g = (W_gate.x)[r][o],  u = (W_up.x)[r][o],
+ * silu(v) = v / (1 + e^-v), g and u in fp32, rounded once to binary16.
+ *   h      out  fp16 [nb][inter]
+ *   w      in   uint8 [2 * inter][in_dim/2]: rows [0, inter) are W_gate, [inter, 2 inter) W_up
+ *   s, b   in   bf16 [2 * inter][in_dim/64], same row order
+ *   x      in   fp16 [nb][in_dim]
+ *   Requires nb in 1..256, inter >= 1 and inter % 16 == 0, in_dim % 64 == 0; w and x 16-byte
+ *   aligned, s, b and h 2-byte aligned. Always runs on the GEMV kernel.
+ */
+Q4A_API q4a_status q4a_gemv_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s, const uint16_t* b,
+                                         const uint16_t* x, int nb, int64_t inter, int64_t in_dim,
+                                         q4a_stream_t stream);
+
+/*
+ * q4a_gemv_rmsnorm_gate_up_silu -- q4a_gemv_gate_up_silu on RMS-normalised activations (the
+ * prologue of q4a_gemv_rmsnorm, one normalisation group): a decode layer's whole first half.
+ *   x_raw, norm_w, eps, shift as q4a_gemv_rmsnorm; nb in 1..32; everything else as
+ *   q4a_gemv_gate_up_silu.
+ */
+Q4A_API q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s,
+                                                 const uint16_t* b, const float* x_raw, const uint16_t* norm_w,
+                                                 float eps, float shift, int nb, int64_t inter, int64_t in_dim,
+                                                 q4a_stream_t stream);
+
+/*
  * q4a_lowbit_pack -- derived low-bit codes of a packed 4-bit matrix ("BATCH_MSL",
  * quantized_rows.metal fn_q2_rows_h and fn_q3_rows_h: codes q4 >> 2 and q4 >> 1).
  *   w_up      out  uint8 [rows][in_dim/4]: the 2-bit codes q4 >> 2 (also the upper two bits of

@@ -39,6 +39,8 @@ def lib():
     lib.q4a_gemv_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     lib.q4a_lowbit_pack.argtypes = [P, P, P, I64, I64, P]
     lib.q4a_gemv_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, I64, I64, P]
+    lib.q4a_gemv_gate_up_silu.argtypes = [P, P, P, P, P, I32, I64, I64, P]
+    lib.q4a_gemv_rmsnorm_gate_up_silu.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
     return lib
 
 
@@ -190,4 +192,19 @@ def test_lowbit_rejections(lib):
     assert g(A, 3, A, A, A, A, A, 1, 64, 576, None) == SHAPE    # 3-bit: in_dim % 128
     assert g(A, 2, A, None, A, A, A, 257, 64, 512, None) == UNSUP
     assert g(A, 2, A + 4, None, A, A, A, 1, 64, 512, None) == ALIGN
+
+
+def test_gate_up_silu_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_gemv_gate_up_silu
+    assert f(None, A, A, A, A, 1, 64, 512, None) == NULL
+    assert f(A, A, A, A, A, 0, 64, 512, None) == SHAPE
+    assert f(A, A, A, A, A, 1, 40, 512, None) == SHAPE      # inter % 16
+    assert f(A, A, A, A, A, 1, 64, 500, None) == SHAPE      # in_dim % 64
+    assert f(A, A, A, A, A, 257, 64, 512, None) == UNSUP
+    assert f(A + 1, A, A, A, A, 1, 64, 512, None) == ALIGN
+    g = lib.q4a_gemv_rmsnorm_gate_up_silu
+    assert g(A, A, A, A, A, A, 1e-6, 0.0, 33, 64, 512, None) == UNSUP
+    assert g(A, A, A, A, A, A, -1.0, 0.0, 1, 64, 512, None) == SHAPE
+    assert g(A, A, A, A, A + 4, A, 1e-6, 0.0, 1, 64, 512, None) == ALIGN
 
