@@ -64,6 +64,8 @@ def _load():
             "q4o_lowbit_pack3lo": (None, [P, P, I, I]),
             "q4o_lowbit_codes": (None, [P, P, P, I, I]),
             "q4o_gemv_lowbit": (None, [P, P, P, P, P, P, P, I, I, I]),
+            "q4o_gemv_f32x": (None, [P, P, P, P, P, P, I, I, I]),
+            "q4o_quantize": (None, [P, P, P, P, I, I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -305,4 +307,29 @@ def gemv_lowbit(w2, wlo, s, b, x_bits):
     bound = np.empty((nb, out_dim), np.float64)
     _load().q4o_gemv_lowbit(_p(y), _p(bound), _p(w2), _p(wlo), _p(s), _p(b), _p(x_bits), nb, out_dim, in_dim)
     return y, bound
+
+
+# ---- prefill helpers ------------------------------------------------------------------------
+
+
+def gemv_f32x(packed, s, b, x_f32):
+    """y = W x with fp32 activations as given ([BATCH_MSL] fn_qmv_small_b). Returns (y, bound)."""
+    packed, s, b, x = _c(packed, np.uint8), _c(s, np.uint16), _c(b, np.uint16), _c(x_f32, np.float32)
+    nb, in_dim = x.shape
+    out_dim = packed.shape[0]
+    y = np.empty((nb, out_dim), np.float64)
+    bound = np.empty((nb, out_dim), np.float64)
+    _load().q4o_gemv_f32x(_p(y), _p(bound), _p(packed), _p(s), _p(b), _p(x), nb, out_dim, in_dim)
+    return y, bound
+
+
+def quantize(w_f32):
+    """4-bit affine min/max quantiser (binary32 steps). Returns (packed, s bits, b bits)."""
+    w = _c(w_f32, np.float32)
+    rows, in_dim = w.shape
+    packed = np.empty((rows, in_dim // 2), np.uint8)
+    s = np.empty((rows, in_dim // 64), np.uint16)
+    b = np.empty((rows, in_dim // 64), np.uint16)
+    _load().q4o_quantize(_p(packed), _p(s), _p(b), _p(w), rows, in_dim)
+    return packed, s, b
 

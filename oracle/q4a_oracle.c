@@ -606,3 +606,81 @@ Q4O_EXPORT void q4o_gemv_lowbit(double* y, double* bound, const uint8_t* w2, con
     free(xv);
     free(w);
 }
+
+/* ---- prefill helpers ---------------------------------------------------------------- */
+
+/* [BATCH_MSL] fn_qmv_small_b: the projection straight from fp32 activations (few output
+ * rows, any number of input rows). y[r][o] = sum_i w[o][i] x[r][i], w = s q + b dequantised
+ * explicitly, x the fp32 values as given, in double; bound as q4o_gemv. */
+Q4O_EXPORT void q4o_gemv_f32x(double* y, double* bound, const uint8_t* packed, const uint16_t* s,
+                              const uint16_t* b, const float* x, int64_t nb, int64_t out_dim, int64_t in_dim)
+{
+    const int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    for (int64_t o = 0; o < out_dim; o++) {
+        dequant_row(w, packed + o * (in_dim / 2), s + o * groups, b + o * groups, in_dim);
+        for (int64_t r = 0; r < nb; r++) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < in_dim; i++) {
+                const double p = w[i] * (double)x[r * in_dim + i];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[r * out_dim + o] = acc;
+            if (bound)
+                bound[r * out_dim + o] = 2e-3 * mag + 1e-5;
+        }
+    }
+    free(w);
+}
+
+/* binary32 -> bfloat16, round to nearest even (NaN -> a quiet NaN). */
+static uint16_t bf16_round(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof(u));
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return 0x7FC0;
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* A 4-bit affine quantiser for float weights. The pages never define one; this is the plain
+ * min/max reading, every step in binary32 (the precision that decides the integer codes):
+ *   b = bf16(min_g w),  s = bf16((max_g w - b) / 15) when max_g w > b, else 0,
+ *   q = clamp(rint((w - b) / s), 0, 15) when s > 0, else 0,
+ * with b and s their bfloat16 values, rint rounding half to even. Writes the packed codes
+ * [rows][in_dim/2] (as q4o_pack), s and b [rows][in_dim/64]. w must be finite. */
+Q4O_EXPORT void q4o_quantize(uint8_t* packed, uint16_t* s, uint16_t* b, const float* w,
+                             int64_t rows, int64_t in_dim)
+{
+    const int64_t groups = in_dim / 64;
+    uint8_t* codes = (uint8_t*)malloc((size_t)in_dim);
+    for (int64_t o = 0; o < rows; o++) {
+        for (int64_t g = 0; g < groups; g++) {
+            const float* wg = w + o * in_dim + g * 64;
+            float mn = wg[0], mx = wg[0];
+            for (int i = 1; i < 64; i++) {
+                if (wg[i] < mn) mn = wg[i];
+                if (wg[i] > mx) mx = wg[i];
+            }
+            const uint16_t bb = bf16_round(mn);
+            const float bf = (float)bf16_value(bb);
+            const float range = mx - bf;
+            const uint16_t sb = range > 0.0f ? bf16_round(range / 15.0f) : (uint16_t)0;
+            const float sf = (float)bf16_value(sb);
+            for (int i = 0; i < 64; i++) {
+                int q = 0;
+                if (sf > 0.0f) {
+                    const float t = rintf((wg[i] - bf) / sf);
+                    q = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
+                }
+                codes[g * 64 + i] = (uint8_t)q;
+            }
+            s[o * groups + g] = sb;
+            b[o * groups + g] = bb;
+        }
+        q4o_pack(packed + o * (in_dim / 2), codes, 1, in_dim);
+    }
+    free(codes);
+}

@@ -574,3 +574,61 @@ def test_lowbit_gemv_brute_force_tiny():
                     acc += w * xf[r, i]
                 assert abs(y[r, o] - acc) <= 1e-12 * (1 + abs(acc))
         assert np.all(bound > 0)
+
+
+# ---- prefill helpers ([BATCH_MSL] fn_qmv_small_b; the min/max quantiser) -------------------
+
+
+def test_quantize_hand_worked(golden):
+    g = golden("quantize_ramp.txt")
+    w = (np.arange(64, dtype=np.float32) * 0.25).reshape(1, 64)
+    packed, s, b = oracle.quantize(w)
+    assert int(s[0, 0]) == int(g["s"][0], 16) and int(b[0, 0]) == int(g["b"][0], 16)
+    codes = oracle.unpack(packed, 64)[0]
+    for item in g["codes"]:
+        i, q = item.split("=")
+        assert int(codes[int(i)]) == int(q), i
+
+
+def test_quantize_exact_grid_and_constant_groups():
+    k = np.tile(np.arange(16), 4)
+    w = np.stack([-1.0 + 0.125 * k, np.full(64, 2.0), 3.0 + 0.5 * k[::-1]]).astype(np.float32)
+    packed, s, b = oracle.quantize(w)
+    codes = oracle.unpack(packed, 64)
+    assert np.array_equal(codes[0], k) and s[0, 0] == 0x3E00 and b[0, 0] == 0xBF80   # 0.125, -1
+    assert s[1, 0] == 0 and b[1, 0] == 0x4000 and not codes[1].any()                 # constant 2.0
+    assert np.array_equal(codes[2], k[::-1]) and s[2, 0] == 0x3F00 and b[2, 0] == 0x4040
+
+
+def test_quantize_reconstruction_error():
+    rng = np.random.default_rng(51)
+    w = rng.normal(0, 0.05, (9, 256)).astype(np.float32)
+    packed, s, b = oracle.quantize(w)
+    codes = oracle.unpack(packed, 256).astype(np.float64)
+    sf = np.repeat(wl.bf16_bits_to_f32(s).astype(np.float64), 64, axis=1)
+    bf = np.repeat(wl.bf16_bits_to_f32(b).astype(np.float64), 64, axis=1)
+    err = np.abs(sf * codes + bf - w)
+    # half a step, plus the bf16 rounding of the bias (below the minimum) and of the step
+    gmin = np.repeat(w.reshape(9, 4, 64).min(axis=2), 64, axis=1)
+    assert np.all(err <= 0.5 * sf + np.abs(bf - gmin) + 15 * sf * 2.0 ** -8 + 1e-7)
+    assert np.all(codes[codes > 0] <= 15)
+
+
+def test_gemv_f32x_matches_the_fp16_product_on_fp16_values():
+    rng = np.random.default_rng(52)
+    codes = rng.integers(0, 16, (5, 128), dtype=np.uint8)
+    s = wl.f32_to_bf16_bits(np.abs(rng.normal(0, 0.02, (5, 2))).astype(np.float32))
+    b = wl.f32_to_bf16_bits((-8 * rng.normal(0, 0.01, (5, 2))).astype(np.float32))
+    x16 = wl.f16_bits(rng.normal(0, 1, (3, 128)))
+    packed = oracle.pack(codes)
+    y16, _ = oracle.gemv(packed, s, b, x16)
+    y32, bound = oracle.gemv_f32x(packed, s, b, x16.view(np.float16).astype(np.float32))
+    np.testing.assert_allclose(y32, y16, rtol=0, atol=1e-12)
+    # brute force with fp32 activations that fp16 cannot hold
+    x = rng.normal(0, 1, (2, 128)).astype(np.float32) * np.float32(1 + 2 ** -20)
+    y, _ = oracle.gemv_f32x(packed, s, b, x)
+    sf, bf = wl.bf16_bits_to_f32(s).astype(float), wl.bf16_bits_to_f32(b).astype(float)
+    for r in range(2):
+        for o in range(5):
+            ref = sum((sf[o, i // 64] * codes[o, i] + bf[o, i // 64]) * float(x[r, i]) for i in range(128))
+            assert abs(y[r, o] - ref) <= 1e-12 * (1 + abs(ref))
