@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "q4a_gemv": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_silu": (I32, [P, P, P, P, P, F, I32, I64, I64, P]),
         "q4a_lowbit_pack": (I32, [P, P, P, I64, I64, P]),
+        "q4a_quantize": (I32, [P, P, P, P, I64, I64, P]),
+        "q4a_gemv_f32x": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_gate_up_silu": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_gate_up_silu": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
@@ -143,6 +145,30 @@ def gemv_rmsnorm_gate_up_silu(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: 
         _dev(out, "h", _F16), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
         _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift), nb, inter,
         in_dim, _stream(stream)))
+    return out
+
+
+def quantize(w: torch.Tensor, stream=None):
+    """4-bit min/max quantisation of fp32 weights [rows][in]: (packed codes, s bf16, b bf16)."""
+    rows, in_dim = w.shape
+    packed = torch.empty((rows, in_dim // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((rows, in_dim // 64), dtype=torch.bfloat16, device=w.device)
+    b = torch.empty((rows, in_dim // 64), dtype=torch.bfloat16, device=w.device)
+    _check("q4a_quantize", _lib.q4a_quantize(_dev(packed, "w_packed", _U8), _dev(s, "s", _BF16),
+                                             _dev(b, "b", _BF16), _dev(w, "w", _F32), rows, in_dim,
+                                             _stream(stream)))
+    return packed, s, b
+
+
+def gemv_f32x(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = W x from fp32 activations (narrow projections of prefill)."""
+    nb, in_dim = x.shape
+    out_dim = w.shape[0]
+    if out is None:
+        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
+    _check("q4a_gemv_f32x", _lib.q4a_gemv_f32x(
+        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
+        _dev(x, "x", _F32), nb, out_dim, in_dim, _stream(stream)))
     return out
 
 

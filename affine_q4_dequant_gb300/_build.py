@@ -19,6 +19,7 @@ LIB = os.path.join(HERE, "libq4a.so")
 BUILD_DIR = os.path.join(ROOT, "_build", "q4a")
 SOURCES = ["q4a_api.cu", "q4a_gemv.cu", "q4a_dense_tc.cu", "q4a_elementwise.cu"]
 HEADERS = [os.path.join(CSRC, "q4a_internal.h"), os.path.join(CSRC, "q4a_device.cuh"),
+           os.path.join(CSRC, "q4a_prefill.h"),
            os.path.join(ROOT, "include", "q4a.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "q4a_internal.h"
+#include "q4a_prefill.h"
 
 namespace q4a {
 
@@ -78,6 +79,26 @@ q4a_status q4a_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_packed
     if (rows < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
     if (!aligned(w_packed, 16) || !aligned(w_up, 16) || (w_lo && !aligned(w_lo, 16))) return Q4A_ERR_ALIGN;
     return launch_lowbit_pack(w_up, w_lo, w_packed, rows, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_quantize(uint8_t* w_packed, uint16_t* s, uint16_t* b, const float* w, int64_t rows, int64_t in_dim,
+                        q4a_stream_t stream) {
+    if (!w_packed || !s || !b || !w) return Q4A_ERR_NULL;
+    if (rows < 1 || in_dim < kGroup || in_dim % kGroup != 0) return Q4A_ERR_SHAPE;
+    if (!aligned(w_packed, 16) || !aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2)) return Q4A_ERR_ALIGN;
+    return launch_quantize(w_packed, s, b, w, rows, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_f32x(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b, const float* x, int nb,
+                         int64_t out_dim, int64_t in_dim, q4a_stream_t stream) {
+    if (!y || !w || !s || !b || !x) return Q4A_ERR_NULL;
+    if (nb < 1) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if ((int64_t)nb * out_dim > ((int64_t)1 << 36)) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    return launch_gemv_f32x(y, w, s, b, x, nb, out_dim, in_dim, (cudaStream_t)stream);
 }
 
 q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_dim, q4a_stream_t stream) {

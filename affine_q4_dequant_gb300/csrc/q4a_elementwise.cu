@@ -3,12 +3,16 @@
 //   q4a_xsum           (A2) per-64-group sums of fp16 activations
 //   q4a_silu_mul_xsum  (A7) h = fp16(silu(gate) * up) plus group sums of h
 //   q4a_moe_combine    routing-weighted sum of expert rows plus the gated shared expert
-//   a NaN fill for routed-expert segments with an out-of-range expert id.
+//   a NaN fill for routed-expert segments with an out-of-range expert id,
+//   q4a_quantize       a 4-bit min/max quantiser for float weights (prefill helper)
+//   q4a_gemv_f32x      the projection straight from fp32 activations (prefill helper).
 // The elementwise ones are grid-stride kernels over 16-byte vectors, sized to a multiple
 // of the SM count, with no shared memory and no waits.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "q4a_internal.h"
+#include "q4a_prefill.h"
 
 namespace q4a {
 namespace {
@@ -80,6 +84,115 @@ __global__ void lowbit_pack_kernel(uint2* __restrict__ w2, uint32_t* __restrict_
                 }
         w2[i] = make_uint2(up[0], up[1]);
         if (wlo) wlo[i] = lo;
+    }
+    __threadfence();
+    grid_dep_launch();
+}
+
+// Min/max quantiser, one thread per 64-input group, every step in binary32 (it decides the
+// integer codes): b = bf16(min), s = bf16((max - b) / 15) when max > b, else 0, and
+// q = clamp(rint((w - b) / s), 0, 15) (0 when s = 0), with b and s their bfloat16 values.
+__global__ void quantize_kernel(uint4* __restrict__ packed, uint16_t* __restrict__ s_out,
+                                uint16_t* __restrict__ b_out, const float4* __restrict__ w, int64_t n_groups) {
+    grid_dep_wait();
+    for (int64_t gi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gi < n_groups;
+         gi += (int64_t)gridDim.x * blockDim.x) {
+        float v[64];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float4 f = w[gi * 16 + k];
+            v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+        }
+        float mn = v[0], mx = v[0];
+#pragma unroll
+        for (int i = 1; i < 64; ++i) {
+            mn = v[i] < mn ? v[i] : mn;
+            mx = v[i] > mx ? v[i] : mx;
+        }
+        const __nv_bfloat16 bb = __float2bfloat16_rn(mn);
+        const float bf = __bfloat162float(bb);
+        const float range = __fsub_rn(mx, bf);
+        const __nv_bfloat16 sb = range > 0.0f ? __float2bfloat16_rn(__fdiv_rn(range, 15.0f)) : __float2bfloat16_rn(0.0f);
+        const float sf = __bfloat162float(sb);
+        uint32_t words[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            uint32_t wd = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                uint32_t q = 0u;
+                if (sf > 0.0f) {
+                    const float t = rintf(__fdiv_rn(__fsub_rn(v[8 * k + e], bf), sf));
+                    q = t < 0.0f ? 0u : (t > 15.0f ? 15u : (uint32_t)t);
+                }
+                wd |= q << (4 * e);   // element 8k + e: nibble e of word k (low nibble first per byte)
+            }
+            words[k] = wd;
+        }
+        packed[gi * 2] = make_uint4(words[0], words[1], words[2], words[3]);
+        packed[gi * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
+        s_out[gi] = __bfloat16_as_ushort(sb);
+        b_out[gi] = __bfloat16_as_ushort(bb);
+    }
+    __threadfence();
+    grid_dep_launch();
+}
+
+// y = W x from fp32 activations, for a few output rows over any number of activation rows:
+// one warp per (output row, block of up to 4 activation rows). Lane l takes the 32-bit code
+// words l, l + 32, ... of the row (word wi holds elements 8wi .. 8wi+7, element 8wi + e in
+// nibble e); per word and activation row sum(q x) and sum(x) in fp32, then
+// acc += s * sum(q x) + b * sum(x) with the word's group scale and bias; a fixed xor-shuffle
+// tree sums the lanes.
+__global__ void gemv_f32x_kernel(float* __restrict__ y, const uint32_t* __restrict__ w,
+                                 const uint16_t* __restrict__ s, const uint16_t* __restrict__ b,
+                                 const float* __restrict__ x, int64_t nb, int64_t out_dim, int64_t in_dim) {
+    grid_dep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t n_tb = (nb + 3) / 4;
+    const int64_t n_items = out_dim * n_tb;
+    const int64_t words = in_dim / 8;
+    const int64_t groups = in_dim / 64;
+    for (int64_t item = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; item < n_items;
+         item += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t o = item / n_tb;
+        const int64_t r0 = (item - o * n_tb) * 4;
+        const int nr = (int)(nb - r0 < 4 ? nb - r0 : 4);
+        const uint32_t* wr = w + o * words;
+        const uint16_t* sr = s + o * groups;
+        const uint16_t* br = b + o * groups;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int64_t wi = lane; wi < words; wi += 32) {
+            const uint32_t wd = __ldg(wr + wi);
+            const float sv = __bfloat162float(__ushort_as_bfloat16(__ldg(sr + (wi >> 3))));
+            const float bv = __bfloat162float(__ushort_as_bfloat16(__ldg(br + (wi >> 3))));
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (t < nr) {
+                    const float4* xr = reinterpret_cast<const float4*>(x + (r0 + t) * in_dim + wi * 8);
+                    const float4 x0 = __ldg(xr), x1 = __ldg(xr + 1);
+                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    float qd = 0.f, xs = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        qd = fmaf((float)((wd >> (4 * e)) & 15u), xv[e], qd);
+                        xs += xv[e];
+                    }
+                    acc[t] = fmaf(sv, qd, fmaf(bv, xs, acc[t]));
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+        }
+        if (lane < nr) {
+            float v = acc[0];
+#pragma unroll
+            for (int t = 1; t < 4; ++t) v = lane == t ? acc[t] : v;
+            y[(r0 + lane) * out_dim + o] = v;
+        }
     }
     __threadfence();
     grid_dep_launch();
@@ -272,6 +385,20 @@ q4a_status launch_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_pac
     const int64_t n = rows * in_dim / 32;
     return launch_pdl(lowbit_pack_kernel, grid_for(n, 256), 256, stream, reinterpret_cast<uint2*>(w_up),
                       reinterpret_cast<uint32_t*>(w_lo), reinterpret_cast<const uint4*>(w_packed), n);
+}
+
+q4a_status launch_quantize(uint8_t* w_packed, uint16_t* s, uint16_t* b, const float* w, int64_t rows,
+                           int64_t in_dim, cudaStream_t stream) {
+    const int64_t n = rows * (in_dim / kGroup);
+    return launch_pdl(quantize_kernel, grid_for(n, 128), 128, stream, reinterpret_cast<uint4*>(w_packed), s, b,
+                      reinterpret_cast<const float4*>(w), n);
+}
+
+q4a_status launch_gemv_f32x(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b, const float* x,
+                            int64_t nb, int64_t out_dim, int64_t in_dim, cudaStream_t stream) {
+    const int64_t warps = out_dim * ((nb + 3) / 4);
+    return launch_pdl(gemv_f32x_kernel, grid_for(warps * 32, 256), 256, stream, y,
+                      reinterpret_cast<const uint32_t*>(w), s, b, x, nb, out_dim, in_dim);
 }
 
 q4a_status launch_xsum(float* xsum, const uint16_t* x, int64_t nb, int64_t in_dim, cudaStream_t stream) {

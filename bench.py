@@ -490,6 +490,55 @@ def run_kernel_mode(args):
                           "launches_timed": n, "weight_copies": copies}), flush=True)
 
 
+def run_prefill_mode(args):
+    """The prefill helpers: q4a_quantize on the 12288 x 4096 gate|up weights (fp32 in, packed
+    codes + bf16 scales/biases out) and q4a_gemv_f32x on a narrow 64 x 4096 projection at
+    NB = 1, 128 and 512 (fp32 activations). Per-call time from CUDA graphs of back-to-back
+    calls; GB/s = bytes read and written / time."""
+    import torch
+
+    import affine_q4_dequant_gb300 as q4a
+
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    peak, kind = load_peaks()
+    rows, cols = INTER2, HIDDEN
+    w = torch.randn(rows, cols, device=dev, generator=g) * 0.05
+
+    def quant(i):
+        q4a.quantize(w)
+
+    quant(0)
+    torch.cuda.synchronize()
+    us = graph_us(torch, quant, 20)
+    nbytes = rows * cols * 4 + rows * cols / 2 + 2 * rows * (cols // 64) * 2
+    print(json.dumps({"kernel": "q4a_quantize", "shape": f"{rows}x{cols} fp32", "us_per_call": us,
+                      "gbs": nbytes / us / 1e3, "frac_of_peak": nbytes / us / 1e3 / peak, "peak": peak,
+                      "peak_kind": kind}), flush=True)
+    out_dim = 64
+    ws = []
+    for _ in range(8):
+        codes = torch.randint(0, 16, (out_dim, cols), dtype=torch.uint8, device=dev, generator=g)
+        ws.append((q4a.pack(codes), (torch.rand(out_dim, cols // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
+                   (torch.randn(out_dim, cols // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
+    for nb in (1, 128, 512):
+        x = torch.randn(nb, cols, device=dev, generator=g)
+        y = torch.empty(nb, out_dim, device=dev)
+
+        def proj(i):
+            wq, s_, b_ = ws[i % 8]
+            q4a.gemv_f32x(wq, s_, b_, x, out=y)
+
+        proj(0)
+        torch.cuda.synchronize()
+        us = graph_us(torch, proj, 40)
+        nbytes = out_dim * cols * BYTES_PER_WEIGHT + nb * cols * 4 + nb * out_dim * 4
+        print(json.dumps({"kernel": "q4a_gemv_f32x", "shape": f"{cols}->{out_dim}", "nb": nb, "us_per_call": us,
+                          "gbs": nbytes / us / 1e3, "gflops": 2.0 * out_dim * cols * nb / us / 1e3,
+                          "peak": peak, "peak_kind": kind}), flush=True)
+
+
 def graph_us(torch, fn, n, trials=5):
     """Median per-call time of a CUDA graph of n back-to-back fn(i) calls."""
     graph = torch.cuda.CUDAGraph()
@@ -647,7 +696,7 @@ def main():
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe"], default=None,
+    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe", "prefill"], default=None,
                     help="time one GEMV shape per launch instead of the decode-layer step")
     ap.add_argument("--reps", type=int, default=60)
     ap.add_argument("--bits", type=int, choices=[4, 3, 2], default=4,
@@ -657,6 +706,9 @@ def main():
     args = ap.parse_args()
     if args.kernel == "moe":
         run_moe_mode(args)
+        return
+    if args.kernel == "prefill":
+        run_prefill_mode(args)
         return
     if args.kernel:
         run_kernel_mode(args)

@@ -134,6 +134,33 @@ Q4A_API q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, 
                                                  q4a_stream_t stream);
 
 /*
+ * q4a_quantize -- a 4-bit affine quantiser for float weights (a prefill helper; the pages define
+ * none). Per 64-input group, every step in binary32:
+ *     b = bf16(min w),  s = bf16((max w - b) / 15) if max w > b else 0,
+ *     q = clamp(rint((w - b) / s), 0, 15) if s > 0 else 0   (b, s their bfloat16 values)
+ *   w_packed  out  uint8 [rows][in_dim/2] as q4a_pack writes it
+ *   s, b      out  bf16 [rows][in_dim/64]
+ *   w         in   fp32 [rows][in_dim], finite values
+ *   Requires rows >= 1, in_dim % 64 == 0, w and w_packed 16-byte aligned, s and b 2-byte aligned.
+ */
+Q4A_API q4a_status q4a_quantize(uint8_t* w_packed, uint16_t* s, uint16_t* b, const float* w, int64_t rows,
+                                int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_gemv_f32x -- y = W.x straight from fp32 activations, for a few output rows over any number
+ * of activation rows ("BATCH_MSL", hyperconnection.metal fn_qmv_small_b: the narrow projections
+ * of prefill). Code word wi of a row holds elements 8wi .. 8wi+7, element 8wi + e in nibble e;
+ * per word the kernel accumulates s * sum(q x) + b * sum(x) in fp32.
+ *   y        out  fp32 [nb][out_dim]
+ *   w, s, b  in   as q4a_gemv
+ *   x        in   fp32 [nb][in_dim]
+ *   Requires nb >= 1, in_dim % 64 == 0, w and x 16-byte aligned. CUDA cores, not tensor cores:
+ *   meant for narrow outputs; wide ones belong to q4a_gemv.
+ */
+Q4A_API q4a_status q4a_gemv_f32x(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b, const float* x,
+                                 int nb, int64_t out_dim, int64_t in_dim, q4a_stream_t stream);
+
+/*
  * q4a_lowbit_pack -- derived low-bit codes of a packed 4-bit matrix ("BATCH_MSL",
  * quantized_rows.metal fn_q2_rows_h and fn_q3_rows_h: codes q4 >> 2 and q4 >> 1).
  *   w_up      out  uint8 [rows][in_dim/4]: the 2-bit codes q4 >> 2 (also the upper two bits of

@@ -40,6 +40,8 @@ def lib():
     lib.q4a_lowbit_pack.argtypes = [P, P, P, I64, I64, P]
     lib.q4a_gemv_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_gate_up_silu.argtypes = [P, P, P, P, P, I32, I64, I64, P]
+    lib.q4a_quantize.argtypes = [P, P, P, P, I64, I64, P]
+    lib.q4a_gemv_f32x.argtypes = [P, P, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_rmsnorm_gate_up_silu.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
     return lib
 
@@ -207,4 +209,18 @@ def test_gate_up_silu_rejections(lib):
     assert g(A, A, A, A, A, A, 1e-6, 0.0, 33, 64, 512, None) == UNSUP
     assert g(A, A, A, A, A, A, -1.0, 0.0, 1, 64, 512, None) == SHAPE
     assert g(A, A, A, A, A + 4, A, 1e-6, 0.0, 1, 64, 512, None) == ALIGN
+
+
+def test_prefill_rejections(lib):
+    A = 0x1000
+    q = lib.q4a_quantize
+    assert q(None, A, A, A, 4, 64, None) == NULL
+    assert q(A, A, A, A, 0, 64, None) == SHAPE
+    assert q(A, A, A, A, 4, 100, None) == SHAPE
+    assert q(A, A, A, A + 4, 4, 64, None) == ALIGN
+    f = lib.q4a_gemv_f32x
+    assert f(A, A, A, A, None, 1, 8, 64, None) == NULL
+    assert f(A, A, A, A, A, 0, 8, 64, None) == SHAPE
+    assert f(A, A, A, A, A, 1, 8, 96, None) == SHAPE
+    assert f(A, A, A, A, A + 8, 1, 8, 64, None) == ALIGN
 
