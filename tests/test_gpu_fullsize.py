@@ -77,6 +77,33 @@ def test_gate_up_4096x12288(gate_up, nb):
     check(y, y_ref, bound, f"gate_up nb={nb}")
     yf = host(q4a.gemv_rmsnorm(gate_up.w, gate_up.s, gate_up.b, dev(a), dev(nw), eps=1e-6))
     check(yf, y_ref, bound, f"gate_up fused rmsnorm nb={nb}")
+    # the decode layer's first half as bench.py runs it: RMSNorm prologue, silu(gate) * up
+    # epilogue (rows [0, 6144) gate, [6144, 12288) up); bar as in test_gpu_gate_up_silu.py
+    inter = c.out_dim // 2
+    h = host(q4a.gemv_rmsnorm_gate_up_silu(gate_up.w, gate_up.s, gate_up.b, dev(a), dev(nw), eps=1e-6))
+    g, u = y_ref[:, :inter], y_ref[:, inter:]
+    bg, bu = bound[:, :inter], bound[:, inter:]
+    sg = g / (1.0 + np.exp(-g))
+    tol = 1.1 * (np.abs(u) + bu) * bg + (np.abs(sg) + 1.1 * bg) * bu + 2.0 ** -11 * np.abs(sg * u) + 2.0 ** -24
+    check(h.astype(np.float64), sg * u, tol, f"gate_up fused rmsnorm + silu*up nb={nb}")
+    q4a.check_device_error()
+
+
+@pytest.mark.parametrize("nb,bits", [(1, 2), (8, 2), (1, 3), (8, 3)])
+def test_gate_up_4096x12288_lowbit(gate_up, nb, bits):
+    """The derived 2/3-bit codes of the gate|up weights (packed on the device from the 4-bit
+    ones, bit-exact), the product against the oracle's."""
+    c = wl.DENSE_GATE_UP_CASE
+    x = wl.normal_f16(c.config_id, wl.T_X, (nb, c.in_dim))
+    w_up, w_lo = q4a.lowbit_pack(gate_up.w)
+    ref_up = oracle.lowbit_pack2(gate_up.qm.codes)
+    ref_lo = oracle.lowbit_pack3lo(gate_up.qm.codes) if bits == 3 else None
+    assert np.array_equal(host(w_up), ref_up)
+    if bits == 3:
+        assert np.array_equal(host(w_lo), ref_lo)
+    y = host(q4a.gemv_lowbit(bits, w_up, w_lo, gate_up.s, gate_up.b, dev(x)))
+    y_ref, bound = oracle.gemv_lowbit(ref_up, ref_lo, gate_up.qm.scale, gate_up.qm.bias, x)
+    check(y, y_ref, bound, f"gate_up {bits}-bit nb={nb}")
     q4a.check_device_error()
 
 
