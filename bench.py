@@ -40,6 +40,8 @@ import q4a_workloads as wl  # noqa: E402
 HIDDEN, INTER2, INTER = 4096, 12288, 6144         # gate|up = 2 x 6144
 DOWN_IN, DOWN_OUT = 12288, 4096
 BYTES_PER_WEIGHT = 0.5 + 4.0 / 64.0                # codes + bf16 scale and bias per 64
+WORKLOAD = ("dense decode-layer MLP: 4096->2x6144 gate|up (RMSNorm prologue, silu(gate)*up epilogue) + "
+            "12288->4096 down; affine-Q4 group 64")
 METRIC = "achieved HBM GB/s (and % of roofline) per q4a_gemv call vs NB; us/decode-layer"
 
 
@@ -169,11 +171,12 @@ def oracle_sample(seconds_target: float = 12.0):
             a = wl.normal_f32(wl.DENSE_GATE_UP, wl.T_A, (nb, HIDDEN))
             xn, _ = oracle.rmsnorm_f16(a, nw, eps=1e-6)
             y, _ = oracle.gemv(p_gu, qm_gu.scale, qm_gu.bias, xn)
-            h = oracle.silu_mul_f16(np.concatenate([y, y], axis=1).astype(np.float32))
+            h = oracle.silu_mul_f16(y.astype(np.float32))    # 256 gate rows, then 256 up rows
             xd = wl.normal_f16(wl.DENSE_DOWN, wl.T_X, (nb, DOWN_IN))
             oracle.gemv(p_dn, qm_dn.scale, qm_dn.bias, xd)
-            total_bytes += (gemv_bytes(rows_gu, HIDDEN, nb, 4) + gemv_bytes(rows_dn, DOWN_IN, nb, 2)
-                            + h.size * 2)
+            # the same accounting as layer_bytes, for the sampled rows
+            total_bytes += (rows_gu * HIDDEN * BYTES_PER_WEIGHT + nb * HIDDEN * 4 + HIDDEN * 2 + h.size * 2
+                            + gemv_bytes(rows_dn, DOWN_IN, nb, 2))
         reps += 1
         if time.perf_counter() - t0 >= seconds_target:
             break
@@ -198,8 +201,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "dense decode-layer MLP 4096->12288 gate|up (RMSNorm fused) + silu*up + "
-                               "12288->4096 down, affine-Q4 group 64", "nbs": args.nbs},
+        "config": {"workload": WORKLOAD, "nbs": [int(v) for v in args.nbs.split(",")]},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -370,8 +372,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xu4->f32", "data": "synthetic",
-        "config": {"workload": "dense decode-layer MLP: 4096->2x6144 gate|up (RMSNorm prologue, "
-                               "silu(gate)*up epilogue) + 12288->4096 down; affine-Q4 group 64",
+        "config": {"workload": WORKLOAD,
                    "step": "per NB: the decode layer on each of the weight sets, then the same "
                            "gate|up and down launches as one back-to-back chain per kind",
                    "nbs": nbs, "layers_cycled": L,
