@@ -647,7 +647,8 @@ static uint16_t bf16_round(float f)
 
 /* A 4-bit affine quantiser for float weights. The pages never define one; this is the plain
  * min/max reading, every step in binary32 (the precision that decides the integer codes):
- *   b = bf16(min_g w),  s = bf16((max_g w - b) / 15) when max_g w > b, else 0,
+ *   b = bf16(min_g w) (a zero minimum stored as +0),  s = bf16((max_g w - b) / 15) when
+ *   max_g w > b, else 0,
  *   q = clamp(rint((w - b) / s), 0, 15) when s > 0, else 0,
  * with b and s their bfloat16 values, rint rounding half to even. Writes the packed codes
  * [rows][in_dim/2] (as q4o_pack), s and b [rows][in_dim/64]. w must be finite. */
@@ -664,7 +665,7 @@ Q4O_EXPORT void q4o_quantize(uint8_t* packed, uint16_t* s, uint16_t* b, const fl
                 if (wg[i] < mn) mn = wg[i];
                 if (wg[i] > mx) mx = wg[i];
             }
-            const uint16_t bb = bf16_round(mn);
+            const uint16_t bb = bf16_round(mn == 0.0f ? 0.0f : mn);   /* a zero minimum is +0 */
             const float bf = (float)bf16_value(bb);
             const float range = mx - bf;
             const uint16_t sb = range > 0.0f ? bf16_round(range / 15.0f) : (uint16_t)0;

@@ -632,3 +632,13 @@ def test_gemv_f32x_matches_the_fp16_product_on_fp16_values():
         for o in range(5):
             ref = sum((sf[o, i // 64] * codes[o, i] + bf[o, i // 64]) * float(x[r, i]) for i in range(128))
             assert abs(y[r, o] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_quantize_zero_minimum_is_positive_zero():
+    w = np.zeros((2, 64), np.float32)
+    w[0, 5] = 1.5
+    w[1, :] = -0.0
+    w[1, 7] = 3.0
+    _, s, b = oracle.quantize(w)
+    assert b[0, 0] == 0 and b[1, 0] == 0 and s[0, 0] == 0x3DCD and s[1, 0] == 0x3E4D
+
