@@ -89,50 +89,64 @@ __global__ void lowbit_pack_kernel(uint2* __restrict__ w2, uint32_t* __restrict_
     grid_dep_launch();
 }
 
-// Min/max quantiser, one thread per 64-input group, every step in binary32 (it decides the
-// integer codes): b = bf16(min), s = bf16((max - b) / 15) when max > b, else 0, and
+// Min/max quantiser, every step in binary32 (it decides the integer codes):
+// b = bf16(min), s = bf16((max - b) / 15) when max > b, else 0, and
 // q = clamp(rint((w - b) / s), 0, 15) (0 when s = 0), with b and s their bfloat16 values.
-__global__ void quantize_kernel(uint4* __restrict__ packed, uint16_t* __restrict__ s_out,
+// Four lanes per 64-input group: lane j loads float4 number 4k + j of the group (k = 0..3), so
+// the four lanes of a group read 64 contiguous bytes per load; the group's min and max meet
+// over two xor shuffles, and each lane writes the two packed bytes of each of its vectors.
+__global__ void quantize_kernel(uint8_t* __restrict__ packed, uint16_t* __restrict__ s_out,
                                 uint16_t* __restrict__ b_out, const float4* __restrict__ w, int64_t n_groups) {
     grid_dep_wait();
-    for (int64_t gi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; gi < n_groups;
-         gi += (int64_t)gridDim.x * blockDim.x) {
-        float v[64];
+    const int j = threadIdx.x & 3;
+    const int64_t n_threads = n_groups * 4;
+    // warp-uniform trip count (the shuffles take every lane); lanes past the end load zeros
+    for (int64_t ti = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; ti - (threadIdx.x & 31) < n_threads;
+         ti += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t gi = ti >> 2;
+        const bool live = gi < n_groups;
+        float4 v[4];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float4 f = w[gi * 16 + k];
-            v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
-        }
-        float mn = v[0], mx = v[0];
+        for (int k = 0; k < 4; ++k)
+            v[k] = live ? w[gi * 16 + 4 * k + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mn = v[0].x, mx = v[0].x;
 #pragma unroll
-        for (int i = 1; i < 64; ++i) {
-            mn = v[i] < mn ? v[i] : mn;
-            mx = v[i] > mx ? v[i] : mx;
+        for (int k = 0; k < 4; ++k) {
+            mn = fminf(fminf(fminf(fminf(mn, v[k].x), v[k].y), v[k].z), v[k].w);
+            mx = fmaxf(fmaxf(fmaxf(fmaxf(mx, v[k].x), v[k].y), v[k].z), v[k].w);
         }
-        const __nv_bfloat16 bb = __float2bfloat16_rn(mn);
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        }
+        // a zero minimum is stored as +0 (min/max leave the sign of a zero undefined)
+        const __nv_bfloat16 bb = __float2bfloat16_rn(mn == 0.0f ? 0.0f : mn);
         const float bf = __bfloat162float(bb);
         const float range = __fsub_rn(mx, bf);
         const __nv_bfloat16 sb = range > 0.0f ? __float2bfloat16_rn(__fdiv_rn(range, 15.0f)) : __float2bfloat16_rn(0.0f);
         const float sf = __bfloat162float(sb);
-        uint32_t words[8];
+        if (!live) continue;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            uint32_t wd = 0u;
+        for (int k = 0; k < 4; ++k) {
+            const float e[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            uint32_t q[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                uint32_t q = 0u;
+            for (int t = 0; t < 4; ++t) {
+                q[t] = 0u;
                 if (sf > 0.0f) {
-                    const float t = rintf(__fdiv_rn(__fsub_rn(v[8 * k + e], bf), sf));
-                    q = t < 0.0f ? 0u : (t > 15.0f ? 15u : (uint32_t)t);
+                    const float r = rintf(__fdiv_rn(__fsub_rn(e[t], bf), sf));
+                    q[t] = r < 0.0f ? 0u : (r > 15.0f ? 15u : (uint32_t)r);
                 }
-                wd |= q << (4 * e);   // element 8k + e: nibble e of word k (low nibble first per byte)
             }
-            words[k] = wd;
+            // elements 4(4k + j) .. +3: bytes 2(4k + j) and 2(4k + j) + 1 of the group's 32
+            const uint16_t two = (uint16_t)(q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12));
+            *reinterpret_cast<uint16_t*>(packed + gi * 32 + 2 * (4 * k + j)) = two;
         }
-        packed[gi * 2] = make_uint4(words[0], words[1], words[2], words[3]);
-        packed[gi * 2 + 1] = make_uint4(words[4], words[5], words[6], words[7]);
-        s_out[gi] = __bfloat16_as_ushort(sb);
-        b_out[gi] = __bfloat16_as_ushort(bb);
+        if (j == 0) {
+            s_out[gi] = __bfloat16_as_ushort(sb);
+            b_out[gi] = __bfloat16_as_ushort(bb);
+        }
     }
     __threadfence();
     grid_dep_launch();
@@ -390,7 +404,7 @@ q4a_status launch_lowbit_pack(uint8_t* w_up, uint8_t* w_lo, const uint8_t* w_pac
 q4a_status launch_quantize(uint8_t* w_packed, uint16_t* s, uint16_t* b, const float* w, int64_t rows,
                            int64_t in_dim, cudaStream_t stream) {
     const int64_t n = rows * (in_dim / kGroup);
-    return launch_pdl(quantize_kernel, grid_for(n, 128), 128, stream, reinterpret_cast<uint4*>(w_packed), s, b,
+    return launch_pdl(quantize_kernel, grid_for(4 * n, 256), 256, stream, w_packed, s, b,
                       reinterpret_cast<const float4*>(w), n);
 }
 

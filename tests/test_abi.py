@@ -224,3 +224,10 @@ def test_prefill_rejections(lib):
     assert f(A, A, A, A, A, 1, 8, 96, None) == SHAPE
     assert f(A, A, A, A, A + 8, 1, 8, 64, None) == ALIGN
 
+
+def test_gemv_batch_limits(lib):
+    A = 0x1000
+    # 9 groups are not tensor-core eligible: the GEMV kernel takes at most 256 rows
+    assert lib.q4a_gemv(A, A, A, A, A, 257, 64, 576, None) == UNSUP
+    assert lib.q4a_gemv(A, A, A, A, A, 0, 64, 576, None) == SHAPE
+

@@ -99,6 +99,9 @@ GEMV_CASES = [
     (24, 12288, 2),     # long rows, cluster of 4
     (17, 12288, 16),    # long rows, cluster of 8
     (2000, 256, 4),     # many tiles per cluster
+    (40, 131072, 1),    # 2048 groups per row: an 8-CTA K split with 256-group slices
+    (20, 576, 63),      # the widest batch below the tensor-core path (two segments)
+    (10, 576, 256),     # 9 groups keep NB 256 on the GEMV kernel: eight 32-row segments
 ]
 
 

@@ -46,6 +46,17 @@ def test_quantize_bit_exact(rows, in_dim):
     assert np.array_equal(bits16(b), b_ref)
 
 
+def test_quantize_signed_zero_minimum():
+    w = np.abs(np.random.default_rng(3).normal(0, 1, (3, 128))).astype(np.float32)
+    w[0, :64:2] = -0.0                    # minimum -0 and +0 in one group
+    w[1, 64:] = 0.0
+    w[2, 3] = -0.0
+    packed, s, b = q4a.quantize(dev(w))
+    p_ref, s_ref, b_ref = oracle.quantize(w)
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+    assert np.array_equal(bits16(s), s_ref) and np.array_equal(bits16(b), b_ref)
+
+
 @pytest.mark.parametrize("out_dim,in_dim,nb", [(64, 4096, 1), (16, 2048, 7), (3, 640, 33), (256, 512, 128),
                                                (5, 12288, 2)])
 def test_gemv_f32x_matches_oracle(out_dim, in_dim, nb):
