@@ -99,6 +99,12 @@ Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_d
  *   x        in   fp16 [nb][in_dim]
  *   Requires nb >= 1, out_dim >= 1 (any value, odd included), in_dim >= 64,
  *   in_dim % 64 == 0; w and x 16-byte aligned; s and b 2-byte aligned.
+ *   The GEMV kernel (NB < 64, or rows not eligible for the tensor-core path) keeps a CTA's
+ *   K-slice of the activations and of the row block's scales and biases in shared memory:
+ *   rows longer than that budget allows, even split across 8 CTAs, return
+ *   Q4A_ERR_UNSUPPORTED before any launch. Every in_dim up to 98304 runs at NB 1, up to
+ *   65536 at NB <= 4, up to 16384 at NB <= 16 and up to 4096 at any NB (8192, 12288 and
+ *   16384 run at any NB too).
  *   ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b over quantized_rows.metal
  *   fn_q4_rows_h; experts.metal fn_moe_down_b for the two-rows-per-pass form.)
  */
