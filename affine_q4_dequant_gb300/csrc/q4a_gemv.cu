@@ -388,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* sbfull_b = bars + 2 * S;    // [2]  a row block's scales/biases landed
     uint64_t* sbempty_b = bars + 2 * S + 2;  // [2] every consumer warp is done with them
     uint64_t* rawfull_b = bars + 2 * S + 4;  // [2] raw mode: a row block's raw scales/biases landed
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 6);
+    uint64_t* rawempty_b = bars + 2 * S + 6; // [2] raw mode: the consumers rearranged them
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(sbfull_b + q), 1);
             mbar_init(smem_addr(sbempty_b + q), kConsumerWarps);
             mbar_init(smem_addr(rawfull_b + q), 1);
+            mbar_init(smem_addr(rawempty_b + q), 1);
         }
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -485,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const int nsb = (int)L.n_sb;
                 const int q = blk % nsb;
-                if (blk >= nsb) mbar_wait(smem_addr(sbempty_b + q), (uint32_t)(blk / nsb - 1) & 1u, abort_flag);
+                // (raw mode: the consumers write the rearranged scales themselves)
+                if (blk >= nsb && p.sb_mode != kSbRaw)
+                    mbar_wait(smem_addr(sbempty_b + q), (uint32_t)(blk / nsb - 1) & 1u, abort_flag);
                 uint8_t* sdst = sbuf + (size_t)q * L.sb_buf;
                 const uint32_t bar = smem_addr(sbfull_b + q);
                 if (p.sb_mode == kSbTma) {
@@ -510,28 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else if (p.sb_mode == kSbRaw) {
-                    {   // the next row block's raw scales/biases, while this one is rearranged
-                        int t2 = t;
-                        Job jn;
-                        if (next_job(p, t2, t_end, jn)) raw_issue(jn, (blk + 1) & 1);
+                    // the next row block's raw scales/biases, into the buffer the consumers
+                    // finished rearranging a row block ago (they rearrange this one)
+                    int t2 = t;
+                    Job jn;
+                    if (next_job(p, t2, t_end, jn)) {
+                        const int nbuf = (blk + 1) & 1;
+                        if (blk + 1 >= 2)
+                            mbar_wait(smem_addr(rawempty_b + nbuf), (uint32_t)((blk + 1) / 2 - 1) & 1u, abort_flag);
+                        raw_issue(jn, nbuf);
                     }
-                    mbar_wait(smem_addr(rawfull_b + (blk & 1)), (uint32_t)(blk >> 1) & 1u, abort_flag);
-                    const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(raw + (size_t)(blk & 1) * 2u * L.raw_elems * 2u);
-                    const int64_t e0 = trow0 * p.groups;
-                    const int off = (int)(e0 - (e0 & ~(int64_t)7));
-                    const int gpad = (gsz + 15) / 16 * 16;   // zero groups up to the next 16-group block
-                    for (int r = lane; r < rows_valid; r += 32) {
-                        const uint16_t* srw = rs_ + off + r * gsz;
-                        for (int k = 0; k < gpad; ++k) {
-                            const uint32_t o = (uint32_t)(((k >> 6) * MT * 16 + r) * 128) +
-                                               ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
-                            const bool in = k < gsz;
-                            *reinterpret_cast<uint16_t*>(sdst + o) = in ? srw[k] : (uint16_t)0;
-                            *reinterpret_cast<uint16_t*>(sdst + L.sb_pitch + o) = in ? srw[L.raw_elems + k] : (uint16_t)0;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar);
                 } else {
                     // element copies into the swizzled layout (full K: one CTA per cluster);
                     // groups up to the next 16-group block are zeroed for the bias contraction
@@ -676,7 +668,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) acc[mi][nt][k] = 0.f;
 
             const int q = blk % (int)L.n_sb;
-            mbar_wait(smem_addr(sbfull_b + q), (uint32_t)(blk / (int)L.n_sb) & 1u, abort_flag);
+            if (p.sb_mode == kSbRaw) {
+                // Rearrange the row block's raw [rows][groups] scales and biases into the
+                // swizzled [64-group chunk][row][128 B] layout: one thread per (scales | biases,
+                // row, 8-group granule), one 16-byte store each; groups up to the next 16-group
+                // block are zeros for the bias contraction. Every warp of the previous row block
+                // has passed its epilogue barrier, so the buffer is free.
+                mbar_wait(smem_addr(rawfull_b + (blk & 1)), (uint32_t)(blk >> 1) & 1u, abort_flag);
+                const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(smem + L.raw + (size_t)(blk & 1) * 2u * L.raw_elems * 2u);
+                uint8_t* sdst = sbuf + (size_t)q * L.sb_buf;
+                const int64_t e0 = ((int64_t)sg.row0 + (int64_t)j.tile * 16) * p.groups;
+                const int off = (int)(e0 - (e0 & ~(int64_t)7));
+                const int ngr = (gsz + 15) / 16 * 2;                 // 8-group granules, padded
+                const int rv = (int)llmin((int64_t)j.ntile * 16, p.out_dim - (int64_t)j.tile * 16);
+                const int items = 2 * rv * ngr;
+                for (int it2 = ctid; it2 < items; it2 += kConsumerWarps * 32) {
+                    const int isb = it2 >= rv * ngr;
+                    const int rest = it2 - isb * rv * ngr;
+                    const int r = rest / ngr;
+                    const int u = rest - r * ngr;
+                    const uint16_t* src = rs_ + (size_t)isb * L.raw_elems + off + r * gsz;
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k0 = 8 * u + 2 * e;
+                        const uint32_t lo = k0 < gsz ? (uint32_t)src[k0] : 0u;
+                        const uint32_t hi = k0 + 1 < gsz ? (uint32_t)src[k0 + 1] : 0u;
+                        pk[e] = lo | (hi << 16);
+                    }
+                    const uint32_t o = (uint32_t)((((u >> 3) * MT * 16) + r) * 128) + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sdst + (size_t)isb * L.sb_pitch + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                consumer_sync();
+                if (ctid == 0) mbar_arrive(smem_addr(rawempty_b + (blk & 1)));
+            } else {
+                mbar_wait(smem_addr(sbfull_b + q), (uint32_t)(blk / (int)L.n_sb) & 1u, abort_flag);
+            }
             const uint8_t* sbs = sbuf + (size_t)q * L.sb_buf;         // scales
             const uint8_t* sbb = sbs + L.sb_pitch;                    // biases
             const uint32_t s_blk = smem_addr(sbs) + s_lane;

@@ -99,8 +99,8 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     // a row block's elements plus up to 7 in front (the box start is rounded down to 16 bytes)
     L.raw_elems = sb_mode == kSbRaw ? align_up(rows * (uint32_t)gs + 7u, (uint32_t)kRawBox) : 0u;
     L.bars = align_up(L.raw + 2u * 2u * L.raw_elems * 2u, 8);
-    // full[stages] empty[stages] sbfull[2] sbempty[2] rawfull[2], then the abort flag
-    L.total = L.bars + (2u * (uint32_t)stages + 6u) * 8u + 16u;
+    // full[stages] empty[stages] sbfull[2] sbempty[2] rawfull[2] rawempty[2], then the abort flag
+    L.total = L.bars + (2u * (uint32_t)stages + 8u) * 8u + 16u;
     return L;
 }
 
