@@ -32,7 +32,7 @@ constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation
 //   kSbTma   2D TMA boxes of 64 groups x rows (groups % 8 == 0, 16-byte aligned bases)
 //   kSbRaw   the row block's [rows][groups] scales (and biases) are contiguous: 1D TMA boxes
 //            of 256 elements fetch them, one row block ahead, into a raw staging buffer,
-//            and the producer lanes rearrange them in shared memory (16-byte aligned bases,
+//            and the consumer warps rearrange them in shared memory (16-byte aligned bases,
 //            any group count up to a staging budget; full K only)
 //   kSbPlain producer lanes copy element by element (anything else; full K only)
 enum SbMode : int { kSbTma = 0, kSbRaw = 1, kSbPlain = 2 };
