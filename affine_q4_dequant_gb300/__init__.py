@@ -26,8 +26,9 @@ from . import _build
 
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
-    "gemv_rmsnorm_grouped",
-    "silu_mul_xsum", "moe_combine", "check_device_error", "STATUS", "MAX_SEGMENTS",
+    "gemv_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "lowbit_pack",
+    "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error",
+    "STATUS", "MAX_SEGMENTS",
 ]
 
 MAX_SEGMENTS = 512
