@@ -92,19 +92,27 @@ def _check(fn: str, status: int) -> None:
         raise Q4AError(fn, status, detail)
 
 
-def _stream(stream=None) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _dev(t: torch.Tensor, name: str, dtypes) -> ctypes.c_void_p:
+def _stream(stream=None) -> int:
+    """The cudaStream_t to launch on: the given torch stream, else the current stream of the
+    current device (a plain integer handle; the call happens per launch, so it stays cheap)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 _U8 = (torch.uint8,)
