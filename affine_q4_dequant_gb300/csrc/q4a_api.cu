@@ -235,6 +235,8 @@ q4a_status q4a_gemv_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* 
     if (st != Q4A_OK) return st;
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(h, 2))
         return Q4A_ERR_ALIGN;
+    // the fused row blocks fetch the gate and up rows' scales with 2D TMA boxes only
+    if (in_dim % 512 != 0 || !aligned(s, 16) || !aligned(b, 16)) return Q4A_ERR_UNSUPPORTED;
     std::vector<Segment> segs;
     push_segments(segs, 0, 0, nb);
     if ((int)segs.size() > kDenseMaxSeg) return Q4A_ERR_UNSUPPORTED;
@@ -265,6 +267,7 @@ q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, const ui
     if (!aligned(w, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(s, 2) ||
         !aligned(b, 2) || !aligned(h, 2))
         return Q4A_ERR_ALIGN;
+    if (in_dim % 512 != 0 || !aligned(s, 16) || !aligned(b, 16)) return Q4A_ERR_UNSUPPORTED;
     std::vector<Segment> segs;
     push_segments(segs, 0, 0, nb);
     GemvLaunch L = {};

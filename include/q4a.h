@@ -122,7 +122,9 @@ Q4A_API q4a_status q4a_gemv(float* y, const uint8_t* w, const uint16_t* s, const
  *   s, b   in   bf16 [2 * inter][in_dim/64], same row order
  *   x      in   fp16 [nb][in_dim]
  *   Requires nb in 1..256, inter >= 1 and inter % 16 == 0, in_dim % 64 == 0; w and x 16-byte
- *   aligned, s, b and h 2-byte aligned. Always runs on the GEMV kernel.
+ *   aligned, s, b and h 2-byte aligned. Always runs on the GEMV kernel, whose fused row blocks
+ *   fetch scales and biases with 2D TMA boxes only: in_dim % 512 != 0, or s / b not 16-byte
+ *   aligned, returns Q4A_ERR_UNSUPPORTED.
  */
 Q4A_API q4a_status q4a_gemv_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s, const uint16_t* b,
                                          const uint16_t* x, int nb, int64_t inter, int64_t in_dim,

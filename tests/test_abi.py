@@ -205,10 +205,13 @@ def test_gate_up_silu_rejections(lib):
     assert f(A, A, A, A, A, 1, 64, 500, None) == SHAPE      # in_dim % 64
     assert f(A, A, A, A, A, 257, 64, 512, None) == UNSUP
     assert f(A + 1, A, A, A, A, 1, 64, 512, None) == ALIGN
+    assert f(A, A, A, A, A, 1, 64, 576, None) == UNSUP       # 9 groups: no 2D scale boxes
+    assert f(A, A, A + 2, A, A, 1, 64, 512, None) == UNSUP   # scales not 16-byte aligned
     g = lib.q4a_gemv_rmsnorm_gate_up_silu
     assert g(A, A, A, A, A, A, 1e-6, 0.0, 33, 64, 512, None) == UNSUP
     assert g(A, A, A, A, A, A, -1.0, 0.0, 1, 64, 512, None) == SHAPE
     assert g(A, A, A, A, A + 4, A, 1e-6, 0.0, 1, 64, 512, None) == ALIGN
+    assert g(A, A, A, A, A, A, 1e-6, 0.0, 1, 64, 640, None) == UNSUP
 
 
 def test_prefill_rejections(lib):
