@@ -4,7 +4,9 @@
  *
  * TEST INFRASTRUCTURE, NOT THE PRODUCT. Only the test-suite, the smoke check
  * and the benchmark's CPU-baseline leg load this file's library. It is plain,
- * single-threaded C computing in IEEE double precision. It shares no code,
+ * single-threaded C computing in IEEE double precision (the quantiser alone
+ * works in binary32: those steps decide integer codes, and both sides take
+ * them in the same precision). It shares no code,
  * header, table, constant generator or helper with the CUDA library: its own
  * binary16 / bfloat16 decoders, its own nibble extraction, its own loops.
  *
