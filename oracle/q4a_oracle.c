@@ -23,7 +23,7 @@
  *                (host_route_softmax_topk with its denominator floor,
  *                f32_to_bf16_rne).
  *
- * What the method computes (spec contract, restated):
+ * What the method computes (restated):
  *   W is [out][in] with 4-bit codes q in 0..15; byte k of a packed row holds
  *   element 2k in its low nibble and element 2k+1 in its high nibble. Every
  *   run of 64 inputs (a group g) has a bfloat16 scale s[o][g] and bias
@@ -101,7 +101,7 @@ static uint16_t half_round(double v)
 }
 
 /* The code of element i of a packed row: low nibble of byte i/2 for even i,
- * high nibble for odd i (spec layout; [BATCH_MSL] fn_q4_rows_h pairs the
+ * high nibble for odd i (the packed layout; [BATCH_MSL] fn_q4_rows_h pairs the
  * low nibbles with the even x stream and the high nibbles with the odd one). */
 static int code_at(const uint8_t* row, int64_t i)
 {
