@@ -60,6 +60,7 @@ def _load():
             "q4o_moe_combine": (None, [P, P, P, P, P, P, P, P, P, I, I, I, I]),
             "q4o_gemv_silu": (None, [P, P, P, P, P, P, P, D, I, I, I]),
             "q4o_rmsnorm_groups_f16": (None, [P, P, P, P, D, D, I, I, I]),
+            "q4o_inject_rmsnorm_groups_f16": (None, [P, P, P, P, P, P, D, D, I, I, I]),
             "q4o_lowbit_pack2": (None, [P, P, I, I]),
             "q4o_lowbit_pack3lo": (None, [P, P, I, I]),
             "q4o_lowbit_codes": (None, [P, P, P, I, I]),
@@ -264,6 +265,23 @@ def rmsnorm_groups_f16(x_raw, norm_w, groups: int, eps: float = 1e-6, shift: flo
     _load().q4o_rmsnorm_groups_f16(_p(xn), _p(inv), _p(x_raw), _p(norm_w), float(eps), float(shift), nb, n,
                                    int(groups))
     return xn, inv
+
+
+def inject_rmsnorm_groups_f16(x_raw, out, logit, norm_w, groups: int, eps: float = 1e-6, shift: float = 0.0):
+    """Hyper-connection injection, then the grouped RMSNorm ([BATCH_MSL] hyperconnection.metal
+    fn_inject_b; fn_norm_prep_b with inject = 1): stream g of row r (inputs g*n .. g*n+n-1,
+    n = in_dim / groups) becomes x + out[r] * 2 sigmoid(logit[r][g] / groups), then each stream
+    is normalised on its own. x_raw fp32 [nb][in_dim], out fp32 [nb][n], logit fp32
+    [nb][groups]. Returns (xn fp16 bits [nb][in_dim], x_new float64 [nb][in_dim])."""
+    x_raw, out, logit, norm_w = (_c(x_raw, np.float32), _c(out, np.float32), _c(logit, np.float32),
+                                 _c(norm_w, np.uint16))
+    nb, in_dim = x_raw.shape
+    assert out.shape == (nb, in_dim // groups) and logit.shape == (nb, groups)
+    xn = np.empty((nb, in_dim), np.uint16)
+    x_new = np.empty((nb, in_dim), np.float64)
+    _load().q4o_inject_rmsnorm_groups_f16(_p(xn), _p(x_new), _p(x_raw), _p(out), _p(logit), _p(norm_w), float(eps),
+                                          float(shift), nb, in_dim, int(groups))
+    return xn, x_new
 
 
 # ---- derived low-bit codes ([BATCH_MSL] fn_q2_rows_h, fn_q3_rows_h) ------------------------

@@ -15,7 +15,7 @@
  *                library. Sections used: quantized_rows.metal (fn_q4_rows_h,
  *                fn_q4_2rows_h: the affine-Q4 row dot products),
  *                hyperconnection.metal (fn_group_norm_b, fn_norm_prep_b,
- *                fn_qmv_silu_b), experts.metal (fn_topk_softmax_b,
+ *                fn_inject_b, fn_qmv_silu_b), experts.metal (fn_topk_softmax_b,
  *                fn_moe_gate_up_b, fn_moe_act_b, fn_moe_down_b),
  *                expert_gemm.metal (fn_expert_qmm) and the prefill helper
  *                fn_qmv_small_b (explicit nibble order and affine form).
@@ -487,6 +487,33 @@ Q4O_EXPORT void q4o_rmsnorm_groups_f16(uint16_t* xn, double* inv_rms, const floa
                 inv_rms[r * groups + g] = inv;
             for (int64_t i = 0; i < n; i++)
                 xn[r * in_dim + g * n + i] = half_round((double)xs[i] * inv * (bf16_value(w[g * n + i]) + shift));
+        }
+}
+
+/* [BATCH_MSL] hyperconnection.metal fn_inject_b, and fn_norm_prep_b with inject = 1. A row
+ * holds `groups` hyper-connection streams of n = in_dim / groups inputs each; stream g of row r
+ * first receives the layer output scaled by twice a sigmoid of its mixing logit,
+ *     x'[r][g n + i] = x[r][g n + i] + out[r][i] * 2 / (1 + e^(-logit[r][g] / groups)),
+ * and is then RMS-normalised on its own, exactly as q4o_rmsnorm_groups_f16 does:
+ *     xn[r][g n + i] = fp16( x'[r][g n + i] * rsqrt(mean_i x'[r][g n + i]^2 + eps) * (w[g n + i] + shift) ).
+ * Every step in double; x_new receives x'. */
+Q4O_EXPORT void q4o_inject_rmsnorm_groups_f16(uint16_t* xn, double* x_new, const float* x, const float* out,
+                                              const float* logit, const uint16_t* w, double eps, double shift,
+                                              int64_t nb, int64_t in_dim, int64_t groups)
+{
+    const int64_t n = in_dim / groups;
+    for (int64_t r = 0; r < nb; r++)
+        for (int64_t g = 0; g < groups; g++) {
+            const double wgt = 2.0 / (1.0 + exp(-(double)logit[r * groups + g] / (double)groups));
+            double* xs = x_new + r * in_dim + g * n;
+            double ss = 0.0;
+            for (int64_t i = 0; i < n; i++) {
+                xs[i] = (double)x[r * in_dim + g * n + i] + (double)out[r * n + i] * wgt;
+                ss += xs[i] * xs[i];
+            }
+            const double inv = 1.0 / sqrt(ss / (double)n + eps);
+            for (int64_t i = 0; i < n; i++)
+                xn[r * in_dim + g * n + i] = half_round(xs[i] * inv * (bf16_value(w[g * n + i]) + shift));
         }
 }
 

@@ -495,6 +495,72 @@ def test_rmsnorm_groups_unit_rms_per_segment():
     assert np.allclose(np.sqrt((v ** 2).mean(axis=2)), 1.0, rtol=2e-3)
 
 
+# ---- NEXT-3 injection ("BATCH_MSL" hyperconnection.metal fn_inject_b, fn_norm_prep_b inject = 1) ----
+
+def test_inject_zero_logit_adds_out_once():
+    """2 sigmoid(0) = 1 exactly: every stream receives out itself. With small integers x + out is
+    exact in binary32, so the normalisation equals the pinned grouped RMSNorm of x + out."""
+    rng = np.random.default_rng(61)
+    nb, groups, n = 3, 4, 64
+    x = rng.integers(-8, 9, (nb, groups * n)).astype(np.float32)
+    out = rng.integers(-8, 9, (nb, n)).astype(np.float32)
+    w = wl.norm_weight(0, 2, groups * n)
+    xn, x_new = oracle.inject_rmsnorm_groups_f16(x, out, np.zeros((nb, groups), np.float32), w, groups, eps=1e-6,
+                                                 shift=0.25)
+    summed = x + np.tile(out, (1, groups))
+    assert np.array_equal(x_new, summed.astype(np.float64))
+    ref, _ = oracle.rmsnorm_groups_f16(summed, w, groups, eps=1e-6, shift=0.25)
+    assert np.array_equal(xn, ref)
+
+
+def test_inject_zero_out_is_the_grouped_norm():
+    rng = np.random.default_rng(62)
+    x = rng.normal(0, 2, (2, 384)).astype(np.float32)
+    logit = rng.normal(0, 3, (2, 3)).astype(np.float32)
+    w = wl.norm_weight(0, 3, 384)
+    xn, x_new = oracle.inject_rmsnorm_groups_f16(x, np.zeros((2, 128), np.float32), logit, w, 3)
+    ref, _ = oracle.rmsnorm_groups_f16(x, w, 3)
+    assert np.array_equal(x_new, x.astype(np.float64)) and np.array_equal(xn, ref)
+
+
+def test_inject_weight_closed_forms_per_stream():
+    """Stream g of row r takes the logit of (r, g), divided by the stream count: with
+    logit = groups * ln 3 the weight is 2 * 3/4 = 1.5; a large positive logit saturates at 2 and
+    a large negative one at 0. Rows and streams get different logits (nb != groups), so a
+    transposed index or a sign slip fails."""
+    nb, groups, n = 2, 3, 64
+    x = np.ones((nb, groups * n), np.float32)
+    out = np.full((nb, n), 2.0, np.float32)
+    out[1] = -4.0
+    logit = np.array([[groups * math.log(3.0), 1e4, -1e4],
+                      [0.0, groups * math.log(3.0), 1e4]], np.float32)
+    _, x_new = oracle.inject_rmsnorm_groups_f16(x, out, logit, wl.f32_to_bf16_bits(np.ones(groups * n, np.float32)),
+                                                groups)
+    expect_w = [[2.0 / (1.0 + math.exp(-float(logit[0, 0]) / groups)), 2.0, 0.0],
+                [1.0, 2.0 / (1.0 + math.exp(-float(logit[1, 1]) / groups)), 2.0]]
+    assert expect_w[0][0] == pytest.approx(1.5, rel=1e-6)
+    for r in range(nb):
+        for g in range(groups):
+            seg = x_new[r, g * n:(g + 1) * n]
+            assert np.allclose(seg, 1.0 + float(out[r, 0]) * expect_w[r][g], rtol=1e-12, atol=1e-300), (r, g)
+    # a positive logit weighs the output above 1, a negative one below
+    _, hi = oracle.inject_rmsnorm_groups_f16(x[:1, :n], out[:1], np.array([[0.5]], np.float32),
+                                             wl.f32_to_bf16_bits(np.ones(n, np.float32)), 1)
+    assert hi[0, 0] > 1.0 + 2.0
+
+
+def test_inject_is_linear_in_out_before_the_norm():
+    rng = np.random.default_rng(63)
+    nb, groups, n = 2, 2, 128
+    x = rng.normal(0, 1, (nb, groups * n)).astype(np.float32)
+    o1 = rng.integers(-4, 5, (nb, n)).astype(np.float32)
+    logit = rng.normal(0, 2, (nb, groups)).astype(np.float32)
+    w = wl.norm_weight(0, 4, groups * n)
+    _, a = oracle.inject_rmsnorm_groups_f16(x, o1, logit, w, groups)
+    _, b2 = oracle.inject_rmsnorm_groups_f16(x, 2 * o1, logit, w, groups)
+    assert np.allclose(b2 - x, 2 * (a - x), rtol=1e-12, atol=1e-12)
+
+
 # ---- derived low-bit codes ([BATCH_MSL] fn_q2_rows_h, fn_q3_rows_h) ----------------------
 
 
