@@ -26,7 +26,7 @@ from . import _build
 
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
-    "gemv_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "lowbit_pack",
+    "gemv_rmsnorm_grouped", "gemv_inject_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "decode_mlp", "lowbit_pack",
     "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error",
     "STATUS", "MAX_SEGMENTS",
 ]
@@ -66,10 +66,12 @@ def _load() -> ctypes.CDLL:
         "q4a_gemv_f32x": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_gate_up_silu": (I32, [P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_gate_up_silu": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
+        "q4a_decode_mlp": (I32, [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_grouped": (I32, [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
+        "q4a_gemv_inject_rmsnorm_grouped": (I32, [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
         "q4a_silu_mul_xsum": (I32, [P, P, P, I64, I64, P]),
         "q4a_moe_combine": (I32, [P, P, P, P, I32, I32, I64, I64, P, P, P, P]),
         "q4a_check_device_error": (I32, [P]),
@@ -105,151 +107,244 @@ def _stream(stream=None) -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
-def _dev(t: torch.Tensor, name: str, dtypes) -> int:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype not in dtypes:
-        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return t.data_ptr()
-
-
 _U8 = (torch.uint8,)
 _F16 = (torch.float16, torch.int16, torch.uint16)
 _BF16 = (torch.bfloat16, torch.int16, torch.uint16)
 _F32 = (torch.float32,)
 _I32 = (torch.int32,)
+_ANY = None   # any dtype (prefetch hints)
+_NULL = ctypes.c_void_p(0)
+
+
+def _ptrs(*specs):
+    """Device pointers for specs (tensor, name, dtypes, shape); a spec may be None (a NULL
+    pointer). Every shape is checked first, then dtypes, CUDA residency, contiguity and the
+    device: a mis-shaped buffer would be read or written past its end by the kernels, so it is
+    refused here, before anything launches."""
+    for sp in specs:
+        if sp is None:
+            continue
+        t, name, _, shape = sp
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if shape is not None and tuple(t.shape) != tuple(int(v) for v in shape):
+            raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(int(v) for v in shape)}")
+    dev = None
+    out = []
+    for sp in specs:
+        if sp is None:
+            out.append(_NULL)
+            continue
+        t, name, dtypes, _ = sp
+        if dtypes is not None and t.dtype not in dtypes:
+            raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dev is None:
+            dev = torch.cuda.current_device()
+        if t.device.index != dev:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{dev}")
+        out.append(t.data_ptr())
+    return out
+
+
+def _dims(t: torch.Tensor, name: str, ndim: int = 2):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name}: {t.dim()} dimensions, expected {ndim}")
+    return tuple(int(v) for v in t.shape)
+
+
+def _mat(w, s, b, out_dim: int, in_dim: int, wname="w", sname="s", bname="b", code_cols=None):
+    """Specs of a packed matrix: codes [out_dim][code_cols] (in_dim/2 by default), scales and
+    biases [out_dim][in_dim/64]."""
+    if in_dim % 64 != 0:
+        raise ValueError(f"in_dim {in_dim} is not a multiple of 64")
+    code_cols = in_dim // 2 if code_cols is None else code_cols
+    return [(w, wname, _U8, (out_dim, code_cols)), (s, sname, _BF16, (out_dim, in_dim // 64)),
+            (b, bname, _BF16, (out_dim, in_dim // 64))]
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
 
 
 def pack(codes: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    rows, in_dim = codes.shape
-    if out is None:
-        out = torch.empty((rows, in_dim // 2), dtype=torch.uint8, device=codes.device)
-    _check("q4a_pack", _lib.q4a_pack(_dev(out, "out", _U8), _dev(codes, "codes", _U8), rows, in_dim,
-                                     _stream(stream)))
-    return out
-
-
-def gemv_gate_up_silu(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """h = fp16(silu(W_gate x) * (W_up x)); w holds the gate rows, then the up rows."""
-    nb, in_dim = x.shape
-    inter = w.shape[0] // 2
-    if out is None:
-        out = torch.empty((nb, inter), dtype=torch.float16, device=x.device)
-    _check("q4a_gemv_gate_up_silu", _lib.q4a_gemv_gate_up_silu(
-        _dev(out, "h", _F16), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x, "x", _F16), nb, inter, in_dim, _stream(stream)))
-    return out
-
-
-def gemv_rmsnorm_gate_up_silu(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
-                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """gemv_gate_up_silu on RMS-normalised fp32 activations (one normalisation group)."""
-    nb, in_dim = x_raw.shape
-    inter = w.shape[0] // 2
-    if out is None:
-        out = torch.empty((nb, inter), dtype=torch.float16, device=x_raw.device)
-    _check("q4a_gemv_rmsnorm_gate_up_silu", _lib.q4a_gemv_rmsnorm_gate_up_silu(
-        _dev(out, "h", _F16), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift), nb, inter,
-        in_dim, _stream(stream)))
-    return out
-
-
-def quantize(w: torch.Tensor, stream=None):
-    """4-bit min/max quantisation of fp32 weights [rows][in]: (packed codes, s bf16, b bf16)."""
-    rows, in_dim = w.shape
-    packed = torch.empty((rows, in_dim // 2), dtype=torch.uint8, device=w.device)
-    s = torch.empty((rows, in_dim // 64), dtype=torch.bfloat16, device=w.device)
-    b = torch.empty((rows, in_dim // 64), dtype=torch.bfloat16, device=w.device)
-    _check("q4a_quantize", _lib.q4a_quantize(_dev(packed, "w_packed", _U8), _dev(s, "s", _BF16),
-                                             _dev(b, "b", _BF16), _dev(w, "w", _F32), rows, in_dim,
-                                             _stream(stream)))
-    return packed, s, b
-
-
-def gemv_f32x(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = W x from fp32 activations (narrow projections of prefill)."""
-    nb, in_dim = x.shape
-    out_dim = w.shape[0]
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
-    _check("q4a_gemv_f32x", _lib.q4a_gemv_f32x(
-        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x, "x", _F32), nb, out_dim, in_dim, _stream(stream)))
-    return out
-
-
-def lowbit_pack(w_packed: torch.Tensor, with_lowest: bool = True, stream=None):
-    """Derived low-bit codes of a packed 4-bit matrix: (w_up [rows][in/4], w_lo [rows][in/8]
-    or None). w_up alone is the 2-bit matrix; w_up with w_lo the 3-bit one."""
-    rows, half = w_packed.shape
-    in_dim = 2 * half
-    w_up = torch.empty((rows, in_dim // 4), dtype=torch.uint8, device=w_packed.device)
-    w_lo = torch.empty((rows, in_dim // 8), dtype=torch.uint8, device=w_packed.device) if with_lowest else None
-    _check("q4a_lowbit_pack", _lib.q4a_lowbit_pack(
-        _dev(w_up, "w_up", _U8), ctypes.c_void_p(0) if w_lo is None else _dev(w_lo, "w_lo", _U8),
-        _dev(w_packed, "w_packed", _U8), rows, in_dim, _stream(stream)))
-    return w_up, w_lo
-
-
-def gemv_lowbit(bits: int, w_up, w_lo, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = W.x with W from derived 2-bit (bits=2, w_lo unused) or 3-bit codes."""
-    out_dim = w_up.shape[0]
-    nb, in_dim = x.shape
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
-    lo = ctypes.c_void_p(0) if (w_lo is None or bits == 2) else _dev(w_lo, "w_lo", _U8)
-    _check("q4a_gemv_lowbit", _lib.q4a_gemv_lowbit(
-        _dev(out, "y", _F32), int(bits), _dev(w_up, "w_up", _U8), lo, _dev(s, "s", _BF16),
-        _dev(b, "b", _BF16), _dev(x, "x", _F16), nb, out_dim, in_dim, _stream(stream)))
+    rows, in_dim = _dims(codes, "codes")
+    out = _empty((rows, in_dim // 2), torch.uint8, codes) if out is None else out
+    po, pc = _ptrs((out, "out", _U8, (rows, in_dim // 2)), (codes, "codes", _U8, None))
+    _check("q4a_pack", _lib.q4a_pack(po, pc, rows, in_dim, _stream(stream)))
     return out
 
 
 def xsum(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    nb, in_dim = x.shape
-    if out is None:
-        out = torch.empty((nb, in_dim // 64), dtype=torch.float32, device=x.device)
-    _check("q4a_xsum", _lib.q4a_xsum(_dev(out, "out", _F32), _dev(x, "x", _F16), nb, in_dim,
-                                     _stream(stream)))
+    nb, in_dim = _dims(x, "x")
+    out = _empty((nb, in_dim // 64), torch.float32, x) if out is None else out
+    po, px = _ptrs((out, "out", _F32, (nb, in_dim // 64)), (x, "x", _F16, None))
+    _check("q4a_xsum", _lib.q4a_xsum(po, px, nb, in_dim, _stream(stream)))
     return out
 
 
 def gemv(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    out_dim = w.shape[0]
-    nb, in_dim = x.shape
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
-    _check("q4a_gemv", _lib.q4a_gemv(_dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16),
-                                     _dev(b, "b", _BF16), _dev(x, "x", _F16), nb, out_dim, in_dim,
-                                     _stream(stream)))
-    return out
-
-
-def gemv_rmsnorm(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
-                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    out_dim = w.shape[0]
-    nb, in_dim = x_raw.shape
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x_raw.device)
-    _check("q4a_gemv_rmsnorm", _lib.q4a_gemv_rmsnorm(
-        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift), nb,
-        out_dim, in_dim, _stream(stream)))
+    """y = W x (fp32 [nb][out_dim]) from fp16 activations x [nb][in_dim]."""
+    out_dim = _dims(w, "w")[0]
+    nb, in_dim = _dims(x, "x")
+    out = _empty((nb, out_dim), torch.float32, x) if out is None else out
+    py, pw, ps, pb, px = _ptrs((out, "y", _F32, (nb, out_dim)), *_mat(w, s, b, out_dim, in_dim), (x, "x", _F16, None))
+    _check("q4a_gemv", _lib.q4a_gemv(py, pw, ps, pb, px, nb, out_dim, in_dim, _stream(stream)))
     return out
 
 
 def gemv_silu(w: torch.Tensor, s: torch.Tensor, b: torch.Tensor, x: torch.Tensor, div: float,
               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y = silu((W.x) / div) elementwise; otherwise as gemv()."""
-    nb, in_dim = x.shape
-    out_dim = w.shape[0]
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x.device)
-    _check("q4a_gemv_silu", _lib.q4a_gemv_silu(
-        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x, "x", _F16), float(div), nb, out_dim, in_dim, _stream(stream)))
+    nb, in_dim = _dims(x, "x")
+    out_dim = _dims(w, "w")[0]
+    out = _empty((nb, out_dim), torch.float32, x) if out is None else out
+    py, pw, ps, pb, px = _ptrs((out, "y", _F32, (nb, out_dim)), *_mat(w, s, b, out_dim, in_dim), (x, "x", _F16, None))
+    _check("q4a_gemv_silu", _lib.q4a_gemv_silu(py, pw, ps, pb, px, float(div), nb, out_dim, in_dim, _stream(stream)))
+    return out
+
+
+def gemv_gate_up_silu(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h = fp16(silu(W_gate x) * (W_up x)); w holds the gate rows, then the up rows."""
+    nb, in_dim = _dims(x, "x")
+    inter = _dims(w, "w")[0] // 2
+    out = _empty((nb, inter), torch.float16, x) if out is None else out
+    ph, pw, ps, pb, px = _ptrs((out, "h", _F16, (nb, inter)), *_mat(w, s, b, 2 * inter, in_dim), (x, "x", _F16, None))
+    _check("q4a_gemv_gate_up_silu", _lib.q4a_gemv_gate_up_silu(ph, pw, ps, pb, px, nb, inter, in_dim,
+                                                               _stream(stream)))
+    return out
+
+
+def gemv_rmsnorm_gate_up_silu(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gemv_gate_up_silu on RMS-normalised fp32 activations (one normalisation group)."""
+    nb, in_dim = _dims(x_raw, "x_raw")
+    inter = _dims(w, "w")[0] // 2
+    out = _empty((nb, inter), torch.float16, x_raw) if out is None else out
+    ph, pw, ps, pb, px, pn = _ptrs((out, "h", _F16, (nb, inter)), *_mat(w, s, b, 2 * inter, in_dim),
+                                   (x_raw, "x_raw", _F32, None), (norm_w, "norm_w", _BF16, (in_dim,)))
+    _check("q4a_gemv_rmsnorm_gate_up_silu", _lib.q4a_gemv_rmsnorm_gate_up_silu(
+        ph, pw, ps, pb, px, pn, float(eps), float(shift), nb, inter, in_dim, _stream(stream)))
+    return out
+
+
+def decode_mlp(w_gu, s_gu, b_gu, x_raw, norm_w, w_dn, s_dn, b_dn, eps: float = 1e-6, shift: float = 0.0,
+               out: torch.Tensor | None = None, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode layer's MLP: h = fp16(silu(W_gate xn) * (W_up xn)) with xn the RMS-normalised
+    x_raw, then y = W_down h (fp32 [nb][hidden]). w_gu holds the gate rows, then the up rows."""
+    nb, hidden = _dims(x_raw, "x_raw")
+    inter = _dims(w_gu, "w_gu")[0] // 2
+    out = _empty((nb, hidden), torch.float32, x_raw) if out is None else out
+    h = _empty((nb, inter), torch.float16, x_raw) if h is None else h
+    py, ph, pgw, pgs, pgb, px, pn, pdw, pds, pdb = _ptrs(
+        (out, "y", _F32, (nb, hidden)), (h, "h", _F16, (nb, inter)),
+        *_mat(w_gu, s_gu, b_gu, 2 * inter, hidden, "w_gu", "s_gu", "b_gu"),
+        (x_raw, "x_raw", _F32, None), (norm_w, "norm_w", _BF16, (hidden,)),
+        *_mat(w_dn, s_dn, b_dn, hidden, inter, "w_dn", "s_dn", "b_dn"))
+    _check("q4a_decode_mlp", _lib.q4a_decode_mlp(py, ph, pgw, pgs, pgb, px, pn, float(eps), float(shift), pdw, pds,
+                                                 pdb, nb, hidden, inter, _stream(stream)))
+    return out
+
+
+def gemv_rmsnorm(w, s, b, x_raw, norm_w, eps: float = 1e-6, shift: float = 0.0,
+                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out_dim = _dims(w, "w")[0]
+    nb, in_dim = _dims(x_raw, "x_raw")
+    out = _empty((nb, out_dim), torch.float32, x_raw) if out is None else out
+    py, pw, ps, pb, px, pn = _ptrs((out, "y", _F32, (nb, out_dim)), *_mat(w, s, b, out_dim, in_dim),
+                                   (x_raw, "x_raw", _F32, None), (norm_w, "norm_w", _BF16, (in_dim,)))
+    _check("q4a_gemv_rmsnorm", _lib.q4a_gemv_rmsnorm(py, pw, ps, pb, px, pn, float(eps), float(shift), nb, out_dim,
+                                                     in_dim, _stream(stream)))
+    return out
+
+
+def gemv_rmsnorm_grouped(w, s, b, x_raw, norm_w, norm_groups: int, eps: float = 1e-6, shift: float = 0.0,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """gemv_rmsnorm with norm_groups equal segments per row, each normalised on its own."""
+    nb, in_dim = _dims(x_raw, "x_raw")
+    out_dim = _dims(w, "w")[0]
+    out = _empty((nb, out_dim), torch.float32, x_raw) if out is None else out
+    py, pw, ps, pb, px, pn = _ptrs((out, "y", _F32, (nb, out_dim)), *_mat(w, s, b, out_dim, in_dim),
+                                   (x_raw, "x_raw", _F32, None), (norm_w, "norm_w", _BF16, (in_dim,)))
+    _check("q4a_gemv_rmsnorm_grouped", _lib.q4a_gemv_rmsnorm_grouped(
+        py, pw, ps, pb, px, pn, float(eps), float(shift), int(norm_groups), nb, out_dim, in_dim, _stream(stream)))
+    return out
+
+
+def gemv_inject_rmsnorm_grouped(w, s, b, x_raw, out, logit, norm_w, norm_groups: int, eps: float = 1e-6,
+                                shift: float = 0.0, y: torch.Tensor | None = None, x_new: torch.Tensor | None = None,
+                                want_x_new: bool = True, stream=None):
+    """Inject out [nb][n] into each of the norm_groups streams of x_raw [nb][n * norm_groups]
+    with weight 2 sigmoid(logit[r][g] / norm_groups), then the grouped RMSNorm and y = W.xn.
+    Returns (y, x_new): x_new is the injected stream (None when want_x_new is False)."""
+    nb, in_dim = _dims(x_raw, "x_raw")
+    out_dim = _dims(w, "w")[0]
+    if norm_groups < 1 or in_dim % norm_groups != 0:
+        raise ValueError(f"in_dim {in_dim} does not split into {norm_groups} streams")
+    y = _empty((nb, out_dim), torch.float32, x_raw) if y is None else y
+    if x_new is None and want_x_new:
+        x_new = _empty((nb, in_dim), torch.float32, x_raw)
+    py, pxn, pw, ps, pb, px, po, pl, pn = _ptrs(
+        (y, "y", _F32, (nb, out_dim)), None if x_new is None else (x_new, "x_new", _F32, (nb, in_dim)),
+        *_mat(w, s, b, out_dim, in_dim), (x_raw, "x_raw", _F32, None), (out, "out", _F32, (nb, in_dim // norm_groups)),
+        (logit, "logit", _F32, (nb, norm_groups)), (norm_w, "norm_w", _BF16, (in_dim,)))
+    _check("q4a_gemv_inject_rmsnorm_grouped", _lib.q4a_gemv_inject_rmsnorm_grouped(
+        py, pxn, pw, ps, pb, px, po, pl, pn, float(eps), float(shift), int(norm_groups), nb, out_dim, in_dim,
+        _stream(stream)))
+    return y, x_new
+
+
+def quantize(w: torch.Tensor, stream=None):
+    """4-bit min/max quantisation of fp32 weights [rows][in]: (packed codes, s bf16, b bf16)."""
+    rows, in_dim = _dims(w, "w")
+    packed = _empty((rows, in_dim // 2), torch.uint8, w)
+    s = _empty((rows, in_dim // 64), torch.bfloat16, w)
+    b = _empty((rows, in_dim // 64), torch.bfloat16, w)
+    pp, ps, pb, pw = _ptrs((packed, "w_packed", _U8, None), (s, "s", _BF16, None), (b, "b", _BF16, None),
+                           (w, "w", _F32, None))
+    _check("q4a_quantize", _lib.q4a_quantize(pp, ps, pb, pw, rows, in_dim, _stream(stream)))
+    return packed, s, b
+
+
+def gemv_f32x(w, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = W x from fp32 activations (narrow projections of prefill)."""
+    nb, in_dim = _dims(x, "x")
+    out_dim = _dims(w, "w")[0]
+    out = _empty((nb, out_dim), torch.float32, x) if out is None else out
+    py, pw, ps, pb, px = _ptrs((out, "y", _F32, (nb, out_dim)), *_mat(w, s, b, out_dim, in_dim), (x, "x", _F32, None))
+    _check("q4a_gemv_f32x", _lib.q4a_gemv_f32x(py, pw, ps, pb, px, nb, out_dim, in_dim, _stream(stream)))
+    return out
+
+
+def lowbit_pack(w_packed: torch.Tensor, with_lowest: bool = True, stream=None):
+    """Derived low-bit codes of a packed 4-bit matrix: (w_up [rows][in/4], w_lo [rows][in/8]
+    or None). w_up alone is the 2-bit matrix; w_up with w_lo the 3-bit one."""
+    rows, half = _dims(w_packed, "w_packed")
+    in_dim = 2 * half
+    w_up = _empty((rows, in_dim // 4), torch.uint8, w_packed)
+    w_lo = _empty((rows, in_dim // 8), torch.uint8, w_packed) if with_lowest else None
+    pu, pl, pp = _ptrs((w_up, "w_up", _U8, None), None if w_lo is None else (w_lo, "w_lo", _U8, None),
+                       (w_packed, "w_packed", _U8, None))
+    _check("q4a_lowbit_pack", _lib.q4a_lowbit_pack(pu, pl, pp, rows, in_dim, _stream(stream)))
+    return w_up, w_lo
+
+
+def gemv_lowbit(bits: int, w_up, w_lo, s, b, x, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = W.x with W from derived 2-bit (bits=2, w_lo unused) or 3-bit codes."""
+    out_dim = _dims(w_up, "w_up")[0]
+    nb, in_dim = _dims(x, "x")
+    out = _empty((nb, out_dim), torch.float32, x) if out is None else out
+    lo = None if (w_lo is None or bits == 2) else (w_lo, "w_lo", _U8, (out_dim, in_dim // 8))
+    py, pw, ps, pb, pl, px = _ptrs((out, "y", _F32, (nb, out_dim)),
+                                   *_mat(w_up, s, b, out_dim, in_dim, "w_up", code_cols=in_dim // 4), lo,
+                                   (x, "x", _F16, None))
+    _check("q4a_gemv_lowbit", _lib.q4a_gemv_lowbit(py, int(bits), pw, pl, ps, pb, px, nb, out_dim, in_dim,
+                                                   _stream(stream)))
     return out
 
 
@@ -259,45 +354,35 @@ def gemv_experts(w_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n
     CUDA int32 tensor or None."""
     expert_ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
     token_offsets = np.ascontiguousarray(token_offsets, dtype=np.int32)
+    if token_offsets.ndim != 1 or expert_ids.ndim != 1 or token_offsets.shape[0] != expert_ids.shape[0] + 1:
+        raise ValueError("token_offsets must have one entry more than expert_ids")
     n_rows = int(token_offsets[-1])
-    in_dim = x.shape[1]
-    if out is None:
-        out = torch.empty((n_rows, out_dim), dtype=torch.float32, device=x.device)
-    xr = ctypes.c_void_p(0) if x_rows is None else _dev(x_rows, "x_rows", _I32)
+    x_n, in_dim = _dims(x, "x")
+    out = _empty((max(n_rows, 0), out_dim), torch.float32, x) if out is None else out
+    if x_rows is None and x_n < n_rows:
+        raise ValueError(f"x has {x_n} rows; without x_rows it needs token_offsets[-1] = {n_rows}")
+    xr = None if x_rows is None else (x_rows, "x_rows", _I32, (n_rows,))
+    py, pw, ps, pb, px, pr = _ptrs(
+        (out, "y", _F32, (n_rows, out_dim)),
+        *_mat(w_bank, s_bank, b_bank, int(n_experts) * int(out_dim), in_dim, "w_bank", "s_bank", "b_bank"),
+        (x, "x", _F16, None), xr)
     _check("q4a_gemv_experts", _lib.q4a_gemv_experts(
-        _dev(out, "y", _F32), _dev(w_bank, "w_bank", _U8), _dev(s_bank, "s_bank", _BF16),
-        _dev(b_bank, "b_bank", _BF16), _dev(x, "x", _F16), xr,
-        ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
-        int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim), int(in_dim),
-        _stream(stream)))
-    return out
-
-
-def gemv_rmsnorm_grouped(w, s, b, x_raw, norm_w, norm_groups: int, eps: float = 1e-6, shift: float = 0.0,
-                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """gemv_rmsnorm with norm_groups equal segments per row, each normalised on its own."""
-    nb, in_dim = x_raw.shape
-    out_dim = w.shape[0]
-    if out is None:
-        out = torch.empty((nb, out_dim), dtype=torch.float32, device=x_raw.device)
-    _check("q4a_gemv_rmsnorm_grouped", _lib.q4a_gemv_rmsnorm_grouped(
-        _dev(out, "y", _F32), _dev(w, "w", _U8), _dev(s, "s", _BF16), _dev(b, "b", _BF16),
-        _dev(x_raw, "x_raw", _F32), _dev(norm_w, "norm_w", _BF16), float(eps), float(shift),
-        int(norm_groups), nb, out_dim, in_dim, _stream(stream)))
+        py, pw, ps, pb, px, pr, ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
+        int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim), int(in_dim), _stream(stream)))
     return out
 
 
 def silu_mul_xsum(gate_up: torch.Tensor, h: torch.Tensor | None = None,
                   hsum: torch.Tensor | None = None, stream=None, want_hsum: bool = True):
-    rows, two_inter = gate_up.shape
+    rows, two_inter = _dims(gate_up, "gate_up")
     inter = two_inter // 2
-    if h is None:
-        h = torch.empty((rows, inter), dtype=torch.float16, device=gate_up.device)
+    h = _empty((rows, inter), torch.float16, gate_up) if h is None else h
     if hsum is None and want_hsum:
-        hsum = torch.empty((rows, inter // 64), dtype=torch.float32, device=gate_up.device)
-    hp = ctypes.c_void_p(0) if hsum is None else _dev(hsum, "hsum", _F32)
-    _check("q4a_silu_mul_xsum", _lib.q4a_silu_mul_xsum(
-        _dev(h, "h", _F16), hp, _dev(gate_up, "gate_up", _F32), rows, inter, _stream(stream)))
+        hsum = _empty((rows, inter // 64), torch.float32, gate_up)
+    ph, phs, pg = _ptrs((h, "h", _F16, (rows, inter)),
+                        None if hsum is None else (hsum, "hsum", _F32, (rows, inter // 64)),
+                        (gate_up, "gate_up", _F32, None))
+    _check("q4a_silu_mul_xsum", _lib.q4a_silu_mul_xsum(ph, phs, pg, rows, inter, _stream(stream)))
     return h, hsum
 
 
@@ -307,17 +392,16 @@ def moe_combine(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, y_shared: 
     """out[t] = sum_k w[t][k] * y[slot[t][k]] (+ sigmoid(gate . x[t]) * y_shared[t]).
     y fp32 [n_slots][hidden]; slot int32 [n_tok][k]; w fp32 [n_tok][k]; y_shared fp32
     [n_tok][hidden] or None; gate bf16 [hidden]; x fp32 [n_tok][hidden]."""
-    n_slots, hidden = y.shape
-    n_tok, top_k = slot.shape
-    if out is None:
-        out = torch.empty((n_tok, hidden), dtype=torch.float32, device=y.device)
-    null = ctypes.c_void_p(0)
-    _check("q4a_moe_combine", _lib.q4a_moe_combine(
-        _dev(out, "out", _F32), _dev(y, "y", _F32), _dev(slot, "slot", _I32), _dev(w, "w", _F32),
-        int(n_tok), int(top_k), int(n_slots), int(hidden),
-        null if y_shared is None else _dev(y_shared, "y_shared", _F32),
-        null if y_shared is None else _dev(gate, "gate", _BF16),
-        null if y_shared is None else _dev(x, "x", _F32), _stream(stream)))
+    n_slots, hidden = _dims(y, "y")
+    n_tok, top_k = _dims(slot, "slot")
+    out = _empty((n_tok, hidden), torch.float32, y) if out is None else out
+    shared = y_shared is not None
+    po, py, ps, pw, pys, pg, px = _ptrs(
+        (out, "out", _F32, (n_tok, hidden)), (y, "y", _F32, None), (slot, "slot", _I32, None),
+        (w, "w", _F32, (n_tok, top_k)), (y_shared, "y_shared", _F32, (n_tok, hidden)) if shared else None,
+        (gate, "gate", _BF16, (hidden,)) if shared else None, (x, "x", _F32, (n_tok, hidden)) if shared else None)
+    _check("q4a_moe_combine", _lib.q4a_moe_combine(po, py, ps, pw, int(n_tok), int(top_k), int(n_slots), int(hidden),
+                                                   pys, pg, px, _stream(stream)))
     return out
 
 

@@ -227,6 +227,52 @@ q4a_status q4a_gemv_rmsnorm_grouped(float* y, const uint8_t* w, const uint16_t* 
     return launch_gemv(L, (cudaStream_t)stream);
 }
 
+q4a_status q4a_gemv_inject_rmsnorm_grouped(float* y, float* x_new, const uint8_t* w, const uint16_t* s,
+                                           const uint16_t* b, const float* x_raw, const float* out,
+                                           const float* logit, const uint16_t* norm_w, float eps, float shift,
+                                           int norm_groups, int nb, int64_t out_dim, int64_t in_dim,
+                                           q4a_stream_t stream) {
+    if (!y || !w || !s || !b || !x_raw || !out || !logit || !norm_w) return Q4A_ERR_NULL;
+    if (nb < 1 || !(eps >= 0.0f) || norm_groups < 1) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (st != Q4A_OK) return st;
+    if (in_dim % ((int64_t)kGroup * norm_groups) != 0) return Q4A_ERR_SHAPE;
+    if (x_new) {
+        // every cluster of the GEMV re-reads x_raw and out: the updated stream may not overlap them
+        const uintptr_t xb = reinterpret_cast<uintptr_t>(x_new), xe = xb + (uintptr_t)(nb * in_dim * 4);
+        const uintptr_t rb = reinterpret_cast<uintptr_t>(x_raw), re = rb + (uintptr_t)(nb * in_dim * 4);
+        const uintptr_t ob = reinterpret_cast<uintptr_t>(out), oe = ob + (uintptr_t)(nb * (in_dim / norm_groups) * 4);
+        if ((xb < re && rb < xe) || (xb < oe && ob < xe)) return Q4A_ERR_SHAPE;
+    }
+    if (nb > 32 || norm_groups > kMaxNormGroups) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(out, 16) || !aligned(logit, 4) ||
+        (x_new && !aligned(x_new, 16)) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    GemvLaunch L = {};
+    L.w = w;
+    L.tensor_rows = out_dim;
+    L.s = s;
+    L.b = b;
+    L.x = x_raw;
+    L.norm_w = norm_w;
+    L.eps = eps;
+    L.shift = shift;
+    L.y = y;
+    L.out_dim = out_dim;
+    L.in_dim = in_dim;
+    L.rmsnorm = true;
+    L.norm_groups = norm_groups;
+    L.inj_out = out;
+    L.inj_logit = logit;
+    L.x_new = x_new;
+    L.nseg = (int)segs.size();
+    L.seg = segs.data();
+    L.max_ntok = nb;
+    return launch_gemv(L, (cudaStream_t)stream);
+}
+
 q4a_status q4a_gemv_gate_up_silu(uint16_t* h, const uint8_t* w, const uint16_t* s, const uint16_t* b,
                                  const uint16_t* x, int nb, int64_t inter, int64_t in_dim, q4a_stream_t stream) {
     if (!h || !w || !s || !b || !x) return Q4A_ERR_NULL;
@@ -289,6 +335,68 @@ q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, const ui
     L.seg = segs.data();
     L.max_ntok = nb;
     return launch_gemv(L, (cudaStream_t)stream);
+}
+
+q4a_status q4a_decode_mlp(float* y, uint16_t* h, const uint8_t* w_gu, const uint16_t* s_gu, const uint16_t* b_gu,
+                          const float* x_raw, const uint16_t* norm_w, float eps, float shift, const uint8_t* w_dn,
+                          const uint16_t* s_dn, const uint16_t* b_dn, int nb, int64_t hidden, int64_t inter,
+                          q4a_stream_t stream) {
+    if (!y || !h || !w_gu || !s_gu || !b_gu || !x_raw || !norm_w || !w_dn || !s_dn || !b_dn) return Q4A_ERR_NULL;
+    if (nb < 1 || !(eps >= 0.0f) || inter < kGroup || inter % kGroup != 0) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(2 * inter, hidden);
+    if (st != Q4A_OK) return st;
+    st = check_matrix_shape(hidden, inter);
+    if (st != Q4A_OK) return st;
+    if (nb > 32) return Q4A_ERR_UNSUPPORTED;
+    if (!aligned(w_gu, 16) || !aligned(x_raw, 16) || !aligned(norm_w, 16) || !aligned(s_gu, 2) ||
+        !aligned(b_gu, 2) || !aligned(h, 16) || !aligned(w_dn, 16) || !aligned(s_dn, 2) || !aligned(b_dn, 2) ||
+        !aligned(y, 4))
+        return Q4A_ERR_ALIGN;
+    if (hidden % 512 != 0 || !aligned(s_gu, 16) || !aligned(b_gu, 16)) return Q4A_ERR_UNSUPPORTED;
+
+    std::vector<Segment> segs;
+    push_segments(segs, 0, 0, nb);
+    GemvLaunch gu = {};
+    gu.w = w_gu;
+    gu.tensor_rows = 2 * inter;
+    gu.s = s_gu;
+    gu.b = b_gu;
+    gu.x = x_raw;
+    gu.norm_w = norm_w;
+    gu.eps = eps;
+    gu.shift = shift;
+    gu.h = h;
+    gu.fused_gate_up = true;
+    gu.out_dim = inter;
+    gu.in_dim = hidden;
+    gu.rmsnorm = true;
+    gu.norm_groups = 1;
+    gu.nseg = (int)segs.size();
+    gu.seg = segs.data();
+    gu.max_ntok = nb;
+
+    GemvLaunch dn = {};
+    dn.w = w_dn;
+    dn.tensor_rows = hidden;
+    dn.s = s_dn;
+    dn.b = b_dn;
+    dn.x = h;
+    dn.y = y;
+    dn.out_dim = hidden;
+    dn.in_dim = inter;
+    dn.nseg = gu.nseg;
+    dn.seg = segs.data();
+    dn.max_ntok = nb;
+    // plan both launches before either is made: a rejected call launches nothing
+    gu.plan_only = dn.plan_only = true;
+    st = launch_gemv(gu, (cudaStream_t)stream);
+    if (st != Q4A_OK) return st;
+    st = launch_gemv(dn, (cudaStream_t)stream);
+    if (st != Q4A_OK) return st;
+    gu.plan_only = dn.plan_only = false;
+    st = launch_gemv(gu, (cudaStream_t)stream);
+    if (st != Q4A_OK) return st;
+    return launch_gemv(dn, (cudaStream_t)stream);
 }
 
 q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,

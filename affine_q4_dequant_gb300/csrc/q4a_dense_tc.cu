@@ -316,6 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     if (warp == kTcWarpProducer) {
         // ======================= TMA producer: codes =======================
         if (lane == 0) {
+            grid_dep_wait();   // the codes may be written by the previous kernel of the stream
             int ci = 0;
             for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
                 const int64_t row0 = (int64_t)unit * kTcUnitRows;
@@ -406,8 +407,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(exp_full + slot));
         };
+        grid_dep_wait();   // scales, biases and y may belong to the previous kernel of the stream
         if ((int)blockIdx.x < p.n_units) exponents(blockIdx.x, 0);
-        grid_dep_wait();                              // y may belong to the previous kernel
         int li = 0;
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             float esc[kTcUm];
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
         const uint32_t rsw = (uint32_t)rl & 7u;
         const uint32_t code_base = smem_addr(smem + L.code) + (uint32_t)(u * kTcTileBytes) + (uint32_t)rl * 128u;
         const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 + (uint32_t)(u * kTcSG * kTcACols);
+        grid_dep_wait();   // scales and biases may be written by the previous kernel of the stream
         int ci = 0, gi = 0, li = 0;
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             const int slot = li & 1;

@@ -32,8 +32,9 @@ __device__ __forceinline__ uint4 ld_nc_16(const void* p) {
 
 // Byte k of the output = code[2k] | code[2k+1] << 4: every output 16-byte vector
 // packs 32 consecutive codes (two input vectors). Codes are masked to 4 bits.
-// It lets dependent kernels launch only after its last store, behind a device-scope
-// fence: a GEMV launched right after it streams the packed weights without waiting.
+// It lets dependent kernels launch only after its last store, behind a device-scope fence;
+// the GEMV kernels still read weights only after griddepcontrol.wait (the previous kernel
+// complete and its memory visible).
 __global__ void pack_kernel(uint4* __restrict__ out, const uint4* __restrict__ in, int64_t n_out_vec) {
     grid_dep_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_out_vec;

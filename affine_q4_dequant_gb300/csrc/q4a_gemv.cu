@@ -140,6 +140,13 @@ __device__ __forceinline__ bool next_job(const P& p, int& t, int t_end, Job& j) 
     return true;
 }
 
+// The injection weight of stream g of activation row slot: 2 sigmoid(logit / streams)
+// ("BATCH_MSL" hyperconnection.metal fn_inject_b, fn_norm_prep_b with inject = 1).
+template <class P>
+__device__ __forceinline__ float inject_weight(const P& p, int64_t slot, int g) {
+    return 2.0f / (1.0f + expf(-p.inj_logit[slot * p.norm_groups + g] / (float)p.norm_groups));
+}
+
 // ---- activation staging -----------------------------------------------------------------
 
 // Writes the CTA's K-slice of the activation rows of one segment as mma B fragments
@@ -155,17 +162,19 @@ __device__ __forceinline__ bool next_job(const P& p, int& t, int t_end, Job& j) 
 // field j is read in place (value 4^j * code), so step j's activations are scaled by 4^-j.
 template <int NT, bool RMS, int CB, class P>
 __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
-                        float* xsum_s, const float* inv_s, int ctid) {
+                        float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     static_assert(CB == 4 || !RMS, "the RMSNorm prologue is built for 4-bit codes only");
     constexpr int NTOK = NT * 8;
     constexpr int BATCH = RMS ? 2 : 4;
+    constexpr int NLD = RMS ? 10 : 2;   // RMSNorm: x (4), norm weight (2), injected output (4)
     constexpr int NTH = kConsumerWarps * 32;
     const int items = sg.ntok * gsz * 4;
     const int ntm = p.ntok_max;
     const uint32_t scale_odd = 0x2C002C00u;   // half2(1/16, 1/16)
+    const bool inj = RMS && p.inj_out != nullptr;
     for (int base = 0; base < items; base += BATCH * NTH) {
         // phase 1: loads
-        uint4 ld[BATCH][RMS ? 6 : 2];
+        uint4 ld[BATCH][NLD];
 #pragma unroll
         for (int k = 0; k < BATCH; ++k) {
             const int i = base + k * NTH + ctid;
@@ -174,7 +183,7 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
             const int tok = rest / gsz;
             const bool on = i < items;
 #pragma unroll
-            for (int q = 0; q < (RMS ? 6 : 2); ++q) ld[k][q] = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < NLD; ++q) ld[k][q] = make_uint4(0, 0, 0, 0);
             if (on) {
                 const int slot = sg.tok0 + tok;
                 const int64_t src = p.x_rows ? (int64_t)p.x_rows[slot] : (int64_t)slot;
@@ -191,6 +200,15 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
                     ld[k][3] = ld_nc_16(xr + 36);
                     ld[k][4] = ld_nc_16(p.norm_w + col);
                     ld[k][5] = ld_nc_16(p.norm_w + col + 32);
+                    if (inj) {
+                        // the item's 16 inputs lie in one 64-group, hence in one stream
+                        const int64_t seg = col / p.norm_width;
+                        const float* orow = p.inj_out + src * p.norm_width + (col - seg * p.norm_width);
+                        ld[k][6] = ld_nc_16(orow);
+                        ld[k][7] = ld_nc_16(orow + 4);
+                        ld[k][8] = ld_nc_16(orow + 32);
+                        ld[k][9] = ld_nc_16(orow + 36);
+                    }
                 }
             }
         }
@@ -211,18 +229,33 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
                 // the item's 16 inputs lie in one 64-group, hence in one normalisation segment
                 const int seg = (int)(((int64_t)(kg0 + gl) * kGroup) / p.norm_width);
                 const float inv = live ? inv_s[tok * p.norm_groups + seg] : 0.f;
+                const int64_t slot = sg.tok0 + tok;
+                const float wgt = inj && live ? inject_weight(p, slot, seg) : 0.f;
+                float* xn_row = write_xnew && live ? p.x_new + slot * p.in_dim + (int64_t)(kg0 + gl) * kGroup + 8 * t
+                                                   : nullptr;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint4 f0 = ld[k][2 * half], f1 = ld[k][2 * half + 1], wv = ld[k][4 + half];
-                    const uint32_t xs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                    const uint4 o0 = ld[k][6 + 2 * half], o1 = ld[k][7 + 2 * half];
+                    float xs[8] = {__uint_as_float(f0.x), __uint_as_float(f0.y), __uint_as_float(f0.z),
+                                   __uint_as_float(f0.w), __uint_as_float(f1.x), __uint_as_float(f1.y),
+                                   __uint_as_float(f1.z), __uint_as_float(f1.w)};
+                    if (inj) {
+                        const uint32_t os[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) xs[e] = fmaf(__uint_as_float(os[e]), wgt, xs[e]);
+                        if (xn_row) {
+                            *reinterpret_cast<float4*>(xn_row + 32 * half) = make_float4(xs[0], xs[1], xs[2], xs[3]);
+                            *reinterpret_cast<float4*>(xn_row + 32 * half + 4) = make_float4(xs[4], xs[5], xs[6], xs[7]);
+                        }
+                    }
                     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
                     uint32_t* dst = half ? u : v;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float w0 = bf16_to_f32(ww[q] & 0xFFFFu) + p.shift;
                         const float w1 = bf16_to_f32(ww[q] >> 16) + p.shift;
-                        __half2 h = __floats2half2_rn(__uint_as_float(xs[2 * q]) * inv * w0,
-                                                      __uint_as_float(xs[2 * q + 1]) * inv * w1);
+                        __half2 h = __floats2half2_rn(xs[2 * q] * inv * w0, xs[2 * q + 1] * inv * w1);
                         dst[q] = *reinterpret_cast<uint32_t*>(&h);
                     }
                 }
@@ -327,6 +360,7 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
     constexpr int NTOK = NT * 8;
     constexpr int U = 16;
     const int G = p.norm_groups;
+    const bool inj = p.inj_out != nullptr;
     const int64_t k_lo = (int64_t)kg0 * kGroup, k_hi = k_lo + (int64_t)gsz * kGroup;
     for (int tok = warp; tok < NTOK; tok += kConsumerWarps) {
         for (int seg = 0; seg < G; ++seg) {
@@ -334,8 +368,14 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
             const int64_t s_hi = llmin(k_hi, (int64_t)(seg + 1) * p.norm_width);
             float acc = 0.f;
             if (tok < sg.ntok && s_lo < s_hi) {
+                const int64_t slot = sg.tok0 + tok;
                 const float4* xr = reinterpret_cast<const float4*>(
-                    static_cast<const float*>(p.x) + (int64_t)(sg.tok0 + tok) * p.in_dim + s_lo);
+                    static_cast<const float*>(p.x) + slot * p.in_dim + s_lo);
+                // injection: the stream's inputs plus out[slot][i] * weight, i = column - seg * width
+                const float4* orow = inj ? reinterpret_cast<const float4*>(p.inj_out + slot * p.norm_width +
+                                                                            (s_lo - (int64_t)seg * p.norm_width))
+                                         : nullptr;
+                const float wgt = inj ? inject_weight(p, slot, seg) : 0.f;
                 const int chunks = (int)((s_hi - s_lo) / 4);   // float4 chunks of this segment's part
                 for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
                     float4 f[U];
@@ -343,6 +383,17 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
                     for (int u = 0; u < U; ++u) {
                         const int c = c0 + u * 32 + lane;
                         f[u] = c < chunks ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    if (inj) {
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            const float4 o = c < chunks ? __ldg(orow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            f[u].x = fmaf(o.x, wgt, f[u].x);
+                            f[u].y = fmaf(o.y, wgt, f[u].y);
+                            f[u].z = fmaf(o.z, wgt, f[u].z);
+                            f[u].w = fmaf(o.w, wgt, f[u].w);
+                        }
                     }
 #pragma unroll
                     for (int u = 0; u < U; ++u)
@@ -434,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ======================= producer warp =======================
-        // The producer reads only the weights (codes, scales, biases), which are inputs of
-        // the whole call, so it never waits for the previous kernel of the stream: under
-        // programmatic dependent launch its streaming overlaps that kernel's tail.
+        // Under programmatic dependent launch this CTA may start while the previous kernel of
+        // the stream still runs, and that kernel may have written the weights (a pack or a
+        // quantiser, or any kernel of the caller's): the weight loads wait for it to complete.
+        grid_dep_wait();
         const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
         const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
         const int64_t srow_bytes = (int64_t)p.groups * 2;
@@ -653,7 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = p.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS, CB>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid);
+                stage_x<NT, RMS, CB>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
+                                     RMS && cid == 0 && p.x_new != nullptr);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
                 consumer_sync();
@@ -1198,6 +1251,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     while (stages > 2 && !fits(C, stages)) --stages;
     if (!fits(C, stages)) return Q4A_ERR_UNSUPPORTED;
     const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C), cb);
+    if (L.plan_only) return Q4A_OK;
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
     memset(&prm, 0, sizeof(prm));
@@ -1229,6 +1283,9 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     prm.x = L.x;
     prm.x_rows = L.x_rows;
     prm.norm_w = L.norm_w;
+    prm.inj_out = L.inj_out;
+    prm.inj_logit = L.inj_logit;
+    prm.x_new = L.inj_out ? L.x_new : nullptr;
     prm.y = L.y;
     prm.h = L.h;
     prm.eps = L.eps;

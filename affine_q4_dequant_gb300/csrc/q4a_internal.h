@@ -119,6 +119,9 @@ struct GemvParams {
     const void* x;            // fp16 [*][in_dim] (or fp32 x_raw for the RMSNorm variant)
     const int32_t* x_rows;    // may be null
     const uint16_t* norm_w;   // bf16 [in_dim] (RMSNorm variant)
+    const float* inj_out;     // RMSNorm variant, injection: fp32 [slots][norm_width] added to every
+    const float* inj_logit;   // stream g of a row with weight 2 sigmoid(logit[slot][g] / norm_groups)
+    float* x_new;             // fp32 [slots][in_dim]: the injected stream (written by cluster 0), or null
     float* y;                 // fp32 [slots][out_dim]
     uint16_t* h;              // fused gate|up: fp16 silu(gate) * up [slots][out_dim]
     float eps, shift;
@@ -159,6 +162,9 @@ struct GemvLaunch {
     bool silu;                // output epilogue y -> silu(y / silu_div)
     float silu_div;
     int norm_groups;          // RMSNorm variant: normalisation segments per row (>= 1)
+    const float* inj_out = nullptr;   // RMSNorm variant: hyper-connection injection (see GemvParams)
+    const float* inj_logit = nullptr;
+    float* x_new = nullptr;
     bool fused_gate_up = false;   // w holds gate rows [0, out_dim) then up rows [out_dim, 2 out_dim);
     uint16_t* h = nullptr;        // the output is h = fp16(silu(gate) * up) [slots][out_dim]
     int code_bits = 4;        // 4 (w: packed nibbles), 2 or 3 (w: 2-bit codes [rows][in/4],
@@ -167,6 +173,7 @@ struct GemvLaunch {
     int nseg;
     const Segment* seg;
     int max_ntok;
+    bool plan_only = false;               // validate and plan, launch nothing
 };
 
 q4a_status launch_gemv(const GemvLaunch& L, cudaStream_t stream);

@@ -237,6 +237,10 @@ def run_ours(args, rank, world, local_rank):
             for key, qm in (("gu", gu), ("dn", dn)):
                 layer[key] = (q4a.pack(to_dev(qm.codes)), to_dev(qm.scale), to_dev(qm.bias))
             layer["norm_w"] = to_dev(wl.norm_weight(wl.DENSE_GATE_UP, wl.T_NORM_W, HIDDEN, seed=l))
+            if args.layer_mode == "decode_mlp":
+                # the down projection that matches the fused gate|up: 6144 -> 4096
+                dm = wl.quant_matrix(wl.DENSE_DOWN, DOWN_OUT, INTER, seed=l)
+                layer["dn_mlp"] = (q4a.pack(to_dev(dm.codes)), to_dev(dm.scale), to_dev(dm.bias))
             layers.append(layer)
         # activations per NB
         acts = {}
@@ -264,8 +268,13 @@ def run_ours(args, rank, world, local_rank):
         q4a.gemv(w, s_, b_, ac["x_dn"], out=ac["y_dn"], stream=stream)
 
     def layer_call(nb, l):
-        gate_up_call(nb, l)
-        down_call(nb, l)
+        if args.layer_mode == "separate":
+            gate_up_call(nb, l)
+            down_call(nb, l)
+            return
+        ly, ac = layers[l], acts[nb]
+        q4a.decode_mlp(*ly["gu"], ac["a"], ly["norm_w"], *ly["dn_mlp"], eps=1e-6, out=ac["y_dn"], h=ac["h"],
+                       stream=stream)
 
     # eager warm-up: first calls fill the library's per-device caches before capture
     with torch.cuda.stream(stream):
@@ -337,8 +346,9 @@ def run_ours(args, rank, world, local_rank):
     for nb in nbs:
         gu_b, dn_b = layer_bytes(nb)
         gu_ms, dn_ms, lay_ms = (kind_ms(k, nb) for k in ("gate_up", "down", "layer"))
+        lay_b = gu_b + (gemv_bytes(DOWN_OUT, INTER, nb, 2) if args.layer_mode == "decode_mlp" else dn_b)
         per_nb[str(nb)] = {
-            "layer_us": lay_ms / n * 1e3,
+            "layer_us": lay_ms / n * 1e3, "layer_gbs": lay_b / (lay_ms / n * 1e-3) / 1e9,
             "gate_up_us": gu_ms / n * 1e3, "gate_up_gbs": gu_b / (gu_ms / n * 1e-3) / 1e9,
             "down_us": dn_ms / n * 1e3, "down_gbs": dn_b / (dn_ms / n * 1e-3) / 1e9,
         }
@@ -702,6 +712,8 @@ def main():
     ap.add_argument("--reps", type=int, default=60)
     ap.add_argument("--bits", type=int, choices=[4, 3, 2], default=4,
                     help="with --kernel: code width (3 and 2: derived low-bit codes, q4a_gemv_lowbit)")
+    ap.add_argument("--layer-mode", choices=["decode_mlp", "separate"], default="decode_mlp",
+                    help="the decode layer as one q4a_decode_mlp call, or as the two GEMV calls")
     ap.add_argument("--profile", action="store_true",
                     help="with --kernel: eager launches only (a target for ncu), no timing")
     args = ap.parse_args()

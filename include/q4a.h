@@ -142,6 +142,28 @@ Q4A_API q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, 
                                                  q4a_stream_t stream);
 
 /*
+ * q4a_decode_mlp -- one decode layer's gated MLP in one call: RMSNorm, the gate and up
+ * projections with the silu(gate)*up epilogue, then the down projection of h; the same result
+ * as q4a_gemv_rmsnorm_gate_up_silu followed by q4a_gemv on h ("BATCH_MSL",
+ * hyperconnection.metal fn_norm_prep_b / fn_group_norm_b, then experts.metal fn_moe_gate_up_b,
+ * fn_moe_act_b and fn_moe_down_b: the dense form of the same chain).
+ *   y         out  fp32 [nb][hidden]
+ *   h         out  fp16 [nb][inter], h = fp16(silu(W_gate.xn) * (W_up.xn)), the down
+ *                  projection's input
+ *   w_gu, s_gu, b_gu   in  [2*inter][hidden/2] codes, [2*inter][hidden/64] bf16: gate rows,
+ *                  then up rows (as q4a_gemv_gate_up_silu)
+ *   x_raw, norm_w, eps, shift   in  as q4a_gemv_rmsnorm (one normalisation group)
+ *   w_dn, s_dn, b_dn   in  [hidden][inter/2] codes, [hidden][inter/64] bf16
+ *   Requires 1 <= nb <= 32, hidden % 512 == 0, inter % 64 == 0; w_gu, w_dn, x_raw, norm_w and
+ *   h 16-byte aligned; s_gu, b_gu 16-byte aligned; s_dn, b_dn 2-byte aligned. Everything is
+ *   planned before anything is launched, so a rejected call launches nothing.
+ */
+Q4A_API q4a_status q4a_decode_mlp(float* y, uint16_t* h, const uint8_t* w_gu, const uint16_t* s_gu,
+                                  const uint16_t* b_gu, const float* x_raw, const uint16_t* norm_w, float eps,
+                                  float shift, const uint8_t* w_dn, const uint16_t* s_dn, const uint16_t* b_dn,
+                                  int nb, int64_t hidden, int64_t inter, q4a_stream_t stream);
+
+/*
  * q4a_quantize -- a 4-bit affine quantiser for float weights (a prefill helper; the pages define
  * none). Per 64-input group, every step in binary32:
  *     b = bf16(min w),  s = bf16((max w - b) / 15) if max w > b else 0,
@@ -264,6 +286,28 @@ Q4A_API q4a_status q4a_gemv_rmsnorm_grouped(float* y, const uint8_t* w, const ui
                                     const uint16_t* b, const float* x_raw, const uint16_t* norm_w,
                                     float eps, float shift, int norm_groups, int nb, int64_t out_dim,
                                     int64_t in_dim, q4a_stream_t stream);
+
+/*
+ * q4a_gemv_inject_rmsnorm_grouped -- q4a_gemv_rmsnorm_grouped whose prologue first injects a
+ * layer output into every hyper-connection stream of the row ("BATCH_MSL",
+ * hyperconnection.metal fn_inject_b, and fn_norm_prep_b with inject = 1): with
+ * n = in_dim / norm_groups, stream g of row r is
+ *     x'[r][g*n + i] = x_raw[r][g*n + i] + out[r][i] * 2 / (1 + e^(-logit[r][g] / norm_groups))
+ * (fp32, one fused multiply-add), then xn = the grouped RMSNorm of x' and y = W.xn.
+ *   y        out  fp32 [nb][out_dim]
+ *   x_new    out  fp32 [nb][in_dim]: x', or NULL. It may not overlap x_raw or out (every CTA
+ *                 cluster of the GEMV re-reads them; Q4A_ERR_SHAPE otherwise).
+ *   x_raw    in   fp32 [nb][in_dim], the hyper-connection streams of each row
+ *   out      in   fp32 [nb][n], the layer output injected into every stream
+ *   logit    in   fp32 [nb][norm_groups], the per-stream mixing logits
+ *   Requires out and x_new 16-byte aligned, logit 4-byte aligned; everything else as
+ *   q4a_gemv_rmsnorm_grouped.
+ */
+Q4A_API q4a_status q4a_gemv_inject_rmsnorm_grouped(float* y, float* x_new, const uint8_t* w, const uint16_t* s,
+                                                   const uint16_t* b, const float* x_raw, const float* out,
+                                                   const float* logit, const uint16_t* norm_w, float eps,
+                                                   float shift, int norm_groups, int nb, int64_t out_dim,
+                                                   int64_t in_dim, q4a_stream_t stream);
 
 /*
  * q4a_silu_mul_xsum -- A7: the step between the two routed-expert GEMVs.

@@ -43,6 +43,8 @@ def lib():
     lib.q4a_quantize.argtypes = [P, P, P, P, I64, I64, P]
     lib.q4a_gemv_f32x.argtypes = [P, P, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_rmsnorm_gate_up_silu.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
+    lib.q4a_decode_mlp.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]
+    lib.q4a_gemv_inject_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     return lib
 
 
@@ -234,3 +236,135 @@ def test_gemv_batch_limits(lib):
     assert lib.q4a_gemv(A, A, A, A, A, 257, 64, 576, None) == UNSUP
     assert lib.q4a_gemv(A, A, A, A, A, 0, 64, 576, None) == SHAPE
 
+
+
+def test_decode_mlp_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_decode_mlp
+
+    def call(y=A, h=A, wg=A, sg=A, bg=A, x=A, nw=A, eps=1e-6, wd=A, sd=A, bd=A, nb=1, hidden=512, inter=128):
+        return f(y, h, wg, sg, bg, x, nw, eps, 0.0, wd, sd, bd, nb, hidden, inter, None)
+
+    assert call(y=None) == NULL
+    assert call(wd=None) == NULL
+    assert call(nb=0) == SHAPE
+    assert call(eps=-1.0) == SHAPE
+    assert call(inter=96) == SHAPE                      # the down projection's in_dim % 64
+    assert call(hidden=500) == SHAPE
+    assert call(nb=33) == UNSUP
+    assert call(h=A + 8) == ALIGN                       # h is the down projection's x: 16 bytes
+    assert call(wd=A + 4) == ALIGN
+    assert call(hidden=576) == UNSUP                    # 9 groups: no 2D scale boxes
+    assert call(sg=A + 2) == UNSUP
+
+
+def test_inject_rejections(lib):
+    A = 0x100000
+    f = lib.q4a_gemv_inject_rmsnorm_grouped
+
+    def call(y=A, xn=0x200000, x=A, o=0x300000, lg=0x400000, nw=A, eps=1e-6, groups=2, nb=2, out_dim=64,
+             in_dim=512):
+        return f(y, xn, A, A, A, x, o, lg, nw, eps, 0.0, groups, nb, out_dim, in_dim, None)
+
+    assert call(o=None) == NULL
+    assert call(lg=None) == NULL
+    assert call(groups=3) == SHAPE                 # 512 % (64 * 3)
+    assert call(eps=-1.0) == SHAPE
+    assert call(xn=A) == SHAPE                     # x_new overlaps x_raw
+    assert call(xn=A + 2048) == SHAPE              # partial overlap (x_raw is 2 x 512 fp32)
+    assert call(xn=0x300000 + 256) == SHAPE        # overlaps out (2 x 256 fp32)
+    assert call(nb=33) == UNSUP
+    assert call(groups=16, in_dim=1024) == UNSUP
+    assert call(o=0x300000 + 4) == ALIGN
+    assert call(xn=0x200000 + 8) == ALIGN
+    assert call(lg=0x400000 + 2) == ALIGN
+
+
+# ---- the Python binding refuses mis-shaped buffers before anything launches -------------
+
+@pytest.fixture(scope="module")
+def q4a():
+    torch = pytest.importorskip("torch")
+    _builder().build()
+    import affine_q4_dequant_gb300 as mod
+
+    return mod, torch
+
+
+def _bad(fn, what):
+    with pytest.raises(ValueError, match=what):
+        fn()
+
+
+def test_binding_checks_matrix_shapes(q4a):
+    mod, torch = q4a
+    u8, bf, f16, f32 = torch.uint8, torch.bfloat16, torch.float16, torch.float32
+    w = torch.zeros(16, 256, dtype=u8)
+    s = torch.zeros(16, 8, dtype=bf)
+    x = torch.zeros(2, 512, dtype=f16)
+    _bad(lambda: mod.gemv(torch.zeros(16, 255, dtype=u8), s, s, x), "w: shape")
+    _bad(lambda: mod.gemv(w, torch.zeros(8, 8, dtype=bf), s, x), "s: shape")
+    _bad(lambda: mod.gemv(w, s, torch.zeros(16, 4, dtype=bf), x), "b: shape")
+    _bad(lambda: mod.gemv(w, s, s, x, out=torch.zeros(1, 16, dtype=f32)), "y: shape")
+    _bad(lambda: mod.gemv(w, s, s, torch.zeros(2, 500, dtype=f16)), "multiple of 64")
+    _bad(lambda: mod.gemv_silu(w, s, s, x, 2.0, out=torch.zeros(2, 17, dtype=f32)), "y: shape")
+    _bad(lambda: mod.gemv_f32x(w, s, s, torch.zeros(2, 512, dtype=f32), out=torch.zeros(3, 16, dtype=f32)),
+         "y: shape")
+    with pytest.raises(TypeError, match="CUDA"):
+        mod.gemv(w, s, s, x)                            # right shapes, but host memory
+
+
+def test_binding_checks_fused_and_norm_shapes(q4a):
+    mod, torch = q4a
+    u8, bf, f16, f32 = torch.uint8, torch.bfloat16, torch.float16, torch.float32
+    w = torch.zeros(32, 256, dtype=u8)                  # 16 gate rows + 16 up rows
+    s = torch.zeros(32, 8, dtype=bf)
+    x = torch.zeros(2, 512, dtype=f16)
+    a = torch.zeros(2, 512, dtype=f32)
+    nw = torch.zeros(512, dtype=bf)
+    _bad(lambda: mod.gemv_gate_up_silu(w, s, s, x, out=torch.zeros(2, 32, dtype=f16)), "h: shape")
+    _bad(lambda: mod.gemv_rmsnorm_gate_up_silu(w, s, s, a, torch.zeros(256, dtype=bf)), "norm_w: shape")
+    _bad(lambda: mod.gemv_rmsnorm(w, s, s, a, nw, out=torch.zeros(2, 16, dtype=f32)), "y: shape")
+    _bad(lambda: mod.gemv_rmsnorm_grouped(w, torch.zeros(32, 4, dtype=bf), s, a, nw, 2), "s: shape")
+    o = torch.zeros(2, 256, dtype=f32)
+    lg = torch.zeros(2, 2, dtype=f32)
+    _bad(lambda: mod.gemv_inject_rmsnorm_grouped(w, s, s, a, torch.zeros(2, 512, dtype=f32), lg, nw, 2), "out: shape")
+    _bad(lambda: mod.gemv_inject_rmsnorm_grouped(w, s, s, a, o, torch.zeros(2, 3, dtype=f32), nw, 2), "logit: shape")
+    _bad(lambda: mod.gemv_inject_rmsnorm_grouped(w, s, s, a, o, lg, nw, 2, x_new=torch.zeros(2, 256, dtype=f32)),
+         "x_new: shape")
+    _bad(lambda: mod.gemv_inject_rmsnorm_grouped(w, s, s, a, o, lg, nw, 3), "streams")
+    # 16 gate + 16 up rows make inter = 16: the down projection's rows are too short
+    _bad(lambda: mod.decode_mlp(w, s, s, a, nw, torch.zeros(512, 8, dtype=u8), torch.zeros(512, 0, dtype=bf),
+                                torch.zeros(512, 0, dtype=bf)), "multiple of 64")
+    w2 = torch.zeros(128, 256, dtype=u8)                # inter 64: down 64 -> 512
+    s2 = torch.zeros(128, 8, dtype=bf)
+    wd2 = torch.zeros(512, 32, dtype=u8)
+    sd2 = torch.zeros(512, 1, dtype=bf)
+    _bad(lambda: mod.decode_mlp(w2, s2, s2, a, nw, torch.zeros(511, 32, dtype=u8), sd2, sd2), "w_dn: shape")
+    _bad(lambda: mod.decode_mlp(w2, s2, s2, a, nw, wd2, sd2, sd2, h=torch.zeros(2, 32, dtype=f16)), "h: shape")
+    _bad(lambda: mod.decode_mlp(w2, s2, s2, a, nw, wd2, sd2, sd2, out=torch.zeros(2, 64, dtype=f32)), "y: shape")
+
+
+def test_binding_checks_expert_and_helper_shapes(q4a):
+    mod, torch = q4a
+    u8, bf, f16, f32, i32 = torch.uint8, torch.bfloat16, torch.float16, torch.float32, torch.int32
+    # a bank of 2 experts x 16 rows, 512 inputs
+    wb = torch.zeros(32, 256, dtype=u8)
+    sb = torch.zeros(32, 8, dtype=bf)
+    x = torch.zeros(3, 512, dtype=f16)
+    _bad(lambda: mod.gemv_experts(torch.zeros(31, 256, dtype=u8), sb, sb, x, None, [0, 1], [0, 2, 3], 2, 16),
+         "w_bank: shape")
+    _bad(lambda: mod.gemv_experts(wb, sb, sb, x, None, [0, 1], [0, 2, 4], 2, 16), "without x_rows")
+    _bad(lambda: mod.gemv_experts(wb, sb, sb, x, torch.zeros(2, dtype=i32), [0, 1], [0, 2, 3], 2, 16),
+         "x_rows: shape")
+    _bad(lambda: mod.gemv_experts(wb, sb, sb, x, None, [0, 1], [0, 3], 2, 16), "one entry more")
+    _bad(lambda: mod.silu_mul_xsum(torch.zeros(2, 256, dtype=f32), h=torch.zeros(2, 64, dtype=f16)), "h: shape")
+    _bad(lambda: mod.xsum(x, out=torch.zeros(3, 4, dtype=f32)), "out: shape")
+    _bad(lambda: mod.pack(torch.zeros(4, 64, dtype=u8), out=torch.zeros(4, 64, dtype=u8)), "out: shape")
+    y = torch.zeros(6, 8, dtype=f32)
+    _bad(lambda: mod.moe_combine(y, torch.zeros(3, 2, dtype=i32), torch.zeros(3, 1, dtype=f32)), "w: shape")
+    _bad(lambda: mod.moe_combine(y, torch.zeros(3, 2, dtype=i32), torch.zeros(3, 2, dtype=f32),
+                                 y_shared=torch.zeros(3, 8, dtype=f32), gate=torch.zeros(4, dtype=bf),
+                                 x=torch.zeros(3, 8, dtype=f32)), "gate: shape")
+    _bad(lambda: mod.gemv_lowbit(3, torch.zeros(16, 128, dtype=u8), torch.zeros(16, 63, dtype=u8),
+                                 torch.zeros(16, 8, dtype=bf), torch.zeros(16, 8, dtype=bf), x[:2]), "w_lo: shape")
