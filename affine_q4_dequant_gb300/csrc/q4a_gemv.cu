@@ -140,6 +140,23 @@ __device__ __forceinline__ bool next_job(const P& p, int& t, int t_end, Job& j) 
     return true;
 }
 
+// This CTA's share of one op: its K-slice (in groups), the stages per row block and its
+// cluster's range of schedule units.
+struct OpRange {
+    int kg0, kg1, gsz, nks, t_begin, t_end;
+};
+
+__device__ __forceinline__ OpRange op_range(const GemvOp& o, int crank, int cid, int n_clusters) {
+    OpRange r;
+    r.kg0 = crank * o.gs;
+    r.kg1 = min(o.groups, r.kg0 + o.gs);
+    r.gsz = r.kg1 - r.kg0;
+    r.nks = (r.gsz + kStageGroups - 1) / kStageGroups;
+    r.t_begin = (int)(((int64_t)cid * o.n_tiles) / n_clusters);
+    r.t_end = (int)(((int64_t)(cid + 1) * o.n_tiles) / n_clusters);
+    return r;
+}
+
 // The injection weight of stream g of activation row slot: 2 sigmoid(logit / streams)
 // ("BATCH_MSL" hyperconnection.metal fn_inject_b, fn_norm_prep_b with inject = 1).
 template <class P>
@@ -161,8 +178,8 @@ __device__ __forceinline__ float inject_weight(const P& p, int64_t slot, int g) 
 // 16t + {0,2,4,6} (j = 0) and 16t + {8,10,12,14} (j = 1), the odd ones after them (j = 2, 3);
 // field j is read in place (value 4^j * code), so step j's activations are scaled by 4^-j.
 template <int NT, bool RMS, int CB, class P>
-__device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
-                        float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
+__device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
+                          float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     static_assert(CB == 4 || !RMS, "the RMSNorm prologue is built for 4-bit codes only");
     constexpr int NTOK = NT * 8;
     constexpr int BATCH = RMS ? 2 : 4;
@@ -310,6 +327,20 @@ __device__ void stage_x(const P& p, const Segment& sg, int kg0, int gsz, uint8_t
     }
 }
 
+// Staging of one op's activations: the RMSNorm form when the op asks for it (kernels built
+// with RMS), the plain fp16 form otherwise.
+template <int NT, bool RMS, int CB, class P>
+__device__ __forceinline__ void stage_x(const P& p, bool rms, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
+                                        float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
+    if constexpr (RMS) {
+        if (rms) {
+            stage_x_t<NT, true, CB>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, write_xnew);
+            return;
+        }
+    }
+    stage_x_t<NT, false, CB>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, false);
+}
+
 // B fragments of the bias term sum_g b[o][g] * xsum[r][g], an m16n8k16 contraction over
 // groups (bf16 operands): per 16-group block, activation row tok and lane quad t, the
 // pairs of groups (2t, 2t+1) and (2t+8, 2t+9) of xsum (already times 2^-24), split into
@@ -352,58 +383,71 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 
 // Sum of squares of this CTA's K-slice of every activation row (the RMSNorm prologue), per
 // normalisation segment of the row (ssq_s[tok * G + seg]; segments outside the slice get 0).
-// Warp w owns rows w, w+8, ...; each lane issues up to 16 independent 16-byte loads per
-// round before accumulating.
+// Work units are (row, segment, part): with fewer rows than consumer warps every row is split
+// into parts so that all warps load at once (one memory round trip at NB 1); each lane keeps
+// 16 independent 16-byte loads in flight. The parts' sums meet in `red` in a fixed order.
 template <int NT, class P>
-__device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, float* ssq_s, int warp,
-                            int lane) {
+__device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, float* ssq_s, float* red, int warp,
+                            int lane, int ctid) {
     constexpr int NTOK = NT * 8;
     constexpr int U = 16;
     const int G = p.norm_groups;
     const bool inj = p.inj_out != nullptr;
+    const int ntok = sg.ntok;
+    const int parts = ntok >= kConsumerWarps ? 1 : kConsumerWarps / ntok;
+    const int units = ntok * G * parts;
     const int64_t k_lo = (int64_t)kg0 * kGroup, k_hi = k_lo + (int64_t)gsz * kGroup;
-    for (int tok = warp; tok < NTOK; tok += kConsumerWarps) {
-        for (int seg = 0; seg < G; ++seg) {
-            const int64_t s_lo = llmax(k_lo, (int64_t)seg * p.norm_width);
-            const int64_t s_hi = llmin(k_hi, (int64_t)(seg + 1) * p.norm_width);
-            float acc = 0.f;
-            if (tok < sg.ntok && s_lo < s_hi) {
-                const int64_t slot = sg.tok0 + tok;
-                const float4* xr = reinterpret_cast<const float4*>(
-                    static_cast<const float*>(p.x) + slot * p.in_dim + s_lo);
-                // injection: the stream's inputs plus out[slot][i] * weight, i = column - seg * width
-                const float4* orow = inj ? reinterpret_cast<const float4*>(p.inj_out + slot * p.norm_width +
-                                                                            (s_lo - (int64_t)seg * p.norm_width))
-                                         : nullptr;
-                const float wgt = inj ? inject_weight(p, slot, seg) : 0.f;
-                const int chunks = (int)((s_hi - s_lo) / 4);   // float4 chunks of this segment's part
-                for (int c0 = 0; c0 < chunks; c0 += 32 * U) {
-                    float4 f[U];
+    for (int u = warp; u < units; u += kConsumerWarps) {
+        const int part = u % parts;
+        const int seg = (u / parts) % G;
+        const int tok = u / parts / G;
+        const int64_t s_lo = llmax(k_lo, (int64_t)seg * p.norm_width);
+        const int64_t s_hi = llmin(k_hi, (int64_t)(seg + 1) * p.norm_width);
+        float acc = 0.f;
+        if (s_lo < s_hi) {
+            const int64_t slot = sg.tok0 + tok;
+            const float4* xr = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + slot * p.in_dim + s_lo);
+            // injection: the stream's inputs plus out[slot][i] * weight, i = column - seg * width
+            const float4* orow = inj ? reinterpret_cast<const float4*>(p.inj_out + slot * p.norm_width +
+                                                                        (s_lo - (int64_t)seg * p.norm_width))
+                                     : nullptr;
+            const float wgt = inj ? inject_weight(p, slot, seg) : 0.f;
+            const int chunks = (int)((s_hi - s_lo) / 4);   // float4 chunks of this segment's part
+            const int c_lo = (int)((int64_t)chunks * part / parts), c_hi = (int)((int64_t)chunks * (part + 1) / parts);
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
+                float4 f[U];
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int c = c0 + u * 32 + lane;
-                        f[u] = c < chunks ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    if (inj) {
-#pragma unroll
-                        for (int u = 0; u < U; ++u) {
-                            const int c = c0 + u * 32 + lane;
-                            const float4 o = c < chunks ? __ldg(orow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            f[u].x = fmaf(o.x, wgt, f[u].x);
-                            f[u].y = fmaf(o.y, wgt, f[u].y);
-                            f[u].z = fmaf(o.z, wgt, f[u].z);
-                            f[u].w = fmaf(o.w, wgt, f[u].w);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-                        acc += f[u].x * f[u].x + f[u].y * f[u].y + f[u].z * f[u].z + f[u].w * f[u].w;
+                for (int k = 0; k < U; ++k) {
+                    const int c = c0 + k * 32 + lane;
+                    f[k] = c < c_hi ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-            }
+                if (inj) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) ssq_s[tok * G + seg] = acc;
+                    for (int k = 0; k < U; ++k) {
+                        const int c = c0 + k * 32 + lane;
+                        const float4 o = c < c_hi ? __ldg(orow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        f[k].x = fmaf(o.x, wgt, f[k].x);
+                        f[k].y = fmaf(o.y, wgt, f[k].y);
+                        f[k].z = fmaf(o.z, wgt, f[k].z);
+                        f[k].w = fmaf(o.w, wgt, f[k].w);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    acc += f[k].x * f[k].x + f[k].y * f[k].y + f[k].z * f[k].z + f[k].w * f[k].w;
+            }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) red[u] = acc;
+    }
+    consumer_sync();
+    for (int e = ctid; e < NTOK * G; e += kConsumerWarps * 32) {
+        const int tok = e / G;
+        float tot = 0.f;
+        if (tok < ntok)
+            for (int q = 0; q < parts; ++q) tot += red[e * parts + q];
+        ssq_s[e] = tot;
     }
 }
 
@@ -415,16 +459,19 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
 // "tile" of the schedule is a unit of 16 gate rows and the 16 up rows with the same index,
 // kept in shared-memory tiles u and MT/2 + u of the row block, and the epilogue writes
 // h = fp16(silu(gate) * up) instead of y ("BATCH_MSL" experts.metal fn_moe_act_b).
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
+// MTT: tiles per row block (0: the default for NT). Rows that a short row block lacks still
+// cost their mma work (the tile loop is unrolled for a fixed tile count), so launches whose
+// clusters get only a few tiles use a kernel built for that many.
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> p) {
+    gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> pp) {
     constexpr int NTOK = NT * 8;
-    constexpr int MT = tiles_per_block(NT);  // tiles per row block
+    constexpr int MT = MTT ? MTT : tiles_per_block(NT);  // tiles per row block
     constexpr int TPW = MT;                  // tiles per consumer warp: all of the row block
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const SmemLayout& L = p.lay;
+    const SmemLayout& L = pp.lay;
     uint8_t* ring = smem + L.ring;
     uint8_t* xfrag = smem + L.xfrag;
     float* xsum_s = reinterpret_cast<float*>(smem + L.xsum);
@@ -433,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* cpart = reinterpret_cast<float*>(smem + L.cpart);
     float* ssq_s = reinterpret_cast<float*>(smem + L.ssq);   // [NTOK] sum of squares, [NTOK] inv
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-    const int S = p.stages;
+    const int S = pp.stages;
     uint64_t* full_b = bars;              // [S]  TMA bytes of a stage landed
     uint64_t* empty_b = bars + S;         // [S]  every consumer warp is done with a stage
     uint64_t* sbfull_b = bars + 2 * S;    // [2]  a row block's scales/biases landed
@@ -444,23 +491,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int C = p.cluster;
+    const int C = pp.cluster;
     const int crank = C > 1 ? (int)cluster_rank() : 0;
     const int cid = blockIdx.x / C;
-
-    // This CTA's K-slice (in groups) and its stage count per row block.
-    const int kg0 = crank * p.gs;
-    const int kg1 = min(p.groups, kg0 + p.gs);
-    const int gsz = kg1 - kg0;
-    const int nks = (gsz + kStageGroups - 1) / kStageGroups;
-
-    // This cluster's tile range.
-    const int t_begin = (int)(((int64_t)cid * p.n_tiles) / p.n_clusters);
-    const int t_end = (int)(((int64_t)(cid + 1) * p.n_tiles) / p.n_clusters);
 
     grid_dep_launch();
     if (warp == kConsumerWarps && lane < 3 * kNumMaps) {
         // fetch the tensor-map descriptors in parallel before their first use
+        const GemvOp& p = pp.op;
         const CUtensorMap* m = lane < kNumMaps ? &p.tmap_w[lane]
                                : lane < 2 * kNumMaps ? &p.tmap_s[lane - kNumMaps] : &p.tmap_b[lane - 2 * kNumMaps];
         if (lane < kNumMaps || p.sb_mode == kSbTma)
@@ -489,24 +527,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the stream still runs, and that kernel may have written the weights (a pack or a
         // quantiser, or any kernel of the caller's): the weight loads wait for it to complete.
         grid_dep_wait();
-        const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
-        const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
-        const int64_t srow_bytes = (int64_t)p.groups * 2;
         int it = 0, blk = 0;
         int rs = 0;             // ring slot and its phase
         uint32_t rph = 0;
         bool pending = false;   // an un-waited cluster-barrier arrival
-        if (RMS && C > 1) {     // matches the consumers' norm exchange
+        uint8_t* raw = smem + L.raw;   // raw mode: [2 buffers][scales | biases][raw_elems] bf16
+        const GemvOp& p = pp.op;
+        const bool fg = FG && p.fg;
+        const OpRange R0 = op_range(p, crank, cid, pp.n_clusters);
+        const int kg0 = R0.kg0, kg1 = R0.kg1, gsz = R0.gsz, nks = R0.nks, t_end = R0.t_end;
+        const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
+        const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
+        const int64_t srow_bytes = (int64_t)p.groups * 2;
+        if (RMS && p.rms && C > 1) {   // matches the consumers' norm exchange
             cluster_arrive();
             pending = true;
         }
-        uint8_t* raw = smem + L.raw;   // raw mode: [2 buffers][scales | biases][raw_elems] bf16
         // Raw mode: 1D boxes over the contiguous [rows][groups] scales and biases of a row
         // block. The first element is rounded down to a 16-byte boundary (TMA rule); the
         // transform skips the difference.
         auto raw_issue = [&](const Job& jb, int buf) {
             if (lane != 0) return;
-            const Segment& sgb = p.seg[jb.seg];
+            const Segment& sgb = pp.seg[jb.seg];
             const int64_t r0 = (int64_t)sgb.row0 + (int64_t)jb.tile * 16;
             const int rv = (int)llmin((int64_t)jb.ntile * 16, p.out_dim - (int64_t)jb.tile * 16);
             const int64_t e0 = r0 * p.groups;
@@ -522,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (int)(e0a + (int64_t)k * kRawBox), bar);
             }
         };
-        int t = t_begin;
+        int t = R0.t_begin;
         Job j;
         if (p.sb_mode == kSbRaw) {
             int t2 = t;
@@ -531,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
         while (next_job(p, t, t_end, j)) {
-            const Segment& sg = p.seg[j.seg];
+            const Segment& sg = pp.seg[j.seg];
             const int64_t lrow0 = (int64_t)j.tile * 16;                 // row within the segment
             const int rows_valid = (int)llmin((int64_t)j.ntile * 16, p.out_dim - lrow0);
             const int64_t trow0 = (int64_t)sg.row0 + lrow0;              // row within the tensor
@@ -547,21 +589,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.sb_mode == kSbTma) {
                     if (lane == 0) {
                         const int nchunk = (gsz + 63) / 64;
-                        mbar_arrive_expect_tx(bar, (uint32_t)((FG ? 4 : 2) * nchunk * j.ntile * kTileBytes));
-                        for (int part = 0; part < (FG ? 2 : 1); ++part) {   // fused: gate rows, up rows
+                        mbar_arrive_expect_tx(bar, (uint32_t)((fg ? 4 : 2) * nchunk * j.ntile * kTileBytes));
+                        for (int part = 0; part < (fg ? 2 : 1); ++part) {   // fused: gate rows, up rows
                             const int64_t prow = trow0 + (part ? p.out_dim : 0);
                             const int mbase = part * (MT / 2);
-                            int m0 = 0;
-                            for (int lg = kNumMaps - 1; lg >= 0; --lg) {
-                                const int h = 1 << lg;
-                                if (j.ntile - m0 < h) continue;
-                                for (int c = 0; c < nchunk; ++c) {
-                                    const uint32_t o = (uint32_t)((c * MT + mbase + m0) * kTileBytes);
-                                    tma_load_2d(smem_addr(sdst + o), &p.tmap_s[lg], kg0 + 64 * c, (int)(prow + 16 * m0), bar);
-                                    tma_load_2d(smem_addr(sdst + L.sb_pitch + o), &p.tmap_b[lg], kg0 + 64 * c,
-                                                (int)(prow + 16 * m0), bar);
-                                }
-                                m0 += h;
+                            const int mi = j.ntile - 1;   // one box of the row block's height
+                            for (int c = 0; c < nchunk; ++c) {
+                                const uint32_t o = (uint32_t)((c * p.sb_tiles + mbase) * kTileBytes);
+                                tma_load_2d(smem_addr(sdst + o), &p.tmap_s[mi], kg0 + 64 * c, (int)prow, bar);
+                                tma_load_2d(smem_addr(sdst + p.sb_pitch + o), &p.tmap_b[mi], kg0 + 64 * c, (int)prow, bar);
                             }
                         }
                     }
@@ -590,9 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (k < gsz)
                             v = *reinterpret_cast<const uint16_t*>((isb ? b8 : s8) + (trow0 + r) * srow_bytes +
                                                                    (int64_t)(kg0 + k) * 2);
-                        const uint32_t o = (uint32_t)(((k >> 6) * MT * 16 + r) * 128) +
+                        const uint32_t o = (uint32_t)(((k >> 6) * p.sb_tiles * 16 + r) * 128) +
                                            ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
-                        *reinterpret_cast<uint16_t*>(sdst + (size_t)isb * L.sb_pitch + o) = v;
+                        *reinterpret_cast<uint16_t*>(sdst + (size_t)isb * p.sb_pitch + o) = v;
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar);
@@ -615,25 +651,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // box columns of 128 bytes: 4 groups of nibbles, 8 groups of 2-bit codes
                 const int nbox = CB == 4 ? (ng + 3) / 4 : 1;
                 if (lane == 0) {
-                    // One tall box per box column for each power-of-two run of tiles: the
-                    // TMA engine pays per box, so few large boxes keep HBM streaming.
-                    mbar_arrive_expect_tx(full, (uint32_t)((FG ? 2 : 1) * j.ntile *
+                    // One box per box column as tall as the row block: the TMA engine pays per
+                    // box (small boxes cap the stream well below HBM), so few large boxes.
+                    mbar_arrive_expect_tx(full, (uint32_t)((fg ? 2 : 1) * j.ntile *
                                                            (nbox * kTileBytes + (CB == 3 ? kLoTileBytes : 0))));
-                    for (int part = 0; part < (FG ? 2 : 1); ++part) {   // fused: gate rows, up rows
+                    const int mi = j.ntile - 1;
+                    for (int part = 0; part < (fg ? 2 : 1); ++part) {   // fused: gate rows, up rows
                         const int64_t prow = trow0 + (part ? p.out_dim : 0);
                         const int mbase = part * (MT / 2);
-                        int m0 = 0;
-                        for (int lg = kNumMaps - 1; lg >= 0; --lg) {
-                            const int h = 1 << lg;
-                            if (j.ntile - m0 < h) continue;
-                            for (int c = 0; c < nbox; ++c)
-                                tma_load_2d(smem_addr(st + (c * MT + mbase + m0) * kTileBytes), &p.tmap_w[lg],
-                                            CB == 4 ? (g0 + 4 * c) * 32 : g0 * 16, (int)(prow + 16 * m0), full);
-                            if constexpr (CB == 3)   // lowest bits: 8 bytes per group and row
-                                tma_load_2d(smem_addr(st + MT * kTileBytes + (mbase + m0) * kLoTileBytes), &p.tmap_lo[lg],
-                                            g0 * 8, (int)(prow + 16 * m0), full);
-                            m0 += h;
-                        }
+                        for (int c = 0; c < nbox; ++c)
+                            tma_load_2d(smem_addr(st + (c * MT + mbase) * kTileBytes), &p.tmap_w[mi],
+                                        CB == 4 ? (g0 + 4 * c) * 32 : g0 * 16, (int)prow, full);
+                        if constexpr (CB == 3)   // lowest bits: 8 bytes per group and row
+                            tma_load_2d(smem_addr(st + MT * kTileBytes + mbase * kLoTileBytes), &p.tmap_lo[mi], g0 * 8,
+                                        (int)prow, full);
                     }
                 }
                 __syncwarp();
@@ -653,11 +684,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = lane >> 2;
         const int tq = lane & 3;
         grid_dep_wait();   // activations, the row map and y may belong to the previous kernel
+        float acc[TPW][NT][4];
+        uint8_t* xbias = smem + L.xbias;
+        int rs = 0;            // ring slot and its phase
+        uint32_t rph = 0;
+        int blk = 0;
+        const GemvOp& p = pp.op;
+        const bool fg = FG && p.fg;
+        const bool rms = RMS && p.rms;
+        const OpRange R0 = op_range(p, crank, cid, pp.n_clusters);
+        const int kg0 = R0.kg0, gsz = R0.gsz, nks = R0.nks, t_end = R0.t_end;
 
-        if (RMS) {
+        if (rms) {
             // Sum of squares of this CTA's K-slice per activation row, exchanged across the
             // cluster so every CTA normalises with the full-row statistics.
-            rms_partial<NT>(p, p.seg[0], kg0, gsz, ssq_s, warp, lane);
+            rms_partial<NT>(p, pp.seg[0], kg0, gsz, ssq_s, wpart, warp, lane, ctid);
             if (C > 1) {
                 cluster_arrive();
                 cluster_wait();
@@ -674,8 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             consumer_sync();
         }
 
-        float acc[TPW][NT][4];
-        uint8_t* xbias = smem + L.xbias;
         // Per-warp constants (32-bit shared addresses; per-tile steps are immediates).
         // ldmatrix: rows 0-7 / 8-15 of a tile, 16-byte granules 2*(wg&3) and 2*(wg&3)+1 of
         // its box column; 128-byte swizzle granule ^= row & 7.
@@ -697,16 +736,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scales: [chunk][row][128 B]; this lane's rows g (and g+8) of the warp's first tile
         const uint32_t s_lane = (uint32_t)(g * 128) + 2u * (uint32_t)wg;
         int staged_seg = -1;
-        int rs = 0;            // ring slot and its phase
-        uint32_t rph = 0;
-        int blk = 0;
-        int t = t_begin;
+        int t = R0.t_begin;
         Job j;
         while (next_job(p, t, t_end, j)) {
-            const Segment& sg = p.seg[j.seg];
+            const Segment& sg = pp.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS, CB>(p, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
-                                     RMS && cid == 0 && p.x_new != nullptr);
+                stage_x<NT, RMS, CB>(p, rms, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
+                                     rms && cid == 0 && p.x_new != nullptr);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
                 consumer_sync();
@@ -749,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t hi = k0 + 1 < gsz ? (uint32_t)src[k0 + 1] : 0u;
                         pk[e] = lo | (hi << 16);
                     }
-                    const uint32_t o = (uint32_t)((((u >> 3) * MT * 16) + r) * 128) + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(sdst + (size_t)isb * L.sb_pitch + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    const uint32_t o = (uint32_t)((((u >> 3) * p.sb_tiles * 16) + r) * 128) + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sdst + (size_t)isb * p.sb_pitch + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 consumer_sync();
                 if (ctid == 0) mbar_arrive(smem_addr(rawempty_b + (blk & 1)));
@@ -758,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(smem_addr(sbfull_b + q), (uint32_t)(blk / (int)L.n_sb) & 1u, abort_flag);
             }
             const uint8_t* sbs = sbuf + (size_t)q * L.sb_buf;         // scales
-            const uint8_t* sbb = sbs + L.sb_pitch;                    // biases
+            const uint8_t* sbb = sbs + p.sb_pitch;                    // biases
             const uint32_t s_blk = smem_addr(sbs) + s_lane;
             bool tok_ok[NT];
 #pragma unroll
@@ -803,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bf[nt][4] = q1.x; bf[nt][5] = q1.y; bf[nt][6] = q1.z; bf[nt][7] = q1.w;
                     }
                     // group gl = 8ks + wg: chunk ks/8, granule (ks & 7) ^ g, element wg
-                    const uint32_t sa = s_blk + (uint32_t)((ks >> 3) * MT * kTileBytes) +
+                    const uint32_t sa = s_blk + (uint32_t)((ks >> 3) * p.sb_tiles * kTileBytes) +
                                         ((uint32_t)((ks & 7) ^ g) << 4);
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
@@ -890,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // groups 16gb..16gb+15 = granules 2*(gb&3), +1 of 64-group chunk gb>>2
                     const uint32_t gran = (uint32_t)(gb & 3) * 2 + (uint32_t)(lane >> 4);
-                    const uint32_t boff = smem_addr(sbb) + (uint32_t)((gb >> 2) * MT * kTileBytes) + lrow * 128 +
+                    const uint32_t boff = smem_addr(sbb) + (uint32_t)((gb >> 2) * p.sb_tiles * kTileBytes) + lrow * 128 +
                                           ((gran ^ (lrow & 7)) << 4);
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
@@ -904,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (CB != 4) {
                             // the reconstruction offset: + (1.5 or 0.5) * sum_g s[o][g] * xsum[r][g]
                             constexpr float koff = CB == 2 ? 1.5f : 0.5f;
-                            ldsm_x4(boff - (uint32_t)L.sb_pitch + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
+                            ldsm_x4(boff - p.sb_pitch + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
                                 float d2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -925,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int mi = 0; mi < TPW; ++mi) {
                 const int m = mi;
-                if ((FG ? m % (MT / 2) : m) >= j.ntile) continue;
+                if ((fg ? m % (MT / 2) : m) >= j.ntile) continue;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float* w0 = wpart + ((size_t)wg * (16 * MT) + m * 16 + g) * NTOK + nt * 8 + 2 * tq;
@@ -936,8 +972,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             consumer_sync();
             float* cp = cpart + (size_t)(blk & 1) * (16 * MT) * NTOK;
             // fused: the gate rows [0, R) and the up rows [8 MT, 8 MT + R) of the row block
-            for (int e0 = ctid; e0 < (FG ? 2 : 1) * R * NTOK; e0 += kConsumerWarps * 32) {
-                const int e = (FG && e0 >= R * NTOK) ? e0 - R * NTOK + 8 * MT * NTOK : e0;
+            for (int e0 = ctid; e0 < (fg ? 2 : 1) * R * NTOK; e0 += kConsumerWarps * 32) {
+                const int e = (fg && e0 >= R * NTOK) ? e0 - R * NTOK + 8 * MT * NTOK : e0;
                 const size_t stride = (size_t)(16 * MT) * NTOK;
                 float v = wpart[e];
 #pragma unroll
@@ -970,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         v = cp[row * NTOK + tok];
                     }
-                    if constexpr (FG) {
+                    if (fg) {
                         float u;
                         if (C > 1) {
                             const uint32_t off = (uint32_t)(((8 * MT + row) * NTOK + tok) * 4);
@@ -1067,9 +1103,9 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1146,9 +1182,9 @@ int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_
                    : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1162,9 +1198,9 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
-    prm.n_clusters = max_clusters < prm.n_tiles ? max_clusters : prm.n_tiles;
+    prm.n_clusters = max_clusters < prm.op.n_tiles ? max_clusters : prm.op.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
     cfg.numAttrs = 2;
     static const bool debug = getenv("Q4A_DEBUG") != nullptr;
@@ -1172,10 +1208,97 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
         fprintf(stderr,
                 "q4a gemv: nt=%d rms=%d segs=%d out=%lld in=%lld cluster=%d gs=%d mt=%d stages=%d "
                 "clusters=%d (max %d) tiles=%d smem=%u sb_mode=%d\n",
-                NT, (int)RMS, prm.nseg, (long long)prm.out_dim, (long long)prm.in_dim, prm.cluster, prm.gs,
-                prm.mt, prm.stages, prm.n_clusters, max_clusters, prm.n_tiles, smem_bytes, prm.sb_mode);
+                NT, (int)RMS, prm.nseg, (long long)prm.op.out_dim, (long long)prm.op.in_dim, prm.cluster, prm.op.gs,
+                prm.op.mt, prm.stages, prm.n_clusters, max_clusters, prm.op.n_tiles, smem_bytes, prm.op.sb_mode);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
     if (e != cudaSuccess) return cuda_fail(e);
+    return Q4A_OK;
+}
+
+// One op of a launch from its description: the tensor maps of its codes (and 3-bit lowest
+// bits), of its scales and biases in the chosen fetch mode, and its shape and schedule.
+q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_mode, int sb_tiles, uint32_t sb_pitch) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return Q4A_ERR_UNSUPPORTED;
+    const int cb = L.code_bits;
+    const int G = (int)(L.in_dim / kGroup);
+    // packed codes: in_dim/2 bytes per row (nibbles) or in_dim/4 (2-bit codes; the 3-bit
+    // codes' upper two bits); the 3-bit lowest-bit plane: in_dim/8 bytes per row
+    const int64_t wrow = cb == 4 ? L.in_dim / 2 : L.in_dim / 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)wrow, (cuuint64_t)L.tensor_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)wrow};
+    const cuuint32_t estr[2] = {1u, 1u};
+    for (int i = 0; i < kNumMaps; ++i) {
+        const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)(16 * (i + 1))};
+        CUresult r = enc(&o.tmap_w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        if (cb == 3) {
+            const cuuint64_t ldims[2] = {(cuuint64_t)(L.in_dim / 8), (cuuint64_t)L.tensor_rows};
+            const cuuint64_t lstrides[1] = {(cuuint64_t)(L.in_dim / 8)};
+            const cuuint32_t lbox[2] = {64u, (cuuint32_t)(16 * (i + 1))};
+            r = enc(&o.tmap_lo[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w_lo), ldims, lstrides,
+                    lbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        }
+    }
+    o.s = L.s;
+    o.b = L.b;
+    o.x = L.x;
+    o.x_rows = L.x_rows;
+    o.norm_w = L.norm_w;
+    o.inj_out = L.inj_out;
+    o.inj_logit = L.inj_logit;
+    o.x_new = L.inj_out ? L.x_new : nullptr;
+    o.y = L.y;
+    o.h = L.h;
+    o.eps = L.eps;
+    o.shift = L.shift;
+    o.norm_groups = L.norm_groups > 0 ? L.norm_groups : 1;
+    o.norm_width = L.in_dim / o.norm_groups;
+    o.post_silu = L.silu ? 1 : 0;
+    o.post_div = L.silu ? L.silu_div : 1.0f;
+    o.out_dim = L.out_dim;
+    o.in_dim = L.in_dim;
+    o.groups = G;
+    o.gs = gs;
+    o.tiles_per_seg = (int)((L.out_dim + 15) / 16);
+    o.n_tiles = o.tiles_per_seg * L.nseg;
+    o.mt = mt_units;
+    o.ntok_max = L.max_ntok;
+    o.sb_mode = sb_mode;
+    o.sb_tiles = sb_tiles;
+    o.sb_pitch = sb_pitch;
+    o.rms = L.rmsnorm ? 1 : 0;
+    o.fg = L.fused_gate_up ? 1 : 0;
+    if (sb_mode == kSbTma) {
+        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
+        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
+        for (int i = 0; i < kNumMaps; ++i) {
+            const cuuint32_t box[2] = {64u, (cuuint32_t)(16 * (i + 1))};
+            for (int k = 0; k < 2; ++k) {
+                CUresult r = enc(k ? &o.tmap_b[i] : &o.tmap_s[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t*>(k ? L.b : L.s), sdims, sstrides, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+            }
+        }
+    }
+    if (sb_mode == kSbRaw) {
+        const cuuint64_t rdims[1] = {(cuuint64_t)(L.tensor_rows * G)};
+        const cuuint64_t rstrides[1] = {0};
+        const cuuint32_t rbox[1] = {(cuuint32_t)kRawBox};
+        for (int k = 0; k < 2; ++k) {
+            CUresult r = enc(k ? &o.tmap_b1 : &o.tmap_s1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1,
+                             const_cast<uint16_t*>(k ? L.b : L.s), rdims, rstrides, rbox, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        }
+    }
     return Q4A_OK;
 }
 
@@ -1184,18 +1307,17 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     static_assert(sizeof(GemvParams<MAXSEG>) < 32000, "kernel parameter block too large");
     const DeviceInfo di = device_info();
     if (!di.ok) return Q4A_ERR_CUDA;
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return Q4A_ERR_UNSUPPORTED;
+    if (!encode_fn()) return Q4A_ERR_UNSUPPORTED;
     if (L.nseg > MAXSEG) return Q4A_ERR_SHAPE;
 
     const int nt = L.max_ntok <= 8 ? 1 : (L.max_ntok <= 16 ? 2 : 4);
-    const int mt = tiles_per_block(nt);
+    int mt = tiles_per_block(nt);
     const int cb = L.code_bits;
     if (cb != 4 && (L.experts || L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
     const bool fg = L.fused_gate_up;
     if (fg && (L.experts || cb != 4 || L.silu || L.out_dim % 16 != 0 || !L.h)) return Q4A_ERR_UNSUPPORTED;
     // schedule units per row block: tiles, or (fused) gate|up tile pairs
-    const int mt_units = fg ? mt / 2 : mt;
+    int mt_units = fg ? mt / 2 : mt;
     const int G = (int)(L.in_dim / kGroup);
 
     // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
@@ -1247,6 +1369,18 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     }
     if (C == 0) return Q4A_ERR_UNSUPPORTED;
     const int gs = slice(C);
+    // Plain dense products whose clusters get at most 2 or 4 tiles run the kernel built for
+    // row blocks of that height (the default height would spend mma work on absent rows).
+    if (MAXSEG == kDenseMaxSeg && !fg && !L.rmsnorm && cb == 4 && nt <= 2) {
+        const int q = cluster_capacity(nt, false, false, C, smem_layout(nt, mt, 3, gs, ntm, sbmode(C), sbufs(C), cb).total + 1024,
+                                       cb, false);
+        const int64_t per = q > 0 ? (n_tiles + q - 1) / q : mt;
+        const int short_mt = per <= 2 ? 2 : (per <= 4 ? 4 : mt);
+        if (short_mt < mt) {
+            mt = short_mt;
+            mt_units = short_mt;
+        }
+    }
     int stages = 8;
     while (stages > 2 && !fits(C, stages)) --stages;
     if (!fits(C, stages)) return Q4A_ERR_UNSUPPORTED;
@@ -1255,83 +1389,11 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
     memset(&prm, 0, sizeof(prm));
-    // packed codes: in_dim/2 bytes per row (nibbles) or in_dim/4 (2-bit codes; the 3-bit
-    // codes' upper two bits); the 3-bit lowest-bit plane: in_dim/8 bytes per row
-    const int64_t wrow = cb == 4 ? L.in_dim / 2 : L.in_dim / 4;
-    const cuuint64_t dims[2] = {(cuuint64_t)wrow, (cuuint64_t)L.tensor_rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)wrow};
-    const cuuint32_t estr[2] = {1u, 1u};
-    for (int i = 0; i < kNumMaps; ++i) {
-        const cuuint32_t box[2] = {(cuuint32_t)kBoxBytes, (cuuint32_t)(16 << i)};
-        CUresult r = enc(&prm.tmap_w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-        if (cb == 3) {
-            const cuuint64_t ldims[2] = {(cuuint64_t)(L.in_dim / 8), (cuuint64_t)L.tensor_rows};
-            const cuuint64_t lstrides[1] = {(cuuint64_t)(L.in_dim / 8)};
-            const cuuint32_t lbox[2] = {64u, (cuuint32_t)(16 << i)};
-            r = enc(&prm.tmap_lo[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(L.w_lo), ldims, lstrides,
-                    lbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-        }
-    }
-
-    prm.s = L.s;
-    prm.b = L.b;
-    prm.x = L.x;
-    prm.x_rows = L.x_rows;
-    prm.norm_w = L.norm_w;
-    prm.inj_out = L.inj_out;
-    prm.inj_logit = L.inj_logit;
-    prm.x_new = L.inj_out ? L.x_new : nullptr;
-    prm.y = L.y;
-    prm.h = L.h;
-    prm.eps = L.eps;
-    prm.shift = L.shift;
-    prm.norm_groups = L.norm_groups > 0 ? L.norm_groups : 1;
-    prm.norm_width = L.in_dim / prm.norm_groups;
-    prm.post_silu = L.silu ? 1 : 0;
-    prm.post_div = L.silu ? L.silu_div : 1.0f;
-    prm.out_dim = L.out_dim;
-    prm.in_dim = L.in_dim;
-    prm.groups = G;
-    prm.gs = gs;
+    q4a_status st = fill_op(prm.op, L, gs, mt_units, sbmode(C), mt, lay.sb_pitch);
+    if (st != Q4A_OK) return st;
     prm.cluster = C;
-    prm.tiles_per_seg = (int)((L.out_dim + 15) / 16);
     prm.nseg = L.nseg;
-    prm.n_tiles = prm.tiles_per_seg * L.nseg;
-    prm.mt = mt_units;
-    prm.ntok_max = ntm;
     prm.stages = stages;
-    prm.sb_mode = sbmode(C);
-    if (prm.sb_mode == kSbTma) {
-        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
-        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
-        for (int i = 0; i < kNumMaps; ++i) {
-            const cuuint32_t box[2] = {64u, (cuuint32_t)(16 << i)};
-            for (int k = 0; k < 2; ++k) {
-                CUresult r = enc(k ? &prm.tmap_b[i] : &prm.tmap_s[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 const_cast<uint16_t*>(k ? L.b : L.s), sdims, sstrides, box, estr,
-                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-            }
-        }
-    }
-    if (prm.sb_mode == kSbRaw) {
-        const cuuint64_t rdims[1] = {(cuuint64_t)(L.tensor_rows * G)};
-        const cuuint64_t rstrides[1] = {0};
-        const cuuint32_t rbox[1] = {(cuuint32_t)kRawBox};
-        for (int k = 0; k < 2; ++k) {
-            CUresult r = enc(k ? &prm.tmap_b1 : &prm.tmap_s1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1,
-                             const_cast<uint16_t*>(k ? L.b : L.s), rdims, rstrides, rbox, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-        }
-    }
     prm.lay = lay;
     for (int i = 0; i < L.nseg; ++i) prm.seg[i] = L.seg[i];
 
@@ -1362,6 +1424,11 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
             if (nt == 2) return launch_variant<2, true, MAXSEG>(prm, smem_bytes, stream);
             return launch_variant<4, true, MAXSEG>(prm, smem_bytes, stream);
         }
+    }
+    if constexpr (MAXSEG == kDenseMaxSeg) {
+        if (nt == 1 && mt == 2) return launch_variant<1, false, MAXSEG, 4, false, 2>(prm, smem_bytes, stream);
+        if (nt == 1 && mt == 4) return launch_variant<1, false, MAXSEG, 4, false, 4>(prm, smem_bytes, stream);
+        if (nt == 2 && mt == 2) return launch_variant<2, false, MAXSEG, 4, false, 2>(prm, smem_bytes, stream);
     }
     if (nt == 1) return launch_variant<1, false, MAXSEG>(prm, smem_bytes, stream);
     if (nt == 2) return launch_variant<2, false, MAXSEG>(prm, smem_bytes, stream);

@@ -14,7 +14,8 @@ constexpr int kGroup = 64;              // inputs per scale/bias group
 constexpr int kStageGroups = 8;         // groups per pipeline stage (512 inputs)
 constexpr int kBoxBytes = 128;          // TMA box width in bytes (4 groups), 128B swizzle
 constexpr int kTileBytes = 16 * kBoxBytes;      // one 16-row tile of one box column: 2 KB
-constexpr int kNumMaps = 4;                     // box heights 16, 32, 64, 128 rows
+constexpr int kNumMaps = 6;                     // box heights 16, 32, ..., 96 rows: one box per
+                                                // box column of a row block (at most 6 tiles)
 constexpr int kGroupSlots = kStageGroups; // one consumer warp per group of a stage
 constexpr int kConsumerWarps = kGroupSlots;       // each owns every tile of the row block
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -79,7 +80,8 @@ __host__ __device__ inline uint32_t sb_bytes(int /*sb_mode*/, int gs, int rows) 
 constexpr uint32_t kLoTileBytes = 16u * 64u;
 
 __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, int gs, int ntok_max,
-                                                  int sb_mode, int sb_bufs, int code_bits = 4) {
+                                                  int sb_mode, int sb_bufs, int code_bits = 4,
+                                                  uint32_t sb_pitch_bytes = 0) {
     SmemLayout L;
     const uint32_t ntok = 8u * nt, rows = 16u * mt;
     L.stage_bytes = (uint32_t)mt * (code_bits == 4 ? 2u : 1u) * kTileBytes +   // [box column][rows][128 B]
@@ -87,7 +89,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     L.ring = 0;                                             // relative to a 1024-aligned base
     L.xfrag = L.ring + (uint32_t)stages * L.stage_bytes;
     L.xsum = L.xfrag + align_up(xfrag_bytes(gs, ntok_max), 16);
-    L.sb_pitch = sb_bytes(sb_mode, gs, rows);               // scales, then biases
+    L.sb_pitch = sb_pitch_bytes ? sb_pitch_bytes : sb_bytes(sb_mode, gs, rows);   // scales, then biases
     L.sb_buf = 2u * L.sb_pitch;
     L.xbias = align_up(L.xsum + (uint32_t)gs * ntok * 4u, 16);   // bf16 hi/lo group sums
     L.sb = align_up(L.xbias + (uint32_t)((gs + 15) / 16) * ntok_max * 64u, 1024);
@@ -104,16 +106,16 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     return L;
 }
 
-template <int MAXSEG>
-struct GemvParams {
+// The product a launch computes: its weights, input, output and schedule.
+struct GemvOp {
     CUtensorMap tmap_w[kNumMaps];  // 2D uint8: dim0 = in_dim/2 bytes, dim1 = tensor rows;
-                                   // box 128 bytes x (16 << i) rows, 128-byte swizzle
+                                   // box 128 bytes x 16 (i + 1) rows, 128-byte swizzle
     CUtensorMap tmap_s[kNumMaps];  // 2D bf16 scales/biases: dim0 = groups, dim1 = rows;
-    CUtensorMap tmap_b[kNumMaps];  // box 64 groups x (16 << i) rows, 128-byte swizzle
+    CUtensorMap tmap_b[kNumMaps];  // box 64 groups x 16 (i + 1) rows, 128-byte swizzle
     CUtensorMap tmap_s1;           // raw mode: 1D bf16 views of s and b (rows * groups
     CUtensorMap tmap_b1;           // elements), box kRawBox elements
     CUtensorMap tmap_lo[kNumMaps]; // 3-bit codes: lowest-bit plane, dim0 = in_dim/8 bytes,
-                                   // box 64 bytes x (16 << i) rows, no swizzle
+                                   // box 64 bytes x 16 (i + 1) rows, no swizzle
     const uint16_t* s;        // bf16 [rows][G]
     const uint16_t* b;
     const void* x;            // fp16 [*][in_dim] (or fp32 x_raw for the RMSNorm variant)
@@ -133,15 +135,24 @@ struct GemvParams {
     int64_t in_dim;
     int32_t groups;           // in_dim / 64
     int32_t gs;               // groups per CTA K-slice
-    int32_t cluster;          // CTAs per cluster (K split)
-    int32_t n_clusters;
     int32_t tiles_per_seg;    // ceil(out_dim / 16)
     int32_t n_tiles;          // nseg * tiles_per_seg
-    int32_t nseg;
-    int32_t mt;               // tiles per row block
+    int32_t mt;               // schedule units per row block (fused gate|up: pairs of tiles)
     int32_t ntok_max;         // activation rows of the widest segment (<= 8 * NT)
-    int32_t stages;           // ring depth
     int32_t sb_mode;
+    int32_t sb_tiles;         // 16-row tiles per 64-group chunk of a row block's staged scales
+    uint32_t sb_pitch;        // bytes from a row block's staged scales to its biases
+    int32_t rms;              // RMSNorm prologue: x is fp32 x_raw (kernels built with RMS)
+    int32_t fg;               // fused gate|up epilogue into h (kernels built with FG)
+};
+
+template <int MAXSEG>
+struct GemvParams {
+    GemvOp op;
+    int32_t cluster;          // CTAs per cluster (K split)
+    int32_t n_clusters;
+    int32_t nseg;
+    int32_t stages;           // ring depth
     SmemLayout lay;
     Segment seg[MAXSEG];
 };

@@ -62,6 +62,7 @@ typedef enum q4a_status {
 /* Upper limits of the host-side schedule. */
 #define Q4A_MAX_SEGMENTS 512   /* routed-expert segments per q4a_gemv_experts call */
 
+
 /* Static string for a status code (never NULL). */
 Q4A_API const char* q4a_status_string(q4a_status status);
 
@@ -154,6 +155,8 @@ Q4A_API q4a_status q4a_gemv_rmsnorm_gate_up_silu(uint16_t* h, const uint8_t* w, 
  *                  then up rows (as q4a_gemv_gate_up_silu)
  *   x_raw, norm_w, eps, shift   in  as q4a_gemv_rmsnorm (one normalisation group)
  *   w_dn, s_dn, b_dn   in  [hidden][inter/2] codes, [hidden][inter/64] bf16
+ *   Two launches, the same kernels as the separate entry points; the second starts under
+ *   programmatic dependent launch while the first drains.
  *   Requires 1 <= nb <= 32, hidden % 512 == 0, inter % 64 == 0; w_gu, w_dn, x_raw, norm_w and
  *   h 16-byte aligned; s_gu, b_gu 16-byte aligned; s_dn, b_dn 2-byte aligned. Everything is
  *   planned before anything is launched, so a rejected call launches nothing.

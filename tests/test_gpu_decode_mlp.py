@@ -60,14 +60,17 @@ def check_y(y, dn, h_bits, what):
     assert worst <= 1.0, f"{what}: y worst err/bound {worst:.3g}"
 
 
-def run_layer(hidden, inter, nb, seed):
+def run_layer(hidden, inter, nb, seed, repeat=1):
+    """One decode layer through q4a_decode_mlp, checked against the oracle."""
     gu = quant(2 * inter, hidden, seed)
     dn = quant(hidden, inter, seed + 1)
     a = wl.normal_f32(93, seed % 7, (nb, hidden)) * 2.0
     nw = wl.norm_weight(93, 1, hidden)
-    y = torch.full((nb, hidden), float("nan"), device=DEV)
-    h = torch.full((nb, inter), float("nan"), dtype=torch.float16, device=DEV)
-    q4a.decode_mlp(*(dev(t) for t in gu), dev(a), dev(nw), *(dev(t) for t in dn), eps=1e-6, out=y, h=h)
+    args = [dev(t) for t in gu] + [dev(a), dev(nw)] + [dev(t) for t in dn]
+    for _ in range(repeat):
+        y = torch.full((nb, hidden), float("nan"), device=DEV)
+        h = torch.full((nb, inter), float("nan"), dtype=torch.float16, device=DEV)
+        q4a.decode_mlp(*args, eps=1e-6, out=y, h=h)
     torch.cuda.synchronize()
     q4a.check_device_error()
     xn, _ = oracle.rmsnorm_f16(a, nw, eps=1e-6)
@@ -79,15 +82,22 @@ def run_layer(hidden, inter, nb, seed):
 
 
 @pytest.mark.parametrize("hidden,inter,nb", [(512, 128, 1), (1024, 640, 3), (2048, 1024, 8), (4096, 1024, 16),
-                                             (512, 256, 32)])
+                                             (512, 256, 32), (1024, 512, 5), (512, 1536, 2)])
 def test_decode_mlp_matches_oracle(hidden, inter, nb):
+    """Shapes from 512 to 4096 inputs, 1 to 32 activation rows."""
     run_layer(hidden, inter, nb, hidden + inter + nb)
 
 
 def test_decode_mlp_full_size():
-    """The dense decode layer of the workloads: 4096 -> 2 x 6144 -> 4096 at NB 1 and 16."""
-    for nb in (1, 16):
+    """The dense decode layer of the workloads: 4096 -> 2 x 6144 -> 4096 at NB 1, 8 and 16."""
+    for nb in (1, 8, 16):
         run_layer(4096, 6144, nb, 7 + nb)
+
+
+def test_decode_mlp_back_to_back():
+    """Several calls on one stream with no sync between them (each launch overlaps the tail of
+    the one before under programmatic dependent launch)."""
+    run_layer(2048, 1024, 4, 21, repeat=6)
 
 
 def test_pack_then_gemv_without_a_sync():
