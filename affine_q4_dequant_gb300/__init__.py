@@ -27,7 +27,7 @@ from . import _build
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
     "gemv_rmsnorm_grouped", "gemv_inject_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "decode_mlp", "lowbit_pack",
-    "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error",
+    "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error", "debug_withhold_stage",
     "STATUS", "MAX_SEGMENTS",
 ]
 
@@ -75,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "q4a_silu_mul_xsum": (I32, [P, P, P, I64, I64, P]),
         "q4a_moe_combine": (I32, [P, P, P, P, I32, I32, I64, I64, P, P, P, P]),
         "q4a_check_device_error": (I32, [P]),
+        "q4a_debug_withhold_stage": (I32, [I32]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -407,3 +408,10 @@ def moe_combine(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, y_shared: 
 
 def check_device_error(stream=None) -> None:
     _check("q4a_check_device_error", _lib.q4a_check_device_error(_stream(stream)))
+
+
+def debug_withhold_stage(stage: int) -> None:
+    """Failure-path testing: the next GEMV-kernel launch from this thread never loads weight
+    stage `stage` of each CTA, so its bounded wait gives up (check_device_error then raises
+    ERR_TIMEOUT). -1 clears the request."""
+    _check("q4a_debug_withhold_stage", _lib.q4a_debug_withhold_stage(int(stage)))

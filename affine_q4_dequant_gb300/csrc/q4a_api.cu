@@ -10,6 +10,13 @@
 namespace q4a {
 
 static thread_local int t_last_cuda_error = 0;
+static thread_local int t_withhold_stage = -1;
+
+int take_withhold_stage() {
+    const int v = t_withhold_stage;
+    t_withhold_stage = -1;
+    return v;
+}
 
 q4a_status cuda_fail(cudaError_t e) {
     t_last_cuda_error = (int)e;
@@ -64,6 +71,12 @@ const char* q4a_status_string(q4a_status status) {
 }
 
 int q4a_last_cuda_error(void) { return t_last_cuda_error; }
+
+q4a_status q4a_debug_withhold_stage(int stage) {
+    if (stage < -1) return Q4A_ERR_SHAPE;
+    t_withhold_stage = stage;
+    return Q4A_OK;
+}
 
 q4a_status q4a_pack(uint8_t* w_packed, const uint8_t* codes, int64_t rows, int64_t in_dim,
                     q4a_stream_t stream) {
@@ -121,7 +134,7 @@ q4a_status gemv_common(float* y, const uint8_t* w, const uint16_t* s, const uint
     if (st != Q4A_OK) return st;
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(s, 2) || !aligned(b, 2) || !aligned(y, 4))
         return Q4A_ERR_ALIGN;
-    if (dense_tc_eligible(s, b, nb, in_dim))
+    if (dense_tc_eligible(s, b, nb, out_dim, in_dim))
         return launch_dense_tc(w, s, b, x, y, nb, out_dim, in_dim, silu, silu_div, stream);
     std::vector<Segment> segs;
     push_segments(segs, 0, 0, nb);

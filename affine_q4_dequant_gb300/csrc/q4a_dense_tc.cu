@@ -156,8 +156,8 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-// 32 TMEM lanes (this warp's quarter) x 32 columns from 32 registers per thread; returns
-// once the stores have completed.
+// 32 TMEM lanes (this warp's quarter) x 32 columns from 32 registers per thread (asynchronous:
+// tc_wait_st orders it before the MMA that reads it).
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -167,13 +167,34 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// Completion of this thread's earlier tcgen05.st: once per operand stage, before the MMA warp
+// is told the stage is ready (a wait after every store would serialise the dequantisation of
+// a stage's groups on the store latency).
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Arrives on the mbarrier once every tcgen05.mma this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// 32 TMEM lanes (this warp's quarter) x 32 fp32 columns, one wait for all of them.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 // 32 TMEM lanes (this warp's quarter) x 16 fp32 columns: thread i gets lane base+i.
@@ -427,21 +448,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             for (int u = 0; u < kTcUm; ++u) {
                 const int64_t row = (int64_t)unit * kTcUnitRows + u * kTcM + rl;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kTcUm + u) * p.n_pad);
-                for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
+                // 32 accumulator columns per TMEM load (one load latency per 32 activation rows)
+                auto emit = [&](int c0, const float* v, int n) {
+                    if (row >= p.out_dim) return;
+                    for (int j = 0; j < n; ++j)
+                        if (c0 + j < p.nb) {
+                            float o = v[j] * esc[u];
+                            if (p.silu) {
+                                const float t = o / p.silu_div;
+                                o = t / (1.0f + expf(-t));
+                            }
+                            p.y[(int64_t)(c0 + j) * p.out_dim + row] = o;
+                        }
+                };
+                int c0 = 0;
+                for (; c0 + 32 <= p.n_pad; c0 += 32) {
+                    float v[32];
+                    tc_ld32(taddr + (uint32_t)c0, v);
+                    emit(c0, v, 32);
+                }
+                if (c0 < p.n_pad) {
                     float v[16];
                     tc_ld16(taddr + (uint32_t)c0, v);
-                    if (row < p.out_dim) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (c0 + j < p.nb) {
-                                float o = v[j] * esc[u];
-                                if (p.silu) {
-                                    const float t = o / p.silu_div;
-                                    o = t / (1.0f + expf(-t));
-                                }
-                                p.y[(int64_t)(c0 + j) * p.out_dim + row] = o;
-                            }
-                    }
+                    emit(c0, v, 16);
                 }
             }
             tc_fence_before();
@@ -507,6 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     }
                     tc_st32(a_lane + (uint32_t)((sa * kTcUm * kTcSG + gg) * kTcACols), h);
                     if (gg == kTcSG - 1) {
+                        tc_wait_st();
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_addr(a_full + sa));
@@ -583,7 +613,7 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
         const cuuint64_t dims[2] = {(cuuint64_t)(in_dim / 2), (cuuint64_t)out_dim};
         const cuuint64_t strides[1] = {(cuuint64_t)(in_dim / 2)};
         const cuuint32_t box[2] = {128u, (cuuint32_t)kTcM};
-        CUresult r = enc(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box,
+        CUresult r = encode_tiled_cached(&prm.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
@@ -593,7 +623,7 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
         const cuuint64_t dims[2] = {(cuuint64_t)in_dim, (cuuint64_t)nb};
         const cuuint64_t strides[1] = {(cuuint64_t)in_dim * 2};
         const cuuint32_t box[2] = {64u, (cuuint32_t)n_pad};
-        CUresult r = enc(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
+        CUresult r = encode_tiled_cached(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
@@ -646,8 +676,12 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
 
 }  // namespace
 
-bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_dim) {
-    return nb >= kDenseTcMinRows && (in_dim / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(s) % 16 == 0 &&
+bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim) {
+    // From NB 64, or from NB 17 on matrices tall enough to give every SM a 256-row unit (the
+    // GEMV kernel's 17..32-row form splits K across a cluster and loses to the contraction there;
+    // on shorter matrices the contraction has too few units to fill the GPU).
+    const bool wide = nb >= kDenseTcMinRows || (nb > 16 && out_dim >= (int64_t)kDenseTcTallRows);
+    return wide && (in_dim / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(s) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(b) % 16 == 0;
 }
 

@@ -76,6 +76,19 @@ __device__ __noinline__ void mbar_wait_slow(uint32_t bar, uint32_t parity, volat
     }
 }
 
+// Waits for a phase that TMA copies complete, whatever the abort flag says: a CTA must not
+// exit while its own copies may still write shared memory. Bounded like every other wait.
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((it & 3) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_device_error, 1u);
+            return;
+        }
+    }
+}
+
 __device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
     if (mbar_try_wait(bar, parity)) return;
     mbar_wait_slow(bar, parity, abort_flag);

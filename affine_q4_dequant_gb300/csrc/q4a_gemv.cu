@@ -31,8 +31,12 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <string.h>
+
 #include <map>
 #include <mutex>
+#include <string>
+#include <unordered_map>
 
 #include "q4a_device.cuh"
 #include "q4a_internal.h"
@@ -531,6 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rs = 0;             // ring slot and its phase
         uint32_t rph = 0;
         bool pending = false;   // an un-waited cluster-barrier arrival
+        // Lane 0's record of the copies it issued (bit 0: the latest), drained before the CTA
+        // exits: after an abort the consumers no longer wait for them. Once the abort flag is
+        // set no new copy is issued; the control flow (and every cluster barrier) stays as is.
+        uint32_t st_bits = 0, sb_bits = 0;
+        int raw_rb[2] = {-1, -1};   // raw mode: the row block whose scales each buffer received
         uint8_t* raw = smem + L.raw;   // raw mode: [2 buffers][scales | biases][raw_elems] bf16
         const GemvOp& p = pp.op;
         const bool fg = FG && p.fg;
@@ -546,8 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Raw mode: 1D boxes over the contiguous [rows][groups] scales and biases of a row
         // block. The first element is rounded down to a 16-byte boundary (TMA rule); the
         // transform skips the difference.
-        auto raw_issue = [&](const Job& jb, int buf) {
-            if (lane != 0) return;
+        auto raw_issue = [&](const Job& jb, int buf, int rb) {
+            if (lane != 0 || *abort_flag) return;
+            if (buf) raw_rb[1] = rb; else raw_rb[0] = rb;
             const Segment& sgb = pp.seg[jb.seg];
             const int64_t r0 = (int64_t)sgb.row0 + (int64_t)jb.tile * 16;
             const int rv = (int)llmin((int64_t)jb.ntile * 16, p.out_dim - (int64_t)jb.tile * 16);
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.sb_mode == kSbRaw) {
             int t2 = t;
             Job j0;
-            if (next_job(p, t2, t_end, j0)) raw_issue(j0, 0);
+            if (next_job(p, t2, t_end, j0)) raw_issue(j0, 0, 0);
             __syncwarp();
         }
         while (next_job(p, t, t_end, j)) {
@@ -587,7 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* sdst = sbuf + (size_t)q * L.sb_buf;
                 const uint32_t bar = smem_addr(sbfull_b + q);
                 if (p.sb_mode == kSbTma) {
-                    if (lane == 0) {
+                    if (lane == 0) sb_bits <<= 1;
+                    if (lane == 0 && !*abort_flag) {
+                        sb_bits |= 1u;
                         const int nchunk = (gsz + 63) / 64;
                         mbar_arrive_expect_tx(bar, (uint32_t)((fg ? 4 : 2) * nchunk * j.ntile * kTileBytes));
                         for (int part = 0; part < (fg ? 2 : 1); ++part) {   // fused: gate rows, up rows
@@ -610,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int nbuf = (blk + 1) & 1;
                         if (blk + 1 >= 2)
                             mbar_wait(smem_addr(rawempty_b + nbuf), (uint32_t)((blk + 1) / 2 - 1) & 1u, abort_flag);
-                        raw_issue(jn, nbuf);
+                        raw_issue(jn, nbuf, blk + 1);
                     }
                 } else {
                     // element copies into the swizzled layout (full K: one CTA per cluster);
@@ -650,7 +662,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ng = min(kStageGroups, kg1 - g0);
                 // box columns of 128 bytes: 4 groups of nibbles, 8 groups of 2-bit codes
                 const int nbox = CB == 4 ? (ng + 3) / 4 : 1;
-                if (lane == 0) {
+                if (lane == 0) st_bits <<= 1;
+                if (lane == 0 && !*abort_flag && it != p.withhold_stage) {
+                    st_bits |= 1u;
                     // One box per box column as tall as the row block: the TMA engine pays per
                     // box (small boxes cap the stream well below HBM), so few large boxes.
                     mbar_arrive_expect_tx(full, (uint32_t)((fg ? 2 : 1) * j.ntile *
@@ -676,6 +690,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++blk;
         }
+        if (lane == 0) {
+            for (int k = 0; k < S && k < it; ++k)
+                if ((st_bits >> k) & 1u) {
+                    const int q = it - 1 - k;
+                    mbar_drain(smem_addr(full_b + q % S), (uint32_t)(q / S) & 1u);
+                }
+            const int nsb = (int)L.n_sb;
+            for (int k = 0; k < nsb && k < blk; ++k)
+                if ((sb_bits >> k) & 1u) {
+                    const int q = blk - 1 - k;
+                    mbar_drain(smem_addr(sbfull_b + q % nsb), (uint32_t)(q / nsb) & 1u);
+                }
+            for (int b = 0; b < 2; ++b) {
+                const int rb = b ? raw_rb[1] : raw_rb[0];
+                if (rb >= 0) mbar_drain(smem_addr(rawfull_b + b), (uint32_t)(rb >> 1) & 1u);
+            }
+        }
+        __syncwarp();
         if (pending) cluster_wait();
     } else {
         // ======================= consumer warps =======================
@@ -1066,20 +1098,75 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+// Encoded tensor maps, keyed by every argument of the encode call: a map is a pure function of
+// them, and a decode step calls the same products with the same buffers over and over, so the
+// host-side encode (several per launch) runs once per buffer instead of once per call.
+CUresult encode_tiled_cached(CUtensorMap* out, CUtensorMapDataType dtype, cuuint32_t rank, void* ptr,
+                             const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                             const cuuint32_t* estr, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                             CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+    struct Key {
+        uint64_t v[20];
+    } key;
+    memset(&key, 0, sizeof(key));
+    key.v[0] = (uint64_t)dtype | ((uint64_t)rank << 8) | ((uint64_t)il << 16) | ((uint64_t)sw << 24) |
+               ((uint64_t)l2 << 32) | ((uint64_t)oob << 40);
+    key.v[1] = reinterpret_cast<uint64_t>(ptr);
+    for (cuuint32_t i = 0; i < rank && i < 5; ++i) {
+        key.v[2 + i] = dims[i];
+        key.v[7 + i] = i + 1 < rank ? strides[i] : 0;
+        key.v[12 + i] = ((uint64_t)box[i] << 32) | estr[i];
+    }
+    const std::string k(reinterpret_cast<const char*>(&key), sizeof(key));
+    static std::mutex mu;
+    static std::unordered_map<std::string, CUtensorMap> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(k);
+        if (it != cache.end()) {
+            *out = it->second;
+            return CUDA_SUCCESS;
+        }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return CUDA_ERROR_NOT_SUPPORTED;
+    const CUresult r = enc(out, dtype, rank, ptr, dims, strides, box, estr, il, sw, l2, oob);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache.size() >= 16384) cache.clear();   // a bound for callers that churn buffers
+        cache.emplace(k, *out);
+    }
+    return r;
+}
+
+namespace {
+
 struct DeviceInfo {
     int sm_count = 0;
     int max_smem_optin = 0;
     bool ok = false;
 };
 
+// The current device's SM count and shared-memory limit; a failing query is recorded for
+// q4a_last_cuda_error (the caller returns Q4A_ERR_CUDA).
 DeviceInfo device_info() {
     int dev = 0;
     DeviceInfo d;
-    if (cudaGetDevice(&dev) != cudaSuccess) return d;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e);
+        return d;
+    }
     static DeviceInfo cache[64];
     if (dev < 64 && cache[dev].ok) return cache[dev];
-    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) {
+        cuda_fail(e);
+        return d;
+    }
     d.ok = d.sm_count > 0;
     if (dev < 64) cache[dev] = d;
     return d;
@@ -1218,8 +1305,8 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
 // One op of a launch from its description: the tensor maps of its codes (and 3-bit lowest
 // bits), of its scales and biases in the chosen fetch mode, and its shape and schedule.
 q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_mode, int sb_tiles, uint32_t sb_pitch) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return Q4A_ERR_UNSUPPORTED;
+    if (!encode_fn()) return Q4A_ERR_UNSUPPORTED;
+    auto enc = encode_tiled_cached;
     const int cb = L.code_bits;
     const int G = (int)(L.in_dim / kGroup);
     // packed codes: in_dim/2 bytes per row (nibbles) or in_dim/4 (2-bit codes; the 3-bit
@@ -1273,6 +1360,7 @@ q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_
     o.sb_pitch = sb_pitch;
     o.rms = L.rmsnorm ? 1 : 0;
     o.fg = L.fused_gate_up ? 1 : 0;
+    o.withhold_stage = L.withhold_stage;
     if (sb_mode == kSbTma) {
         const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
         const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
@@ -1389,7 +1477,9 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
     memset(&prm, 0, sizeof(prm));
-    q4a_status st = fill_op(prm.op, L, gs, mt_units, sbmode(C), mt, lay.sb_pitch);
+    GemvLaunch Lw = L;
+    Lw.withhold_stage = take_withhold_stage();
+    q4a_status st = fill_op(prm.op, Lw, gs, mt_units, sbmode(C), mt, lay.sb_pitch);
     if (st != Q4A_OK) return st;
     prm.cluster = C;
     prm.nseg = L.nseg;

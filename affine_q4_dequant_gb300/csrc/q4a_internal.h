@@ -23,7 +23,8 @@ constexpr int kDenseMaxSeg = 8;         // token chunks of one dense call
 constexpr int kXFragBudget = 128 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
-constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path
+constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path,
+constexpr int kDenseTcTallRows = 152 * 256;   // and from 17 rows on matrices this tall
 constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
 constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation segments per row
 
@@ -144,6 +145,7 @@ struct GemvOp {
     uint32_t sb_pitch;        // bytes from a row block's staged scales to its biases
     int32_t rms;              // RMSNorm prologue: x is fp32 x_raw (kernels built with RMS)
     int32_t fg;               // fused gate|up epilogue into h (kernels built with FG)
+    int32_t withhold_stage;   // failure-path testing: weight stage (per CTA) never loaded, -1 none
 };
 
 template <int MAXSEG>
@@ -185,6 +187,7 @@ struct GemvLaunch {
     const Segment* seg;
     int max_ntok;
     bool plan_only = false;               // validate and plan, launch nothing
+    int withhold_stage = -1;              // see GemvOp
 };
 
 q4a_status launch_gemv(const GemvLaunch& L, cudaStream_t stream);
@@ -204,12 +207,23 @@ q4a_status launch_moe_combine(float* out, const float* y, const int32_t* slot, c
 q4a_status read_and_clear_device_error(cudaStream_t stream, uint32_t* word);
 
 // Dense path for wide batches (q4a_dense_tc.cu): dequantise to binary16 tiles, tcgen05.mma.
-// Eligible when nb >= kDenseTcMinRows, in_dim % 512 == 0 and s, b are 16-byte aligned.
-bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t in_dim);
+// Eligible when in_dim % 512 == 0, s and b are 16-byte aligned, and nb >= kDenseTcMinRows (or
+// nb > 16 with out_dim >= kDenseTcTallRows).
+bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim);
 q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
                            int nb, int64_t out_dim, int64_t in_dim, bool silu, float silu_div,
                            cudaStream_t stream);
 q4a_status read_and_clear_dense_tc_error(uint32_t* word);   // after a stream synchronisation
+
+// cuTensorMapEncodeTiled with a cache keyed by every argument (q4a_gemv.cu).
+CUresult encode_tiled_cached(CUtensorMap* out, CUtensorMapDataType dtype, cuuint32_t rank, void* ptr,
+                             const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                             const cuuint32_t* estr, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                             CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob);
+
+// The stage q4a_debug_withhold_stage asked the next GEMV-kernel launch of this host thread to
+// withhold (-1: none); reading it clears it.
+int take_withhold_stage();
 
 // Records a CUDA error for q4a_last_cuda_error and returns Q4A_ERR_CUDA.
 q4a_status cuda_fail(cudaError_t e);

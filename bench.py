@@ -186,6 +186,25 @@ def oracle_sample(seconds_target: float = 12.0):
     return total_bytes / dt / 1e9, desc, 1
 
 
+def host_info():
+    """The host's logical core count and CPU model (the oracle uses one of the cores)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except Exception:
+        pass
+    if not model:
+        import platform
+
+        model = platform.processor() or platform.machine()
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -202,7 +221,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "nbs": [int(v) for v in args.nbs.split(",")]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
+                         **host_info()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -376,6 +396,11 @@ def run_ours(args, rank, world, local_rank):
                     "timing": "CUDA events around graph replays of back-to-back launches of one kind, "
                               "inside the timed region"}
 
+    # every workload of the set, per launch (rank 0 only; after the timed region)
+    configs = None
+    if rank == 0 and not args.no_per_config:
+        configs = per_config(q4a, torch)
+
     if rank != 0:
         return
     line = {
@@ -391,13 +416,15 @@ def run_ours(args, rank, world, local_rank):
         "per_nb": per_nb,
         "us_per_decode_layer": {k: v["layer_us"] for k, v in per_nb.items()},
         "roofline": roofline,
+        "per_config": configs,
         "e2e": e2e,
         "gpu_launches": args.steps * len(nbs) * L * 4,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
         gbs, desc, cores = oracle_sample(seconds_target=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
+                                **host_info()}
     print(json.dumps(line), flush=True)
 
 
@@ -429,21 +456,26 @@ KERNEL_SHAPES = {"gate_up": (INTER2, HIDDEN), "down": (DOWN_OUT, DOWN_IN), "lm_h
                  "small": (256, 512)}
 
 
-def run_kernel_mode(args):
-    """Per-launch time of one GEMV shape: a CUDA graph of back-to-back q4a_gemv calls
-    cycling through weight copies that total > 3 x L2 (every launch streams from HBM)."""
-    import torch
+def load_tc_peak():
+    """Dense bf16 tensor throughput (burst) from MEASURED_PEAKS.json, in TFLOP/s. The tensor-core
+    path runs f16 x f16 -> f32, whose dense rate equals bf16's."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
-    import affine_q4_dequant_gb300 as q4a
 
-    out_dim, in_dim = KERNEL_SHAPES[args.kernel]
+def time_dense(q4a, torch, out_dim, in_dim, nbs, bits=4, reps=60, profile=False):
+    """Per-launch time of q4a_gemv (or q4a_gemv_lowbit) on one shape: a CUDA graph of
+    back-to-back calls cycling through weight copies that total > 3 x L2, so that every launch
+    streams from HBM; median of 5 replays. One record per NB."""
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
-    wbytes = out_dim * in_dim * (args.bits / 8.0 + 4.0 / 64.0)
+    wbytes = out_dim * in_dim * (bits / 8.0 + 4.0 / 64.0)
     copies = max(2, int(3 * 130e6 // wbytes) + 1)
     ws = []
-    bits = args.bits
     for _ in range(copies):
         codes = torch.randint(0, 16, (out_dim, in_dim), dtype=torch.uint8, device=dev, generator=g)
         w4 = q4a.pack(codes)
@@ -454,7 +486,10 @@ def run_kernel_mode(args):
             del w4
         ws.append((wc, (torch.rand(out_dim, in_dim // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
                    (torch.randn(out_dim, in_dim // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
-    for nb in [int(v) for v in args.nbs.split(",")]:
+    peak, kind = load_peaks()
+    tc_peak, tc_kind = load_tc_peak()
+    out = []
+    for nb in nbs:
         x = torch.randn(nb, in_dim, device=dev, generator=g).half()
         y = torch.empty(nb, out_dim, device=dev)
 
@@ -468,37 +503,43 @@ def run_kernel_mode(args):
         for i in range(3):
             call(i)
         torch.cuda.synchronize()
-        if args.profile:
+        if profile:
             # plain launches for a profiler: no graph, no timing
-            for i in range(args.reps):
+            for i in range(reps):
                 call(3 + i)
             torch.cuda.synchronize()
-            print(json.dumps({"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
-                              "shape": f"{in_dim}->{out_dim}", "nb": nb, "profile_launches": args.reps + 3}), flush=True)
+            out.append({"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
+                        "shape": f"{in_dim}->{out_dim}", "nb": nb, "profile_launches": reps + 3})
             continue
-        n = copies * max(1, args.reps // copies)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(n):
-                call(i)
-        graph.replay()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(5):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            graph.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1) / n * 1e3)
-        us = statistics.median(times)
+        n = copies * max(1, reps // copies)
+        us = graph_us(torch, call, n)
         nbytes = gemv_bytes(out_dim, in_dim, nb, 2, bits)
-        peak, kind = load_peaks()
-        print(json.dumps({"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
-                          "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us,
-                          "gbs": nbytes / us / 1e3, "frac_of_peak": nbytes / us / 1e3 / peak, "peak": peak,
-                          "peak_kind": kind, "weights_per_s": out_dim * in_dim / (us * 1e-6),
-                          "launches_timed": n, "weight_copies": copies}), flush=True)
+        rec = {"kernel": "q4a_gemv" if bits == 4 else "q4a_gemv_lowbit", "bits": bits,
+               "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us, "gbs": nbytes / us / 1e3,
+               "weights_per_s": out_dim * in_dim / (us * 1e-6), "frac_of_peak": nbytes / us / 1e3 / peak,
+               "peak": peak, "peak_kind": kind, "launches_timed": n, "weight_copies": copies}
+        if bits == 4 and nb >= 64 and in_dim % 512 == 0:
+            # the tensor-core path: a contraction, bounded by max(bytes / HBM, flops / tensor peak)
+            tflops = 2.0 * out_dim * in_dim * nb / (us * 1e-6) / 1e12
+            bound_us = max(nbytes / (peak * 1e3), 2.0 * out_dim * in_dim * nb / (tc_peak * 1e12) * 1e6)
+            rec.update({"path": "tcgen05", "tflops": tflops, "tc_peak": tc_peak, "tc_peak_kind": tc_kind,
+                        "frac_of_tc_peak": tflops / tc_peak, "frac_of_bound": bound_us / us})
+        out.append(rec)
+    del ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_kernel_mode(args):
+    """Per-launch time of one GEMV shape (see time_dense)."""
+    import torch
+
+    import affine_q4_dequant_gb300 as q4a
+
+    out_dim, in_dim = KERNEL_SHAPES[args.kernel]
+    for rec in time_dense(q4a, torch, out_dim, in_dim, [int(v) for v in args.nbs.split(",")], args.bits, args.reps,
+                          args.profile):
+        print(json.dumps(rec), flush=True)
 
 
 def run_prefill_mode(args):
@@ -569,15 +610,11 @@ def graph_us(torch, fn, n, trials=5):
     return statistics.median(times)
 
 
-def run_moe_mode(args):
+def time_moe(q4a, torch, reps=60, profile=False):
     """One routed MoE layer on the 64-expert bank (hidden 2048, inter 640, 16 tokens,
     top-8 by N(0,1) logits): q4a_gemv_experts on gate|up with the token map, the
     SiLU*up activation, q4a_gemv_experts on down, and q4a_moe_combine back to one row per
     token (no shared expert in this workload). Bank replicas total > 3 x L2."""
-    import torch
-
-    import affine_q4_dequant_gb300 as q4a
-
     E, H, I, T = wl.MOE_EXPERTS, wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_TOKENS
     r = wl.route_by_logits(wl.moe_logits(), wl.MOE_TOP_K)
     U, slots = int(r.expert_ids.shape[0]), int(r.token_offsets[-1])
@@ -627,14 +664,13 @@ def run_moe_mode(args):
     for i in range(3):
         layer(i)
     torch.cuda.synchronize()
-    if args.profile:
-        for i in range(args.reps):
+    if profile:
+        for i in range(reps):
             layer(3 + i)
         torch.cuda.synchronize()
         q4a.check_device_error()
-        print(json.dumps({"kernel": "moe_layer", "profile_layers": args.reps + 3}), flush=True)
-        return
-    n = copies * max(1, args.reps // copies)
+        return {"kernel": "moe_layer", "profile_layers": reps + 3}
+    n = copies * max(1, reps // copies)
     us = {k: graph_us(torch, fn, n) for k, fn in (("gate_up", gate_up), ("act", act), ("down", down),
                                                    ("combine", combine), ("layer", layer))}
     q4a.check_device_error()
@@ -643,16 +679,51 @@ def run_moe_mode(args):
     dn_b = U * H * I * BYTES_PER_WEIGHT + slots * I * 2 + slots * H * 4
     cb_b = slots * H * 4 + T * H * 4 + slots * 8
     peak, kind = load_peaks()
-    print(json.dumps({
+    del banks
+    torch.cuda.empty_cache()
+    layer_b = gu_b + act_b + dn_b + cb_b
+    return {
         "kernel": "moe_layer", "experts": E, "union_experts": U, "slots": slots,
         "touched_weight_bytes": U * per_expert, "us_per_moe_layer": us["layer"],
+        "weights_per_s": U * 3 * I * H / (us["layer"] * 1e-6),
         "gate_up_us": us["gate_up"], "gate_up_gbs": gu_b / us["gate_up"] / 1e3,
         "act_us": us["act"], "down_us": us["down"], "down_gbs": dn_b / us["down"] / 1e3,
         "combine_us": us["combine"], "combine_gbs": cb_b / us["combine"] / 1e3,
-        "layer_gbs": (gu_b + act_b + dn_b + cb_b) / us["layer"] / 1e3,
+        "layer_gbs": layer_b / us["layer"] / 1e3, "frac_of_peak": layer_b / us["layer"] / 1e3 / peak,
         "frac_of_peak_gate_up": gu_b / us["gate_up"] / 1e3 / peak,
         "frac_of_peak_down": dn_b / us["down"] / 1e3 / peak, "peak": peak, "peak_kind": kind,
-        "launches_timed": n, "bank_copies": copies}), flush=True)
+        "launches_timed": n, "bank_copies": copies}
+
+
+def run_moe_mode(args):
+    import torch
+
+    import affine_q4_dequant_gb300 as q4a
+
+    print(json.dumps(time_moe(q4a, torch, args.reps, args.profile)), flush=True)
+
+
+def per_config(q4a, torch, reps=40):
+    """Every workload of the benchmark set, timed per launch on this GPU: the 256 x 512 GEMV,
+    the 4096 -> 12288 projection (plain, and fused with the RMSNorm prologue and the
+    silu(gate)*up epilogue), the 12288 -> 4096 down projection, the routed MoE layer and the
+    151936-row LM head (NB >= 64 on the tensor-core path)."""
+    def brief(recs):
+        keep = ("nb", "us_per_call", "gbs", "weights_per_s", "frac_of_peak", "path", "tflops", "frac_of_tc_peak",
+                "frac_of_bound")
+        return [{k: r[k] for k in keep if k in r} for r in recs]
+
+    out = {
+        "gemv_256x512": brief(time_dense(q4a, torch, 256, 512, [1], reps=reps)),
+        "gate_up_4096x12288": brief(time_dense(q4a, torch, INTER2, HIDDEN, [1, 2, 4, 8, 16], reps=reps)),
+        "down_12288x4096": brief(time_dense(q4a, torch, DOWN_OUT, DOWN_IN, [1, 4, 16], reps=reps)),
+        "lm_head_4096x151936": brief(time_dense(q4a, torch, 151936, HIDDEN, [1, 8, 32, 64, 128], reps=reps)),
+    }
+    moe = time_moe(q4a, torch, reps=reps)
+    out["moe_layer_64x2048x640"] = {k: moe[k] for k in ("union_experts", "slots", "us_per_moe_layer", "layer_gbs",
+                                                         "weights_per_s", "frac_of_peak", "gate_up_us", "down_us",
+                                                         "act_us", "combine_us")}
+    return out
 
 
 def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
@@ -692,9 +763,26 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
         one(k)
     dt = (time.perf_counter() - t0) / steps
     step_bytes = sum(sum(layer_bytes(nb)) for nb in nbs)
+    # host cost of one call through the binding (argument checks, marshalling, the C ABI's
+    # validation, planning and launch): back-to-back calls on a small product, no sync between
+    ly = layers[0]
+    w, s, b = ly["dn"]
+    x1 = torch.zeros((1, DOWN_IN), dtype=torch.float16, device=dev)
+    y1 = torch.empty((1, DOWN_OUT), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            q4a.gemv(w, s, b, x1, out=y1, stream=stream)
+        stream.synchronize()
+        n_calls = 200
+        h0 = time.perf_counter()
+        for _ in range(n_calls):
+            q4a.gemv(w, s, b, x1, out=y1, stream=stream)
+        host_us = (time.perf_counter() - h0) / n_calls * 1e6
+        stream.synchronize()
     return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
-            "note": "one decode-layer MLP per NB per step, eager launches through the Python binding"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "host_us_per_call": host_us,
+            "note": "one decode-layer MLP per NB per step, eager launches through the Python binding; "
+                    "host_us_per_call: wall time of one q4a.gemv call on the host (launch included)"}
 
 
 def main():
@@ -707,13 +795,16 @@ def main():
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload launch timings")
     ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe", "prefill"], default=None,
                     help="time one GEMV shape per launch instead of the decode-layer step")
     ap.add_argument("--reps", type=int, default=60)
     ap.add_argument("--bits", type=int, choices=[4, 3, 2], default=4,
                     help="with --kernel: code width (3 and 2: derived low-bit codes, q4a_gemv_lowbit)")
-    ap.add_argument("--layer-mode", choices=["decode_mlp", "separate"], default="decode_mlp",
-                    help="the decode layer as one q4a_decode_mlp call, or as the two GEMV calls")
+    ap.add_argument("--layer-mode", choices=["decode_mlp", "separate"], default="separate",
+                    help="separate: the 4096 -> 2 x 6144 fused gate|up and the 12288 -> 4096 down projection "
+                         "(both workloads of the set); decode_mlp: q4a_decode_mlp with its matching "
+                         "6144 -> 4096 down projection")
     ap.add_argument("--profile", action="store_true",
                     help="with --kernel: eager launches only (a target for ncu), no timing")
     args = ap.parse_args()

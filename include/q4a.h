@@ -100,7 +100,10 @@ Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_d
  *   x        in   fp16 [nb][in_dim]
  *   Requires nb >= 1, out_dim >= 1 (any value, odd included), in_dim >= 64,
  *   in_dim % 64 == 0; w and x 16-byte aligned; s and b 2-byte aligned.
- *   The GEMV kernel (NB < 64, or rows not eligible for the tensor-core path) keeps a CTA's
+ *   Kernel choice: the tensor-core path (weights dequantised into TMEM, tcgen05.mma) takes
+ *   nb >= 64, and nb >= 17 when out_dim >= 38912 (enough 256-row units for every SM), provided
+ *   in_dim % 512 == 0 and s, b are 16-byte aligned; everything else runs the GEMV kernel.
+ *   The GEMV kernel keeps a CTA's
  *   K-slice of the activations and of the row block's scales and biases in shared memory:
  *   rows longer than that budget allows, even split across 8 CTAs, return
  *   Q4A_ERR_UNSUPPORTED before any launch. Every in_dim up to 98304 runs at NB 1, up to
@@ -229,7 +232,7 @@ Q4A_API q4a_status q4a_gemv_lowbit(float* y, int bits, const uint8_t* w_up, cons
  * ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b: the gated-residual bottleneck):
  *     y[r][o] = v / (1 + e^-v),  v = (W.x)[r][o] / div
  *   div  finite and nonzero (else Q4A_ERR_SHAPE); all other arguments, layouts, kernel
- *   choice (NB >= 64 takes the tensor-core path) and errors as q4a_gemv.
+ *   choice and errors as q4a_gemv.
  */
 Q4A_API q4a_status q4a_gemv_silu(float* y, const uint8_t* w, const uint16_t* s, const uint16_t* b,
                          const uint16_t* x, float div, int nb, int64_t out_dim, int64_t in_dim,
@@ -348,6 +351,17 @@ Q4A_API q4a_status q4a_moe_combine(float* out, const float* y, const int32_t* sl
                            int n_tok, int top_k, int64_t n_slots, int64_t hidden,
                            const float* y_shared, const uint16_t* gate, const float* x,
                            q4a_stream_t stream);
+
+/*
+ * q4a_debug_withhold_stage -- a hook for testing the failure path: the next launch of the
+ * GEMV kernel made from this host thread (any q4a_gemv* entry point whose work runs there;
+ * not the tensor-core path) never loads weight stage `stage` of each CTA (counted from 0), so
+ * its consumer warps give up their bounded wait on it after about a second, finish the launch
+ * with garbage outputs, and q4a_check_device_error then reports Q4A_ERR_TIMEOUT. The kernel
+ * issues no copy after the give-up and waits for the copies it already issued before it
+ * exits. stage = -1 clears a pending request. Returns Q4A_ERR_SHAPE for stage < -1.
+ */
+Q4A_API q4a_status q4a_debug_withhold_stage(int stage);
 
 /*
  * q4a_check_device_error -- synchronise `stream`, then report and clear the

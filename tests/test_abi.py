@@ -45,6 +45,9 @@ def lib():
     lib.q4a_gemv_rmsnorm_gate_up_silu.argtypes = [P, P, P, P, P, P, F, F, I32, I64, I64, P]
     lib.q4a_decode_mlp.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_inject_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
+    lib.q4a_debug_withhold_stage.argtypes = [I32]
+    lib.q4a_check_device_error.argtypes = [P]
+    lib.q4a_last_cuda_error.restype = I32
     return lib
 
 
@@ -368,3 +371,31 @@ def test_binding_checks_expert_and_helper_shapes(q4a):
                                  x=torch.zeros(3, 8, dtype=f32)), "gate: shape")
     _bad(lambda: mod.gemv_lowbit(3, torch.zeros(16, 128, dtype=u8), torch.zeros(16, 63, dtype=u8),
                                  torch.zeros(16, 8, dtype=bf), torch.zeros(16, 8, dtype=bf), x[:2]), "w_lo: shape")
+
+
+def _has_gpu():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def test_cuda_failure_is_reported(lib):
+    """A valid call on a machine with no usable CUDA device reaches the runtime, which fails:
+    the call returns Q4A_ERR_CUDA and q4a_last_cuda_error holds the runtime's error code (the
+    launchers' error path, made to fail on the host; no GPU is faulted)."""
+    if _has_gpu():
+        pytest.skip("a CUDA device is present: the runtime does not fail here")
+    A = 0x1000
+    assert lib.q4a_gemv(A, A, A, A, A, 1, 64, 512, None) == CUDA
+    assert lib.q4a_last_cuda_error() != 0
+    assert b"CUDA" in lib.q4a_status_string(CUDA)
+    assert lib.q4a_check_device_error(None) == CUDA
+
+
+def test_withhold_stage_hook_arguments(lib):
+    assert lib.q4a_debug_withhold_stage(-2) == SHAPE
+    assert lib.q4a_debug_withhold_stage(3) == OK
+    assert lib.q4a_debug_withhold_stage(-1) == OK     # clears the request
