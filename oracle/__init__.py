@@ -65,6 +65,7 @@ def _load():
             "q4o_lowbit_pack3lo": (None, [P, P, I, I]),
             "q4o_lowbit_codes": (None, [P, P, P, I, I]),
             "q4o_gemv_lowbit": (None, [P, P, P, P, P, P, P, I, I, I]),
+            "q4o_experts_lowbit": (None, [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I]),
             "q4o_gemv_f32x": (None, [P, P, P, P, P, P, I, I, I]),
             "q4o_quantize": (None, [P, P, P, P, I, I]),
         }
@@ -324,6 +325,27 @@ def gemv_lowbit(w2, wlo, s, b, x_bits):
     y = np.empty((nb, out_dim), np.float64)
     bound = np.empty((nb, out_dim), np.float64)
     _load().q4o_gemv_lowbit(_p(y), _p(bound), _p(w2), _p(wlo), _p(s), _p(b), _p(x_bits), nb, out_dim, in_dim)
+    return y, bound
+
+
+def experts_lowbit(w2_bank, wlo_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n_experts: int,
+                   out_dim: int):
+    """Routed low-bit experts ([BATCH_MSL] expert_gemm.metal fn_expert_qmm; the routed form of
+    fn_q2_rows_h / fn_q3_rows_h): 2-bit codes (wlo_bank None) or 3-bit codes, activations fp32
+    (a float32 array) or binary16 bits (a uint16 array). Returns (y, bound) in float64."""
+    w2_bank, s_bank, b_bank = _c(w2_bank, np.uint8), _c(s_bank, np.uint16), _c(b_bank, np.uint16)
+    wlo_bank = None if wlo_bank is None else _c(wlo_bank, np.uint8)
+    x32 = _c(x, np.float32) if np.asarray(x).dtype == np.float32 else None
+    x16 = None if x32 is not None else _c(x, np.uint16)
+    expert_ids, token_offsets = _c(expert_ids, np.int32), _c(token_offsets, np.int32)
+    xr = None if x_rows is None else _c(x_rows, np.int32)
+    in_dim = (x32 if x32 is not None else x16).shape[1]
+    n_rows = int(token_offsets[-1])
+    y = np.empty((n_rows, out_dim), np.float64)
+    bound = np.empty((n_rows, out_dim), np.float64)
+    _load().q4o_experts_lowbit(_p(y), _p(bound), _p(w2_bank), _p(wlo_bank), _p(s_bank), _p(b_bank), _p(x32), _p(x16),
+                               _p(xr), _p(expert_ids), _p(token_offsets), expert_ids.shape[0], n_experts, out_dim,
+                               in_dim)
     return y, bound
 
 

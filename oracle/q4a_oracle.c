@@ -636,6 +636,60 @@ Q4O_EXPORT void q4o_gemv_lowbit(double* y, double* bound, const uint8_t* w2, con
     free(w);
 }
 
+/* [BATCH_MSL] expert_gemm.metal fn_expert_qmm (prefill: 8/16/32-token tiles of fp32
+ * activations) and the routed form of fn_q2_rows_h / fn_q3_rows_h (decode): the low-bit codes
+ * of a routed-expert bank. For segment a (expert e = expert_ids[a], slot rows token_offsets[a]
+ * .. token_offsets[a+1]-1), y[r][o] = sum_i W_e[o][i] * x[src][i] with src = x_rows ? x_rows[r]
+ * : r and the quad or pair midpoint W = s (4 q2 + 1.5) + b (bits 2; wlo_bank NULL) or
+ * W = s (2 q3 + 0.5) + b (bits 3), every step in double; x is fp32 (x32) or binary16 (x16),
+ * taken as given. An expert id outside [0, n_experts) gives NaN rows; bound as q4o_gemv. */
+Q4O_EXPORT void q4o_experts_lowbit(double* y, double* bound, const uint8_t* w2_bank, const uint8_t* wlo_bank,
+                                   const uint16_t* s_bank, const uint16_t* b_bank, const float* x32,
+                                   const uint16_t* x16, const int32_t* x_rows, const int32_t* expert_ids,
+                                   const int32_t* token_offsets, int64_t n_active, int64_t n_experts,
+                                   int64_t out_dim, int64_t in_dim)
+{
+    const int64_t groups = in_dim / 64;
+    double* w = (double*)malloc((size_t)in_dim * sizeof(double));
+    for (int64_t a = 0; a < n_active; a++) {
+        const int64_t e = expert_ids[a];
+        if (e < 0 || e >= n_experts) {
+            for (int64_t r = token_offsets[a]; r < token_offsets[a + 1]; r++)
+                for (int64_t o = 0; o < out_dim; o++) {
+                    y[r * out_dim + o] = NAN;
+                    if (bound)
+                        bound[r * out_dim + o] = NAN;
+                }
+            continue;
+        }
+        for (int64_t o = 0; o < out_dim; o++) {
+            const int64_t row = e * out_dim + o;
+            const uint8_t* w2row = w2_bank + row * (in_dim / 4);
+            const uint8_t* wlorow = wlo_bank ? wlo_bank + row * (in_dim / 8) : NULL;
+            for (int64_t i = 0; i < in_dim; i++) {
+                const double sv = bf16_value(s_bank[row * groups + i / 64]);
+                const double bv = bf16_value(b_bank[row * groups + i / 64]);
+                const double q = (double)lowbit_code_at(w2row, wlorow, i);
+                w[i] = wlorow ? sv * (2.0 * q + 0.5) + bv : sv * (4.0 * q + 1.5) + bv;
+            }
+            for (int64_t r = token_offsets[a]; r < token_offsets[a + 1]; r++) {
+                const int64_t src = x_rows ? x_rows[r] : r;
+                double acc = 0.0, mag = 0.0;
+                for (int64_t i = 0; i < in_dim; i++) {
+                    const double xv = x32 ? (double)x32[src * in_dim + i] : half_value(x16[src * in_dim + i]);
+                    const double p = w[i] * xv;
+                    acc += p;
+                    mag += fabs(p);
+                }
+                y[r * out_dim + o] = acc;
+                if (bound)
+                    bound[r * out_dim + o] = 2e-3 * mag + 1e-5;
+            }
+        }
+    }
+    free(w);
+}
+
 /* ---- prefill helpers ---------------------------------------------------------------- */
 
 /* [BATCH_MSL] fn_qmv_small_b: the projection straight from fp32 activations (few output

@@ -642,6 +642,77 @@ def test_lowbit_gemv_brute_force_tiny():
         assert np.all(bound > 0)
 
 
+def _lowbit_bank(seed, n_exp, out_dim, in_dim):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(n_exp * out_dim, in_dim), dtype=np.uint8)
+    s = wl.f32_to_bf16_bits(np.abs(rng.normal(0, 0.02, (n_exp * out_dim, in_dim // 64))).astype(np.float32))
+    b = wl.f32_to_bf16_bits((-8 * rng.normal(0, 0.01, (n_exp * out_dim, in_dim // 64))).astype(np.float32))
+    return codes, s, b
+
+
+def test_experts_lowbit_equal_the_dense_lowbit_product_per_expert():
+    """Routed low-bit experts (fn_expert_qmm's contraction, routed) reduce to the pinned dense
+    low-bit product of each expert's matrix over its rows (identical arithmetic), for 2- and
+    3-bit codes, with a token map, an empty segment and a repeated expert."""
+    n_exp, out_dim, in_dim = 3, 5, 128
+    codes, s, b = _lowbit_bank(71, n_exp, out_dim, in_dim)
+    x = wl.f16_bits(np.random.default_rng(72).normal(0, 1, (4, in_dim)))
+    ids = np.array([2, 0, 1, 2], np.int32)
+    offs = np.array([0, 2, 2, 5, 6], np.int32)
+    x_rows = np.array([3, 0, 1, 1, 2, 0], np.int32)
+    for bits in (2, 3):
+        w2 = oracle.lowbit_pack2(codes)
+        lo = oracle.lowbit_pack3lo(codes) if bits == 3 else None
+        y, bound = oracle.experts_lowbit(w2, lo, s, b, x, x_rows, ids, offs, n_exp, out_dim)
+        for a, e in enumerate(ids):
+            rows = slice(e * out_dim, (e + 1) * out_dim)
+            r0, r1 = offs[a], offs[a + 1]
+            if r0 == r1:
+                continue
+            ref, rb = oracle.gemv_lowbit(w2[rows], None if lo is None else lo[rows], s[rows], b[rows],
+                                         x[x_rows[r0:r1]])
+            assert np.array_equal(y[r0:r1], ref) and np.array_equal(bound[r0:r1], rb), (bits, a)
+
+
+def test_experts_lowbit_fp32_activations_as_given():
+    """fp32 activations that binary16 represents exactly give the same products as their
+    binary16 bits; values binary16 cannot hold enter exactly (checked against numpy)."""
+    n_exp, out_dim, in_dim = 2, 4, 192
+    codes, s, b = _lowbit_bank(73, n_exp, out_dim, in_dim)
+    xh = wl.f16_bits(np.random.default_rng(74).normal(0, 1, (3, in_dim)))
+    x32 = xh.view(np.float16).astype(np.float32)
+    ids, offs = np.array([1, 0], np.int32), np.array([0, 1, 3], np.int32)
+    w2, lo = oracle.lowbit_pack2(codes), oracle.lowbit_pack3lo(codes)
+    for low in (None, lo):
+        a, _ = oracle.experts_lowbit(w2, low, s, b, x32, None, ids, offs, n_exp, out_dim)
+        h, _ = oracle.experts_lowbit(w2, low, s, b, xh, None, ids, offs, n_exp, out_dim)
+        assert np.array_equal(a, h)
+    xf = (np.random.default_rng(75).normal(0, 1, (3, in_dim)) * 1.000001).astype(np.float32)
+    y, _ = oracle.experts_lowbit(w2, None, s, b, xf, None, ids, offs, n_exp, out_dim)
+    q2 = oracle.lowbit_codes(w2).astype(np.float64)
+    sf = np.repeat(wl.bf16_bits_to_f32(s).astype(np.float64), 64, axis=1)
+    bf = np.repeat(wl.bf16_bits_to_f32(b).astype(np.float64), 64, axis=1)
+    w = sf * (4.0 * q2 + 1.5) + bf
+    ref = np.vstack([xf[0:1].astype(np.float64) @ w[4:8].T, xf[1:3].astype(np.float64) @ w[0:4].T])
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_experts_lowbit_brute_force_and_invalid_id():
+    n_exp, out_dim, in_dim = 2, 2, 64
+    codes, s, b = _lowbit_bank(76, n_exp, out_dim, in_dim)
+    xf = np.random.default_rng(77).normal(0, 1, (2, in_dim)).astype(np.float32)
+    sf, bfv = wl.bf16_bits_to_f32(s).astype(float), wl.bf16_bits_to_f32(b).astype(float)
+    w2, lo = oracle.lowbit_pack2(codes), oracle.lowbit_pack3lo(codes)
+    ids, offs = np.array([1, 5], np.int32), np.array([0, 1, 2], np.int32)   # expert 5 does not exist
+    y, bound = oracle.experts_lowbit(w2, lo, s, b, xf, None, ids, offs, n_exp, out_dim)
+    for o in range(out_dim):
+        row = out_dim + o
+        acc = sum(((2 * (int(codes[row, i]) >> 1) + 0.5) * sf[row, 0] + bfv[row, 0]) * float(xf[0, i])
+                  for i in range(in_dim))
+        assert abs(y[0, o] - acc) <= 1e-12 * (1 + abs(acc))
+    assert np.all(np.isnan(y[1])) and np.all(np.isnan(bound[1]))
+
+
 # ---- prefill helpers ([BATCH_MSL] fn_qmv_small_b; the min/max quantiser) -------------------
 
 
