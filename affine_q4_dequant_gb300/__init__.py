@@ -25,7 +25,8 @@ import torch
 from . import _build
 
 __all__ = [
-    "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_rmsnorm",
+    "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_experts_lowbit",
+    "gemv_rmsnorm",
     "gemv_rmsnorm_grouped", "gemv_inject_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "decode_mlp", "lowbit_pack",
     "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error", "debug_withhold_stage",
     "STATUS", "MAX_SEGMENTS",
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "q4a_decode_mlp": (I32, [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
+        "q4a_gemv_experts_lowbit": (I32, [P, I32, P, P, P, P, P, I32, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_grouped": (I32, [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
         "q4a_gemv_inject_rmsnorm_grouped": (I32, [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
@@ -370,6 +372,35 @@ def gemv_experts(w_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n
     _check("q4a_gemv_experts", _lib.q4a_gemv_experts(
         py, pw, ps, pb, px, pr, ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
         int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim), int(in_dim), _stream(stream)))
+    return out
+
+
+def gemv_experts_lowbit(bits: int, w_up_bank, w_lo_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets,
+                        n_experts: int, out_dim: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Routed experts with derived 2-bit (w_lo_bank unused) or 3-bit codes; x is a float16 or
+    float32 CUDA tensor (fp32 rows are rounded to binary16 when staged). expert_ids and
+    token_offsets are HOST int32 arrays; x_rows a CUDA int32 tensor or None."""
+    expert_ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    token_offsets = np.ascontiguousarray(token_offsets, dtype=np.int32)
+    if token_offsets.ndim != 1 or expert_ids.ndim != 1 or token_offsets.shape[0] != expert_ids.shape[0] + 1:
+        raise ValueError("token_offsets must have one entry more than expert_ids")
+    n_rows = int(token_offsets[-1])
+    x_n, in_dim = _dims(x, "x")
+    rows = int(n_experts) * int(out_dim)
+    out = _empty((max(n_rows, 0), out_dim), torch.float32, x) if out is None else out
+    if x_rows is None and x_n < n_rows:
+        raise ValueError(f"x has {x_n} rows; without x_rows it needs token_offsets[-1] = {n_rows}")
+    f32 = isinstance(x, torch.Tensor) and x.dtype == torch.float32
+    lo = None if (w_lo_bank is None or bits == 2) else (w_lo_bank, "w_lo_bank", _U8, (rows, in_dim // 8))
+    xr = None if x_rows is None else (x_rows, "x_rows", _I32, (n_rows,))
+    py, pw, ps, pb, pl, px, pr = _ptrs(
+        (out, "y", _F32, (n_rows, out_dim)),
+        *_mat(w_up_bank, s_bank, b_bank, rows, in_dim, "w_up_bank", "s_bank", "b_bank", code_cols=in_dim // 4), lo,
+        (x, "x", _F32 if f32 else _F16, None), xr)
+    _check("q4a_gemv_experts_lowbit", _lib.q4a_gemv_experts_lowbit(
+        py, int(bits), pw, pl, ps, pb, px, 1 if f32 else 0, pr, ctypes.c_void_p(expert_ids.ctypes.data),
+        ctypes.c_void_p(token_offsets.ctypes.data), int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim),
+        int(in_dim), _stream(stream)))
     return out
 
 

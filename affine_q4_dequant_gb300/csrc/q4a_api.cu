@@ -418,19 +418,26 @@ q4a_status q4a_gemv_rmsnorm(float* y, const uint8_t* w, const uint16_t* s, const
     return q4a_gemv_rmsnorm_grouped(y, w, s, b, x_raw, norm_w, eps, shift, 1, nb, out_dim, in_dim, stream);
 }
 
-q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_bank,
-                            const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
-                            const int32_t* expert_ids, const int32_t* token_offsets, int n_active,
-                            int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
-                            q4a_stream_t stream) {
-    if (!y || !w_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets) return Q4A_ERR_NULL;
+}  // extern "C"
+
+namespace q4a {
+namespace {
+
+// The routed-expert schedule shared by the 4-bit and the low-bit entry points: host checks of
+// the segment table, NaN rows for out-of-range expert ids, one launch over every segment.
+q4a_status experts_common(float* y, const uint8_t* w_bank, const uint8_t* w_lo_bank, int code_bits,
+                          const uint16_t* s_bank, const uint16_t* b_bank, const void* x, bool x_f32,
+                          const int32_t* x_rows, const int32_t* expert_ids, const int32_t* token_offsets,
+                          int n_active, int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
+                          cudaStream_t stream) {
     if (n_active < 1 || n_active > Q4A_MAX_SEGMENTS || n_experts < 1 || n_rows < 1) return Q4A_ERR_SHAPE;
     q4a_status st = check_matrix_shape(out_dim, in_dim);
     if (st != Q4A_OK) return st;
+    if (code_bits == 3 && in_dim % 128 != 0) return Q4A_ERR_SHAPE;   // lowest-bit rows: 16-byte multiples
     if ((int64_t)n_experts * out_dim > ((int64_t)1 << 31) - 16) return Q4A_ERR_UNSUPPORTED;
     if (n_rows > ((int64_t)1 << 31) - 1) return Q4A_ERR_UNSUPPORTED;
-    if (!aligned(w_bank, 16) || !aligned(x, 16) || !aligned(s_bank, 2) || !aligned(b_bank, 2) ||
-        !aligned(y, 4) || (x_rows && !aligned(x_rows, 4)))
+    if (!aligned(w_bank, 16) || (w_lo_bank && !aligned(w_lo_bank, 16)) || !aligned(x, 16) || !aligned(s_bank, 2) ||
+        !aligned(b_bank, 2) || !aligned(y, 4) || (x_rows && !aligned(x_rows, 4)))
         return Q4A_ERR_ALIGN;
     if (token_offsets[0] != 0 || token_offsets[n_active] != n_rows) return Q4A_ERR_SHAPE;
     for (int a = 0; a < n_active; ++a)
@@ -449,20 +456,17 @@ q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_b
         push_segments(segs, (int32_t)((int64_t)e * out_dim), token_offsets[a], n);
     }
     if ((int)segs.size() > Q4A_MAX_SEGMENTS) return Q4A_ERR_UNSUPPORTED;
-    for (int a : bad) {
-        st = launch_fill_nan(y, token_offsets[a], token_offsets[a + 1] - token_offsets[a], out_dim,
-                             (cudaStream_t)stream);
-        if (st != Q4A_OK) return st;
-    }
-    if (segs.empty()) return Q4A_OK;
     int max_ntok = 0;
     for (const Segment& sg : segs) max_ntok = sg.ntok > max_ntok ? sg.ntok : max_ntok;
     GemvLaunch L = {};
     L.w = w_bank;
+    L.w_lo = code_bits == 3 ? w_lo_bank : nullptr;
+    L.code_bits = code_bits;
     L.tensor_rows = (int64_t)n_experts * out_dim;
     L.s = s_bank;
     L.b = b_bank;
     L.x = x;
+    L.x_f32 = x_f32;
     L.x_rows = x_rows;
     L.y = y;
     L.out_dim = out_dim;
@@ -471,7 +475,46 @@ q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_b
     L.nseg = (int)segs.size();
     L.seg = segs.data();
     L.max_ntok = max_ntok;
-    return launch_gemv(L, (cudaStream_t)stream);
+    if (!segs.empty()) {   // plan before the first launch: a rejected call launches nothing
+        L.plan_only = true;
+        st = launch_gemv(L, stream);
+        if (st != Q4A_OK) return st;
+        L.plan_only = false;
+    }
+    for (int a : bad) {
+        st = launch_fill_nan(y, token_offsets[a], token_offsets[a + 1] - token_offsets[a], out_dim, stream);
+        if (st != Q4A_OK) return st;
+    }
+    if (segs.empty()) return Q4A_OK;
+    return launch_gemv(L, stream);
+}
+
+}  // namespace
+}  // namespace q4a
+
+extern "C" {
+
+q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_bank,
+                            const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
+                            const int32_t* expert_ids, const int32_t* token_offsets, int n_active,
+                            int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
+                            q4a_stream_t stream) {
+    if (!y || !w_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets) return Q4A_ERR_NULL;
+    return experts_common(y, w_bank, nullptr, 4, s_bank, b_bank, x, false, x_rows, expert_ids, token_offsets,
+                          n_active, n_experts, n_rows, out_dim, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_experts_lowbit(float* y, int bits, const uint8_t* w_up_bank, const uint8_t* w_lo_bank,
+                                   const uint16_t* s_bank, const uint16_t* b_bank, const void* x, int x_is_f32,
+                                   const int32_t* x_rows, const int32_t* expert_ids, const int32_t* token_offsets,
+                                   int n_active, int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
+                                   q4a_stream_t stream) {
+    if (bits != 2 && bits != 3) return Q4A_ERR_UNSUPPORTED;
+    if (!y || !w_up_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets || (bits == 3 && !w_lo_bank))
+        return Q4A_ERR_NULL;
+    return experts_common(y, w_up_bank, bits == 3 ? w_lo_bank : nullptr, bits, s_bank, b_bank, x, x_is_f32 != 0,
+                          x_rows, expert_ids, token_offsets, n_active, n_experts, n_rows, out_dim, in_dim,
+                          (cudaStream_t)stream);
 }
 
 q4a_status q4a_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, int64_t rows,

@@ -181,13 +181,16 @@ __device__ __forceinline__ float inject_weight(const P& p, int64_t slot, int g) 
 // step j with the inputs whose codes sit in bit field j of the word's bytes: the even inputs
 // 16t + {0,2,4,6} (j = 0) and 16t + {8,10,12,14} (j = 1), the odd ones after them (j = 2, 3);
 // field j is read in place (value 4^j * code), so step j's activations are scaled by 4^-j.
-template <int NT, bool RMS, int CB, class P>
+// XF: the activations are fp32 (prefill); staging rounds them to binary16, the operand type of
+// the mma, as the pages' prefill contraction does (it rounds its fp32 rows to half).
+template <int NT, bool RMS, int CB, bool XF, class P>
 __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                           float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     static_assert(CB == 4 || !RMS, "the RMSNorm prologue is built for 4-bit codes only");
+    static_assert(!(RMS && XF), "the RMSNorm prologue reads fp32 rows itself");
     constexpr int NTOK = NT * 8;
     constexpr int BATCH = RMS ? 2 : 4;
-    constexpr int NLD = RMS ? 10 : 2;   // RMSNorm: x (4), norm weight (2), injected output (4)
+    constexpr int NLD = RMS ? 10 : (XF ? 4 : 2);   // RMSNorm: x (4), norm weight (2), injected output (4)
     constexpr int NTH = kConsumerWarps * 32;
     const int items = sg.ntok * gsz * 4;
     const int ntm = p.ntok_max;
@@ -209,7 +212,14 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
                 const int slot = sg.tok0 + tok;
                 const int64_t src = p.x_rows ? (int64_t)p.x_rows[slot] : (int64_t)slot;
                 const int64_t col = (int64_t)(kg0 + gl) * kGroup + (CB == 4 ? 8 : 16) * (i & 3);
-                if constexpr (!RMS) {
+                if constexpr (!RMS && XF) {
+                    // fp32: the item's two runs of 8 inputs, 16 bytes at a time
+                    const float* xr = static_cast<const float*>(p.x) + src * p.in_dim + col;
+                    ld[k][0] = ld_nc_16(xr);
+                    ld[k][1] = ld_nc_16(xr + 4);
+                    ld[k][2] = ld_nc_16(xr + (CB == 4 ? 32 : 8));
+                    ld[k][3] = ld_nc_16(xr + (CB == 4 ? 36 : 12));
+                } else if constexpr (!RMS) {
                     const __half* xr = static_cast<const __half*>(p.x) + src * p.in_dim + col;
                     ld[k][0] = ld_nc_16(xr);
                     ld[k][1] = ld_nc_16(xr + (CB == 4 ? 32 : 8));
@@ -243,7 +253,19 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
             const int gl = rest % gsz;
             const int tok = rest / gsz;
             uint32_t v[4], u[4];
-            if constexpr (!RMS) {
+            if constexpr (!RMS && XF) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint4 f0 = ld[k][2 * half], f1 = ld[k][2 * half + 1];
+                    const uint32_t xs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                    uint32_t* dst = half ? u : v;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        __half2 h = __floats2half2_rn(__uint_as_float(xs[2 * q]), __uint_as_float(xs[2 * q + 1]));
+                        dst[q] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                }
+            } else if constexpr (!RMS) {
                 v[0] = ld[k][0].x; v[1] = ld[k][0].y; v[2] = ld[k][0].z; v[3] = ld[k][0].w;
                 u[0] = ld[k][1].x; u[1] = ld[k][1].y; u[2] = ld[k][1].z; u[3] = ld[k][1].w;
             } else {
@@ -333,16 +355,16 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
 
 // Staging of one op's activations: the RMSNorm form when the op asks for it (kernels built
 // with RMS), the plain fp16 form otherwise.
-template <int NT, bool RMS, int CB, class P>
+template <int NT, bool RMS, int CB, bool XF, class P>
 __device__ __forceinline__ void stage_x(const P& p, bool rms, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                                         float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     if constexpr (RMS) {
         if (rms) {
-            stage_x_t<NT, true, CB>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, write_xnew);
+            stage_x_t<NT, true, CB, false>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, write_xnew);
             return;
         }
     }
-    stage_x_t<NT, false, CB>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, false);
+    stage_x_t<NT, false, CB, XF>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, false);
 }
 
 // B fragments of the bias term sum_g b[o][g] * xsum[r][g], an m16n8k16 contraction over
@@ -466,7 +488,7 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
 // MTT: tiles per row block (0: the default for NT). Rows that a short row block lacks still
 // cost their mma work (the tile loop is unrolled for a fixed tile count), so launches whose
 // clusters get only a few tiles use a kernel built for that many.
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> pp) {
     constexpr int NTOK = NT * 8;
@@ -773,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = pp.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS, CB>(p, rms, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
+                stage_x<NT, RMS, CB, XF>(p, rms, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
                                      rms && cid == 0 && p.x_new != nullptr);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
@@ -1190,9 +1212,9 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1269,9 +1291,9 @@ int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_
                    : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1285,7 +1307,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT, XF>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.op.n_tiles ? max_clusters : prm.op.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
@@ -1401,7 +1423,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     const int nt = L.max_ntok <= 8 ? 1 : (L.max_ntok <= 16 ? 2 : 4);
     int mt = tiles_per_block(nt);
     const int cb = L.code_bits;
-    if (cb != 4 && (L.experts || L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
+    if (cb != 4 && (L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
+    if (L.x_f32 && (!L.experts || cb == 4 || L.rmsnorm)) return Q4A_ERR_UNSUPPORTED;
     const bool fg = L.fused_gate_up;
     if (fg && (L.experts || cb != 4 || L.silu || L.out_dim % 16 != 0 || !L.h)) return Q4A_ERR_UNSUPPORTED;
     // schedule units per row block: tiles, or (fused) gate|up tile pairs
@@ -1513,6 +1536,29 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
             if (nt == 1) return launch_variant<1, true, MAXSEG>(prm, smem_bytes, stream);
             if (nt == 2) return launch_variant<2, true, MAXSEG>(prm, smem_bytes, stream);
             return launch_variant<4, true, MAXSEG>(prm, smem_bytes, stream);
+        }
+    }
+    if constexpr (MAXSEG != kDenseMaxSeg) {
+        // routed low-bit experts, binary16 or fp32 activations
+        if (cb == 2 && !L.x_f32) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 2>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 2>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 2>(prm, smem_bytes, stream);
+        }
+        if (cb == 3 && !L.x_f32) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 3>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 3>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 3>(prm, smem_bytes, stream);
+        }
+        if (cb == 2) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 2, false, 0, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 2, false, 0, true>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 2, false, 0, true>(prm, smem_bytes, stream);
+        }
+        if (cb == 3) {
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 3, false, 0, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 3, false, 0, true>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 3, false, 0, true>(prm, smem_bytes, stream);
         }
     }
     if constexpr (MAXSEG == kDenseMaxSeg) {

@@ -180,6 +180,7 @@ struct GemvLaunch {
     float* x_new = nullptr;
     bool fused_gate_up = false;   // w holds gate rows [0, out_dim) then up rows [out_dim, 2 out_dim);
     uint16_t* h = nullptr;        // the output is h = fp16(silu(gate) * up) [slots][out_dim]
+    bool x_f32 = false;       // the activations are fp32 (rounded to binary16 when staged)
     int code_bits = 4;        // 4 (w: packed nibbles), 2 or 3 (w: 2-bit codes [rows][in/4],
     const uint8_t* w_lo = nullptr;  // w_lo: the 3-bit codes' lowest-bit plane [rows][in/8])
     bool experts;

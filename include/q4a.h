@@ -266,6 +266,28 @@ Q4A_API q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint1
                             int64_t in_dim, q4a_stream_t stream);
 
 /*
+ * q4a_gemv_experts_lowbit -- q4a_gemv_experts over derived low-bit codes, on binary16 or fp32
+ * activations: the routed form of the 2/3-bit products ("BATCH_MSL", quantized_rows.metal
+ * fn_q2_rows_h / fn_q3_rows_h for decode rows; expert_gemm.metal fn_expert_qmm, the low-bit
+ * routed-expert contraction of prefill over 8/16/32-token tiles of fp32 rows). The weight of
+ * code q is the quad midpoint s (4 q + 1.5) + b (bits = 2) or the pair midpoint
+ * s (2 q + 0.5) + b (bits = 3, q = 2 * upper + lowest), as q4a_gemv_lowbit.
+ *   w_up_bank, w_lo_bank  in  the bank's codes as q4a_lowbit_pack writes them:
+ *                  [n_experts*out_dim][in_dim/4] and (bits 3) [n_experts*out_dim][in_dim/8]
+ *   x              in  [*][in_dim], binary16 (x_is_f32 = 0) or fp32 (x_is_f32 != 0); fp32 rows are
+ *                  rounded to binary16 when staged, as the pages' contraction rounds them to
+ *                  half (|x| must stay within the binary16 range)
+ *   everything else as q4a_gemv_experts (segments of up to 32 rows run as one tile, longer
+ *   ones in 32-row pieces). bits = 3 needs in_dim % 128 == 0; bits other than 2 or 3 return
+ *   Q4A_ERR_UNSUPPORTED.
+ */
+Q4A_API q4a_status q4a_gemv_experts_lowbit(float* y, int bits, const uint8_t* w_up_bank, const uint8_t* w_lo_bank,
+                                           const uint16_t* s_bank, const uint16_t* b_bank, const void* x,
+                                           int x_is_f32, const int32_t* x_rows, const int32_t* expert_ids,
+                                           const int32_t* token_offsets, int n_active, int n_experts,
+                                           int64_t n_rows, int64_t out_dim, int64_t in_dim, q4a_stream_t stream);
+
+/*
  * q4a_gemv_rmsnorm -- A3 + A4: RMSNorm prologue fused into the GEMV.
  *   x_raw   in  fp32 [nb][in_dim] un-normalised activations
  *   norm_w  in  bf16 [in_dim]

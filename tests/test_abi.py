@@ -46,6 +46,7 @@ def lib():
     lib.q4a_decode_mlp.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_inject_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     lib.q4a_debug_withhold_stage.argtypes = [I32]
+    lib.q4a_gemv_experts_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, P, P, P, I32, I32, I64, I64, I64, P]
     lib.q4a_check_device_error.argtypes = [P]
     lib.q4a_last_cuda_error.restype = I32
     return lib
@@ -399,3 +400,27 @@ def test_withhold_stage_hook_arguments(lib):
     assert lib.q4a_debug_withhold_stage(-2) == SHAPE
     assert lib.q4a_debug_withhold_stage(3) == OK
     assert lib.q4a_debug_withhold_stage(-1) == OK     # clears the request
+
+
+def test_experts_lowbit_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_gemv_experts_lowbit
+    ids = np.array([0, 1], np.int32)
+    offs = np.array([0, 2, 3], np.int32)
+    pi, po = ctypes.c_void_p(ids.ctypes.data), ctypes.c_void_p(offs.ctypes.data)
+
+    def call(y=A, bits=2, w=A, lo=None, s=A, b=A, x=A, f32=1, xr=None, ids_=pi, offs_=po, n_active=2, n_exp=4,
+             n_rows=3, out_dim=8, in_dim=128):
+        return f(y, bits, w, lo, s, b, x, f32, xr, ids_, offs_, n_active, n_exp, n_rows, out_dim, in_dim, None)
+
+    assert call(bits=4) == UNSUP
+    assert call(bits=3) == NULL                     # 3-bit codes need the lowest-bit plane
+    assert call(x=None) == NULL
+    assert call(ids_=None) == NULL
+    assert call(n_active=0) == SHAPE
+    assert call(n_rows=4) == SHAPE                  # offsets end != n_rows
+    assert call(bits=3, lo=A, in_dim=192) == SHAPE  # 3-bit: in_dim % 128
+    assert call(in_dim=100) == SHAPE
+    assert call(w=A + 4) == ALIGN
+    assert call(bits=3, lo=A + 8) == ALIGN
+    assert call(x=A + 8) == ALIGN
