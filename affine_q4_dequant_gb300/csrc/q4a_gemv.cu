@@ -477,6 +477,130 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
     }
 }
 
+// ---- the producer's once-per-row-block paths, out of line ------------------------------
+// A launch starts with a cold instruction cache, and a GEMV kernel carries code for several
+// scale/bias fetch modes of which one runs: keeping these paths out of line keeps the code a
+// launch actually fetches small (the stage loop and the consumers' mma loop stay inline).
+
+// Raw mode: 1D boxes over the contiguous [rows][groups] scales and biases of a row block into
+// a raw staging buffer. The first element is rounded down to a 16-byte boundary (TMA rule);
+// the consumers' transform skips the difference.
+__device__ __noinline__ void raw_issue(const GemvOp& p, const Segment& sgb, int tile, int ntile, uint8_t* dst,
+                                      uint32_t raw_elems, uint32_t bar) {
+    const int64_t r0 = (int64_t)sgb.row0 + (int64_t)tile * 16;
+    const int rv = (int)llmin((int64_t)ntile * 16, p.out_dim - (int64_t)tile * 16);
+    const int64_t e0 = r0 * p.groups;
+    const int64_t e0a = e0 & ~(int64_t)7;
+    const int nbx = (int)((e0 - e0a + (int64_t)rv * p.groups + kRawBox - 1) / kRawBox);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the last transform's reads
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbx * kRawBox * 2));
+#pragma unroll 1
+    for (int k = 0; k < nbx; ++k) {
+        tma_load_1d(smem_addr(dst + k * kRawBox * 2), &p.tmap_s1, (int)(e0a + (int64_t)k * kRawBox), bar);
+        tma_load_1d(smem_addr(dst + raw_elems * 2u + k * kRawBox * 2), &p.tmap_b1, (int)(e0a + (int64_t)k * kRawBox),
+                    bar);
+    }
+}
+
+// 2D-TMA mode: one box per 64-group chunk of the K-slice and per part (fused: gate rows, up
+// rows), as tall as the row block.
+__device__ __noinline__ void sb_tma_issue(const GemvOp& p, uint8_t* sdst, uint32_t bar, int64_t trow0, int kg0,
+                                         int gsz, int ntile, int parts, int half_mt) {
+    const int nchunk = (gsz + 63) / 64;
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * parts * nchunk * ntile * kTileBytes));
+    const int mi = ntile - 1;
+#pragma unroll 1
+    for (int part = 0; part < parts; ++part) {
+        const int64_t prow = trow0 + (part ? p.out_dim : 0);
+        const int mbase = part * half_mt;
+#pragma unroll 1
+        for (int c = 0; c < nchunk; ++c) {
+            const uint32_t o = (uint32_t)((c * p.sb_tiles + mbase) * kTileBytes);
+            tma_load_2d(smem_addr(sdst + o), &p.tmap_s[mi], kg0 + 64 * c, (int)prow, bar);
+            tma_load_2d(smem_addr(sdst + p.sb_pitch + o), &p.tmap_b[mi], kg0 + 64 * c, (int)prow, bar);
+        }
+    }
+}
+
+// Element-copy mode (anything TMA cannot fetch; full K): the producer lanes copy the row
+// block's scales and biases into the swizzled layout; groups up to the next 16-group block are
+// zeroed for the bias contraction.
+__device__ __noinline__ void sb_plain_copy(const GemvOp& p, uint8_t* sdst, int64_t trow0, int rows_valid, int kg0,
+                                          int gsz, int lane) {
+    const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
+    const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
+    const int64_t srow_bytes = (int64_t)p.groups * 2;
+    const int gpad = (gsz + 15) / 16 * 16;
+    const int n = 2 * rows_valid * gpad;
+#pragma unroll 1
+    for (int i = lane; i < n; i += 32) {
+        const int k = i % gpad;
+        const int rr = i / gpad;
+        const int isb = rr >= rows_valid;
+        const int r = rr - isb * rows_valid;
+        uint16_t v = 0;
+        if (k < gsz)
+            v = *reinterpret_cast<const uint16_t*>((isb ? b8 : s8) + (trow0 + r) * srow_bytes + (int64_t)(kg0 + k) * 2);
+        const uint32_t o = (uint32_t)(((k >> 6) * p.sb_tiles * 16 + r) * 128) +
+                           ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
+        *reinterpret_cast<uint16_t*>(sdst + (size_t)isb * p.sb_pitch + o) = v;
+    }
+}
+
+// Before the CTA exits, lane 0 waits for every copy it issued and no consumer waited for
+// (after an abort): the last `S` ring stages (bit k of st_bits: stage it - 1 - k), the last
+// `nsb` scale/bias fetches and the raw buffers' latest fills.
+__device__ __noinline__ void drain_copies(const uint64_t* full_b, int S, int it, uint32_t st_bits, const uint64_t* sbfull_b,
+                                         int nsb, int blk, uint32_t sb_bits, const uint64_t* rawfull_b, int raw_rb0,
+                                         int raw_rb1) {
+    int slot = (it - 1) % S, round = (it - 1) / S;
+#pragma unroll 1
+    for (int k = 0; k < S && k < it; ++k) {
+        if ((st_bits >> k) & 1u) mbar_drain(smem_addr(full_b + slot), (uint32_t)round & 1u);
+        if (--slot < 0) {
+            slot = S - 1;
+            --round;
+        }
+    }
+#pragma unroll 1
+    for (int k = 0; k < nsb && k < blk; ++k)
+        if ((sb_bits >> k) & 1u) {
+            const int q = blk - 1 - k;
+            mbar_drain(smem_addr(sbfull_b + q % nsb), (uint32_t)(q / nsb) & 1u);
+        }
+    if (raw_rb0 >= 0) mbar_drain(smem_addr(rawfull_b), (uint32_t)(raw_rb0 >> 1) & 1u);
+    if (raw_rb1 >= 0) mbar_drain(smem_addr(rawfull_b + 1), (uint32_t)(raw_rb1 >> 1) & 1u);
+}
+
+// Raw mode, consumer side: rearrange a row block's raw [rows][groups] scales and biases into
+// the swizzled [64-group chunk][row][128 B] layout, one thread per (scales | biases, row,
+// 8-group granule), one 16-byte store each; groups up to the next 16-group block are zeros for
+// the bias contraction.
+__device__ __noinline__ void raw_rearrange(const GemvOp& p, const uint16_t* rs_, uint32_t raw_elems, uint8_t* sdst,
+                                          int64_t e0, int gsz, int rv, int ctid) {
+    const int off = (int)(e0 - (e0 & ~(int64_t)7));
+    const int ngr = (gsz + 15) / 16 * 2;                 // 8-group granules, padded
+    const int items = 2 * rv * ngr;
+#pragma unroll 1
+    for (int it2 = ctid; it2 < items; it2 += kConsumerWarps * 32) {
+        const int isb = it2 >= rv * ngr;
+        const int rest = it2 - isb * rv * ngr;
+        const int r = rest / ngr;
+        const int u = rest - r * ngr;
+        const uint16_t* src = rs_ + (size_t)isb * raw_elems + off + r * gsz;
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k0 = 8 * u + 2 * e;
+            const uint32_t lo = k0 < gsz ? (uint32_t)src[k0] : 0u;
+            const uint32_t hi = k0 + 1 < gsz ? (uint32_t)src[k0 + 1] : 0u;
+            pk[e] = lo | (hi << 16);
+        }
+        const uint32_t o = (uint32_t)((((u >> 3) * p.sb_tiles * 16) + r) * 128) + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sdst + (size_t)isb * p.sb_pitch + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+}
+
 // ---- the kernel --------------------------------------------------------------------------
 
 // CB: code bits. 4: packed nibbles. 2: derived 2-bit codes q4 >> 2, w = (4 q + 1.5) s + b.
@@ -567,41 +691,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool fg = FG && p.fg;
         const OpRange R0 = op_range(p, crank, cid, pp.n_clusters);
         const int kg0 = R0.kg0, kg1 = R0.kg1, gsz = R0.gsz, nks = R0.nks, t_end = R0.t_end;
-        const uint8_t* s8 = reinterpret_cast<const uint8_t*>(p.s);
-        const uint8_t* b8 = reinterpret_cast<const uint8_t*>(p.b);
-        const int64_t srow_bytes = (int64_t)p.groups * 2;
         if (RMS && p.rms && C > 1) {   // matches the consumers' norm exchange
             cluster_arrive();
             pending = true;
         }
-        // Raw mode: 1D boxes over the contiguous [rows][groups] scales and biases of a row
-        // block. The first element is rounded down to a 16-byte boundary (TMA rule); the
-        // transform skips the difference.
-        auto raw_issue = [&](const Job& jb, int buf, int rb) {
+        auto raw_issue_to = [&](const Job& jb, int buf, int rb) {
             if (lane != 0 || *abort_flag) return;
             if (buf) raw_rb[1] = rb; else raw_rb[0] = rb;
-            const Segment& sgb = pp.seg[jb.seg];
-            const int64_t r0 = (int64_t)sgb.row0 + (int64_t)jb.tile * 16;
-            const int rv = (int)llmin((int64_t)jb.ntile * 16, p.out_dim - (int64_t)jb.tile * 16);
-            const int64_t e0 = r0 * p.groups;
-            const int64_t e0a = e0 & ~(int64_t)7;
-            const int nbx = (int)((e0 - e0a + (int64_t)rv * p.groups + kRawBox - 1) / kRawBox);
-            const uint32_t bar = smem_addr(rawfull_b + buf);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the last transform's reads
-            mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbx * kRawBox * 2));
-            uint8_t* dst = raw + (size_t)buf * 2u * L.raw_elems * 2u;
-            for (int k = 0; k < nbx; ++k) {
-                tma_load_1d(smem_addr(dst + k * kRawBox * 2), &p.tmap_s1, (int)(e0a + (int64_t)k * kRawBox), bar);
-                tma_load_1d(smem_addr(dst + L.raw_elems * 2u + k * kRawBox * 2), &p.tmap_b1,
-                            (int)(e0a + (int64_t)k * kRawBox), bar);
-            }
+            raw_issue(p, pp.seg[jb.seg], jb.tile, jb.ntile, raw + (size_t)buf * 2u * L.raw_elems * 2u, L.raw_elems,
+                      smem_addr(rawfull_b + buf));
         };
         int t = R0.t_begin;
         Job j;
         if (p.sb_mode == kSbRaw) {
             int t2 = t;
             Job j0;
-            if (next_job(p, t2, t_end, j0)) raw_issue(j0, 0, 0);
+            if (next_job(p, t2, t_end, j0)) raw_issue_to(j0, 0, 0);
             __syncwarp();
         }
         while (next_job(p, t, t_end, j)) {
@@ -622,18 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) sb_bits <<= 1;
                     if (lane == 0 && !*abort_flag) {
                         sb_bits |= 1u;
-                        const int nchunk = (gsz + 63) / 64;
-                        mbar_arrive_expect_tx(bar, (uint32_t)((fg ? 4 : 2) * nchunk * j.ntile * kTileBytes));
-                        for (int part = 0; part < (fg ? 2 : 1); ++part) {   // fused: gate rows, up rows
-                            const int64_t prow = trow0 + (part ? p.out_dim : 0);
-                            const int mbase = part * (MT / 2);
-                            const int mi = j.ntile - 1;   // one box of the row block's height
-                            for (int c = 0; c < nchunk; ++c) {
-                                const uint32_t o = (uint32_t)((c * p.sb_tiles + mbase) * kTileBytes);
-                                tma_load_2d(smem_addr(sdst + o), &p.tmap_s[mi], kg0 + 64 * c, (int)prow, bar);
-                                tma_load_2d(smem_addr(sdst + p.sb_pitch + o), &p.tmap_b[mi], kg0 + 64 * c, (int)prow, bar);
-                            }
-                        }
+                        sb_tma_issue(p, sdst, bar, trow0, kg0, gsz, j.ntile, fg ? 2 : 1, MT / 2);
                     }
                 } else if (p.sb_mode == kSbRaw) {
                     // the next row block's raw scales/biases, into the buffer the consumers
@@ -644,26 +738,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int nbuf = (blk + 1) & 1;
                         if (blk + 1 >= 2)
                             mbar_wait(smem_addr(rawempty_b + nbuf), (uint32_t)((blk + 1) / 2 - 1) & 1u, abort_flag);
-                        raw_issue(jn, nbuf, blk + 1);
+                        raw_issue_to(jn, nbuf, blk + 1);
                     }
                 } else {
-                    // element copies into the swizzled layout (full K: one CTA per cluster);
-                    // groups up to the next 16-group block are zeroed for the bias contraction
-                    const int gpad = (gsz + 15) / 16 * 16;
-                    const int n = 2 * rows_valid * gpad;
-                    for (int i = lane; i < n; i += 32) {
-                        const int k = i % gpad;
-                        const int rr = i / gpad;
-                        const int isb = rr >= rows_valid;
-                        const int r = rr - isb * rows_valid;
-                        uint16_t v = 0;
-                        if (k < gsz)
-                            v = *reinterpret_cast<const uint16_t*>((isb ? b8 : s8) + (trow0 + r) * srow_bytes +
-                                                                   (int64_t)(kg0 + k) * 2);
-                        const uint32_t o = (uint32_t)(((k >> 6) * p.sb_tiles * 16 + r) * 128) +
-                                           ((uint32_t)(((k >> 3) & 7) ^ (r & 7)) << 4) + 2u * (k & 7);
-                        *reinterpret_cast<uint16_t*>(sdst + (size_t)isb * p.sb_pitch + o) = v;
-                    }
+                    sb_plain_copy(p, sdst, trow0, rows_valid, kg0, gsz, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar);
                 }
@@ -712,23 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++blk;
         }
-        if (lane == 0) {
-            for (int k = 0; k < S && k < it; ++k)
-                if ((st_bits >> k) & 1u) {
-                    const int q = it - 1 - k;
-                    mbar_drain(smem_addr(full_b + q % S), (uint32_t)(q / S) & 1u);
-                }
-            const int nsb = (int)L.n_sb;
-            for (int k = 0; k < nsb && k < blk; ++k)
-                if ((sb_bits >> k) & 1u) {
-                    const int q = blk - 1 - k;
-                    mbar_drain(smem_addr(sbfull_b + q % nsb), (uint32_t)(q / nsb) & 1u);
-                }
-            for (int b = 0; b < 2; ++b) {
-                const int rb = b ? raw_rb[1] : raw_rb[0];
-                if (rb >= 0) mbar_drain(smem_addr(rawfull_b + b), (uint32_t)(rb >> 1) & 1u);
-            }
-        }
+        if (lane == 0)
+            drain_copies(full_b, S, it, st_bits, sbfull_b, (int)L.n_sb, blk, sb_bits, rawfull_b, raw_rb[0], raw_rb[1]);
         __syncwarp();
         if (pending) cluster_wait();
     } else {
@@ -812,36 +875,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const int q = blk % (int)L.n_sb;
             if (p.sb_mode == kSbRaw) {
-                // Rearrange the row block's raw [rows][groups] scales and biases into the
-                // swizzled [64-group chunk][row][128 B] layout: one thread per (scales | biases,
-                // row, 8-group granule), one 16-byte store each; groups up to the next 16-group
-                // block are zeros for the bias contraction. Every warp of the previous row block
-                // has passed its epilogue barrier, so the buffer is free.
+                // Rearrange the row block's raw scales and biases (every warp of the previous
+                // row block has passed its epilogue barrier, so the buffer is free).
                 mbar_wait(smem_addr(rawfull_b + (blk & 1)), (uint32_t)(blk >> 1) & 1u, abort_flag);
                 const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(smem + L.raw + (size_t)(blk & 1) * 2u * L.raw_elems * 2u);
-                uint8_t* sdst = sbuf + (size_t)q * L.sb_buf;
                 const int64_t e0 = ((int64_t)sg.row0 + (int64_t)j.tile * 16) * p.groups;
-                const int off = (int)(e0 - (e0 & ~(int64_t)7));
-                const int ngr = (gsz + 15) / 16 * 2;                 // 8-group granules, padded
                 const int rv = (int)llmin((int64_t)j.ntile * 16, p.out_dim - (int64_t)j.tile * 16);
-                const int items = 2 * rv * ngr;
-                for (int it2 = ctid; it2 < items; it2 += kConsumerWarps * 32) {
-                    const int isb = it2 >= rv * ngr;
-                    const int rest = it2 - isb * rv * ngr;
-                    const int r = rest / ngr;
-                    const int u = rest - r * ngr;
-                    const uint16_t* src = rs_ + (size_t)isb * L.raw_elems + off + r * gsz;
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k0 = 8 * u + 2 * e;
-                        const uint32_t lo = k0 < gsz ? (uint32_t)src[k0] : 0u;
-                        const uint32_t hi = k0 + 1 < gsz ? (uint32_t)src[k0 + 1] : 0u;
-                        pk[e] = lo | (hi << 16);
-                    }
-                    const uint32_t o = (uint32_t)((((u >> 3) * p.sb_tiles * 16) + r) * 128) + ((uint32_t)((u & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(sdst + (size_t)isb * p.sb_pitch + o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
+                raw_rearrange(p, rs_, L.raw_elems, sbuf + (size_t)q * L.sb_buf, e0, gsz, rv, ctid);
                 consumer_sync();
                 if (ctid == 0) mbar_arrive(smem_addr(rawempty_b + (blk & 1)));
             } else {

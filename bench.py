@@ -530,12 +530,61 @@ def time_dense(q4a, torch, out_dim, in_dim, nbs, bits=4, reps=60, profile=False)
     return out
 
 
+def time_fused_gate_up(q4a, torch, nbs, reps=60, profile=False):
+    """Per-launch time of q4a_gemv_rmsnorm_gate_up_silu on the 4096 -> 2 x 6144 matrix (the
+    decode layer's first half: RMSNorm prologue, silu(gate) * up epilogue), weight copies > 3 x
+    L2, graph of back-to-back calls, median of 5 replays."""
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    copies = max(2, int(3 * 130e6 // (INTER2 * HIDDEN * BYTES_PER_WEIGHT)) + 1)
+    ws = []
+    for _ in range(copies):
+        codes = torch.randint(0, 16, (INTER2, HIDDEN), dtype=torch.uint8, device=dev, generator=g)
+        ws.append((q4a.pack(codes), (torch.rand(INTER2, HIDDEN // 64, device=dev, generator=g) * 0.02).to(torch.bfloat16),
+                   (torch.randn(INTER2, HIDDEN // 64, device=dev, generator=g) * -0.08).to(torch.bfloat16)))
+        del codes
+    nw = (1.0 + 0.05 * torch.randn(HIDDEN, device=dev, generator=g)).to(torch.bfloat16)
+    peak, kind = load_peaks()
+    out = []
+    for nb in nbs:
+        a = torch.randn(nb, HIDDEN, device=dev, generator=g)
+        h = torch.empty(nb, INTER, dtype=torch.float16, device=dev)
+
+        def call(i):
+            w, s_, b_ = ws[i % copies]
+            q4a.gemv_rmsnorm_gate_up_silu(w, s_, b_, a, nw, eps=1e-6, out=h)
+
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        if profile:
+            for i in range(reps):
+                call(3 + i)
+            torch.cuda.synchronize()
+            out.append({"kernel": "q4a_gemv_rmsnorm_gate_up_silu", "nb": nb, "profile_launches": reps + 3})
+            continue
+        n = copies * max(1, reps // copies)
+        us = graph_us(torch, call, n)
+        nbytes = layer_bytes(nb)[0]
+        out.append({"kernel": "q4a_gemv_rmsnorm_gate_up_silu", "shape": f"{HIDDEN}->2x{INTER}", "nb": nb,
+                    "us_per_call": us, "gbs": nbytes / us / 1e3, "weights_per_s": INTER2 * HIDDEN / (us * 1e-6),
+                    "frac_of_peak": nbytes / us / 1e3 / peak, "peak": peak, "peak_kind": kind, "launches_timed": n})
+    del ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_kernel_mode(args):
     """Per-launch time of one GEMV shape (see time_dense)."""
     import torch
 
     import affine_q4_dequant_gb300 as q4a
 
+    if args.kernel == "fused_gate_up":
+        for rec in time_fused_gate_up(q4a, torch, [int(v) for v in args.nbs.split(",")], args.reps, args.profile):
+            print(json.dumps(rec), flush=True)
+        return
     out_dim, in_dim = KERNEL_SHAPES[args.kernel]
     for rec in time_dense(q4a, torch, out_dim, in_dim, [int(v) for v in args.nbs.split(",")], args.bits, args.reps,
                           args.profile):
@@ -716,6 +765,7 @@ def per_config(q4a, torch, reps=40):
     out = {
         "gemv_256x512": brief(time_dense(q4a, torch, 256, 512, [1], reps=reps)),
         "gate_up_4096x12288": brief(time_dense(q4a, torch, INTER2, HIDDEN, [1, 2, 4, 8, 16], reps=reps)),
+        "fused_rmsnorm_gate_up_silu_4096x2x6144": brief(time_fused_gate_up(q4a, torch, [1, 2, 4, 8, 16], reps=reps)),
         "down_12288x4096": brief(time_dense(q4a, torch, DOWN_OUT, DOWN_IN, [1, 4, 16], reps=reps)),
         "lm_head_4096x151936": brief(time_dense(q4a, torch, 151936, HIDDEN, [1, 8, 32, 64, 128], reps=reps)),
     }
@@ -796,7 +846,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload launch timings")
-    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["moe", "prefill"], default=None,
+    ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["fused_gate_up", "moe", "prefill"], default=None,
                     help="time one GEMV shape per launch instead of the decode-layer step")
     ap.add_argument("--reps", type=int, default=60)
     ap.add_argument("--bits", type=int, choices=[4, 3, 2], default=4,
