@@ -69,6 +69,9 @@ constexpr int kTcDqWarps = 8;
 constexpr int kTcWarpX = kTcWarpDq0 + kTcDqWarps;          // x-tile producer
 constexpr int kTcThreads = (kTcWarpX + 1) * 32;              // 480
 constexpr int kTcMaxN = 128;                // activation rows per launch (MMA N, TMEM budget)
+constexpr int kTcYCols = 16;                // activation rows per y store box (128 weight rows x 16 fp32)
+constexpr int kTcYBox = kTcM * kTcYCols * 4;   // 8 KB; two of them alternate
+constexpr int kTcEpiBarrier = 1;            // named barrier of the epilogue warps
 static_assert(kTcDqWarps * 32 == kTcUnitRows, "one dequantisation thread per unit row");
 static_assert(kTcEpiWarps * 32 == kTcM, "one epilogue thread per TMEM lane");
 static_assert(kTcDqWarps == 4 * kTcUm, "one dequantisation warp per TMEM lane quarter and tile");
@@ -78,6 +81,7 @@ struct TcLayout {
     uint32_t code_stage;
     uint32_t xr;          // x ring: xs stages of [kTcSG groups][n_pad rows][128 bytes]
     uint32_t x_stage;
+    uint32_t ybuf;        // 2 y store boxes [kTcYCols][kTcM] fp32
     uint32_t exps;        // [2][kTcUnitRows] fp32 2^-e of the rows of the next two units
     uint32_t bars;
     uint32_t tmem_slot;
@@ -94,7 +98,8 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
     L.code_stage = (uint32_t)kTcUm * kTcTileBytes;
     L.xr = L.code + (uint32_t)cs * L.code_stage;
     L.x_stage = (uint32_t)kTcSG * n_pad * 128u;             // n_pad % 16 == 0: 2 KB multiples
-    L.exps = L.xr + (uint32_t)xs * L.x_stage;
+    L.ybuf = L.xr + (uint32_t)xs * L.x_stage;
+    L.exps = L.ybuf + 2u * kTcYBox;
     L.bars = L.exps + 2u * kTcUnitRows * 4u;
     // code_full[cs] code_empty[cs] x_full[xs] x_empty[xs] a_full[A] a_empty[A]
     // acc_full[2] acc_empty[2] exp_full[2] exp_empty[2]
@@ -107,6 +112,7 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
 struct TcParams {
     CUtensorMap tmap_w;   // uint8 [out_dim][in_dim/2], box 128 bytes x 128 rows, 128B swizzle
     CUtensorMap tmap_x;   // fp16 [nb][in_dim], box 64 x n_pad, 128B swizzle
+    CUtensorMap tmap_y;   // fp32 [nb][out_dim], box kTcM x kTcYCols, no swizzle (when y_tma)
     const uint16_t* s;    // bf16 [out_dim][groups]
     const uint16_t* b;
     float* y;             // fp32 [nb][out_dim]
@@ -121,6 +127,7 @@ struct TcParams {
     uint32_t idesc;       // tcgen05 instruction descriptor (f16 x f16 -> f32, M 128, N n_pad)
     float silu_div;       // output epilogue silu(y / silu_div) when silu
     int32_t silu;
+    int32_t y_tma;        // y leaves through shared memory and TMA stores (else one store per value)
     TcLayout lay;
 };
 
@@ -209,6 +216,25 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Shared -> global tensor store of one box; completion is tracked per bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most one of this thread's bulk stores may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// All of this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kTcEpiBarrier), "n"(kTcEpiWarps * 32) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
@@ -411,6 +437,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
         // ======================= epilogue =======================
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         const int rl = quarter * 32 + lane;           // row within each 128-row tile
+        const bool elected = warp == kTcWarpEpi0 && lane == 0;   // issues the y stores
+        const uint32_t ybuf = smem_addr(smem + L.ybuf);
+        int ych = 0;                                  // y boxes stored so far (buffer = ych & 1)
+        if (elected && p.y_tma) prefetch_tensormap(&p.tmap_y);
         float esc_next[kTcUm];
         auto exponents = [&](int unit, int slot) {
 #pragma unroll
@@ -446,20 +476,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             tc_fence_after();
 #pragma unroll
             for (int u = 0; u < kTcUm; ++u) {
-                const int64_t row = (int64_t)unit * kTcUnitRows + u * kTcM + rl;
+                const int64_t row0 = (int64_t)unit * kTcUnitRows + u * kTcM;
+                const int64_t row = row0 + rl;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kTcUm + u) * p.n_pad);
-                // 32 accumulator columns per TMEM load (one load latency per 32 activation rows)
+                auto value = [&](float a) {
+                    float o = a * esc[u];
+                    if (p.silu) {
+                        const float t = o / p.silu_div;
+                        o = t / (1.0f + expf(-t));
+                    }
+                    return o;
+                };
+                // 32 accumulator columns per TMEM load (one load latency per 32 activation rows).
+                // With y_tma, each 16 columns go to one of two shared-memory boxes [16][128] and
+                // leave with one tensor store (the box's rows beyond out_dim and columns beyond
+                // nb are clipped by the tensor map): a store instruction per value and activation
+                // row costs far more issue time than the stores' bytes.
                 auto emit = [&](int c0, const float* v, int n) {
+                    if (p.y_tma) {
+#pragma unroll
+                        for (int h = 0; h < n; h += kTcYCols) {
+                            if (elected) bulk_wait_read_1();   // the store that last read this box is done with it
+                            epi_sync();
+                            const uint32_t yb = ybuf + (uint32_t)(ych & 1) * (uint32_t)kTcYBox;
+#pragma unroll
+                            for (int j = 0; j < kTcYCols; ++j)
+                                sts_f32(yb + (uint32_t)(j * kTcM + rl) * 4u, value(v[h + j]));
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            epi_sync();
+                            if (elected && row0 < p.out_dim) tma_store_2d(&p.tmap_y, yb, (int)row0, c0 + h);
+                            ++ych;
+                        }
+                        return;
+                    }
                     if (row >= p.out_dim) return;
                     for (int j = 0; j < n; ++j)
-                        if (c0 + j < p.nb) {
-                            float o = v[j] * esc[u];
-                            if (p.silu) {
-                                const float t = o / p.silu_div;
-                                o = t / (1.0f + expf(-t));
-                            }
-                            p.y[(int64_t)(c0 + j) * p.out_dim + row] = o;
-                        }
+                        if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = value(v[j]);
                 };
                 int c0 = 0;
                 for (; c0 + 32 <= p.n_pad; c0 += 32) {
@@ -477,6 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(acc_empty + buf));
         }
+        if (elected && p.y_tma) bulk_wait_all();   // no CTA exits while its y stores read shared memory
     } else if (warp < kTcWarpX) {
         // ======================= dequantisation =======================
         const int quarter = warp & 3;                     // TMEM lanes this warp may write
@@ -626,6 +679,18 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
         CUresult r = encode_tiled_cached(&prm.tmap_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+    }
+    // y through tensor stores: rows 16-byte aligned (out_dim % 4 == 0, y 16-byte aligned), and at
+    // least one full box of rows so the box never exceeds the tensor.
+    prm.y_tma = (out_dim % 4 == 0 && out_dim >= kTcM && reinterpret_cast<uintptr_t>(y) % 16 == 0) ? 1 : 0;
+    if (prm.y_tma) {
+        const cuuint64_t dims[2] = {(cuuint64_t)out_dim, (cuuint64_t)nb};
+        const cuuint64_t strides[1] = {(cuuint64_t)out_dim * 4};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcM, (cuuint32_t)kTcYCols};
+        CUresult r = encode_tiled_cached(&prm.tmap_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+                                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
     }
     uint32_t smem_bytes = 0;
