@@ -187,35 +187,23 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
-// 32 TMEM lanes (this warp's quarter) x 32 fp32 columns, one wait for all of them.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// 32 TMEM lanes (this warp's quarter) x 16 fp32 columns: thread i gets lane base+i.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 TMEM lanes (this warp's quarter) x 16 fp32 columns: thread i gets lane base+i. The load
+// is asynchronous; tc_ld16_wait completes it and names the registers, so the compiler cannot
+// move a use of them above the wait.
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void tc_ld16_wait(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // Shared -> global tensor store of one box; completion is tracked per bulk group.
@@ -474,55 +462,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             const int buf = li % p.acc_bufs;
             mbar_wait(smem_addr(acc_full + buf), (uint32_t)(li / p.acc_bufs) & 1u, abort_flag);
             tc_fence_after();
-#pragma unroll
+            // The accumulators leave 16 columns at a time in a rolled loop: the epilogue runs once
+            // per unit, so its code is cold each time, and a short loop body fetches far fewer
+            // instruction lines than an unrolled sweep. The next 16 columns' TMEM load is in
+            // flight while the current ones are stored. With y_tma, each 16 columns go to one of
+            // two shared-memory boxes [16][128] and leave with one tensor store (the box's rows
+            // beyond out_dim and columns beyond nb are clipped by the tensor map): a store
+            // instruction per value and activation row costs far more issue time than its bytes.
+            const int nh = p.n_pad / kTcYCols;
+#pragma unroll 1
             for (int u = 0; u < kTcUm; ++u) {
                 const int64_t row0 = (int64_t)unit * kTcUnitRows + u * kTcM;
                 const int64_t row = row0 + rl;
+                const float eu = u == 0 ? esc[0] : esc[1];
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kTcUm + u) * p.n_pad);
-                auto value = [&](float a) {
-                    float o = a * esc[u];
+                uint32_t r[kTcYCols];
+                tc_ld16_issue(taddr, r);
+                tc_ld16_wait(r);
+#pragma unroll 1
+                for (int h = 0; h < nh; ++h) {
+                    uint32_t rn[kTcYCols];   // the next 16 columns (the last ones again at the end)
+                    tc_ld16_issue(taddr + (uint32_t)(min(h + 1, nh - 1) * kTcYCols), rn);
+                    const int c0 = h * kTcYCols;
+                    float o[kTcYCols];
+#pragma unroll
+                    for (int j = 0; j < kTcYCols; ++j) o[j] = __uint_as_float(r[j]) * eu;
                     if (p.silu) {
-                        const float t = o / p.silu_div;
-                        o = t / (1.0f + expf(-t));
-                    }
-                    return o;
-                };
-                // 32 accumulator columns per TMEM load (one load latency per 32 activation rows).
-                // With y_tma, each 16 columns go to one of two shared-memory boxes [16][128] and
-                // leave with one tensor store (the box's rows beyond out_dim and columns beyond
-                // nb are clipped by the tensor map): a store instruction per value and activation
-                // row costs far more issue time than the stores' bytes.
-                auto emit = [&](int c0, const float* v, int n) {
-                    if (p.y_tma) {
 #pragma unroll
-                        for (int h = 0; h < n; h += kTcYCols) {
-                            if (elected) bulk_wait_read_1();   // the store that last read this box is done with it
-                            epi_sync();
-                            const uint32_t yb = ybuf + (uint32_t)(ych & 1) * (uint32_t)kTcYBox;
-#pragma unroll
-                            for (int j = 0; j < kTcYCols; ++j)
-                                sts_f32(yb + (uint32_t)(j * kTcM + rl) * 4u, value(v[h + j]));
-                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                            epi_sync();
-                            if (elected && row0 < p.out_dim) tma_store_2d(&p.tmap_y, yb, (int)row0, c0 + h);
-                            ++ych;
+                        for (int j = 0; j < kTcYCols; ++j) {
+                            const float t = o[j] / p.silu_div;
+                            o[j] = t / (1.0f + expf(-t));
                         }
-                        return;
                     }
-                    if (row >= p.out_dim) return;
-                    for (int j = 0; j < n; ++j)
-                        if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = value(v[j]);
-                };
-                int c0 = 0;
-                for (; c0 + 32 <= p.n_pad; c0 += 32) {
-                    float v[32];
-                    tc_ld32(taddr + (uint32_t)c0, v);
-                    emit(c0, v, 32);
-                }
-                if (c0 < p.n_pad) {
-                    float v[16];
-                    tc_ld16(taddr + (uint32_t)c0, v);
-                    emit(c0, v, 16);
+                    if (p.y_tma) {
+                        if (elected) bulk_wait_read_1();   // the store that last read this box is done with it
+                        epi_sync();
+                        const uint32_t yb = ybuf + (uint32_t)(ych & 1) * (uint32_t)kTcYBox;
+#pragma unroll
+                        for (int j = 0; j < kTcYCols; ++j) sts_f32(yb + (uint32_t)(j * kTcM + rl) * 4u, o[j]);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        epi_sync();
+                        if (elected && row0 < p.out_dim) tma_store_2d(&p.tmap_y, yb, (int)row0, c0);
+                        ++ych;
+                    } else if (row < p.out_dim) {
+#pragma unroll
+                        for (int j = 0; j < kTcYCols; ++j)
+                            if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = o[j];
+                    }
+                    tc_ld16_wait(rn);
+#pragma unroll
+                    for (int j = 0; j < kTcYCols; ++j) r[j] = rn[j];
                 }
             }
             tc_fence_before();
