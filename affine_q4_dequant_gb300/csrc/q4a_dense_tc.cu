@@ -176,6 +176,14 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
         : "memory");
 }
 
+// Keeps 32 registers live up to this point (the sources of an issued tcgen05.st).
+__device__ __forceinline__ void keep32(const uint32_t (&r)[32]) {
+    asm volatile("" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                 "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
 // Completion of this thread's earlier tcgen05.st: once per operand stage, before the MMA warp
 // is told the stage is ready (a wait after every store would serialise the dequantisation of
 // a stage's groups on the store latency).
@@ -551,8 +559,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                 const int cs_ = ci % CS;
                 mbar_wait(smem_addr(code_full + cs_), (uint32_t)(ci / CS) & 1u, abort_flag);
                 const uint32_t cb = code_base + (uint32_t)cs_ * L.code_stage;
-                const int ng = min(kTcChunkGroups, G - c * kTcChunkGroups);
-                for (int k = 0; k < ng; ++k) {
+                // Groups alternate between two register sets: a tcgen05.st reads its source
+                // registers after it issues, so the next group's unpack must not overwrite them.
+                uint32_t hb[2][32];
+#pragma unroll
+                for (int k = 0; k < kTcChunkGroups; ++k) {   // G % 8 == 0: every chunk is full
                     const int sa = gi % AS;
                     const int gg = k % kTcSG;           // group within the operand stage
                     const uint32_t sp = k < 2 ? s_cur.x : s_cur.y;
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     const uint4 q0 = lds_v4(cb + ((((uint32_t)(2 * k)) ^ rsw) << 4));
                     const uint4 q1 = lds_v4(cb + ((((uint32_t)(2 * k + 1)) ^ rsw) << 4));
                     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    uint32_t h[32];
+                    uint32_t (&h)[32] = hb[k & 1];
 #pragma unroll
                     for (int w8 = 0; w8 < 8; ++w8) {
                         h[4 * w8 + 0] = dequant_pair<0>(words[w8], sc, bi);
@@ -577,6 +588,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                         tc_fence_after();
                     }
                     tc_st32(a_lane + (uint32_t)((sa * kTcUm * kTcSG + gg) * kTcACols), h);
+                    if (k > 0) keep32(hb[(k + 1) & 1]);
                     if (gg == kTcSG - 1) {
                         tc_wait_st();
                         tc_fence_before();
