@@ -189,6 +189,14 @@ __device__ __forceinline__ void keep32(const uint32_t (&r)[32]) {
 // a stage's groups on the store latency).
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// One thread of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}" : "=r"(pred)::"memory");
+    return pred != 0;
+}
+
 // Arrives on the mbarrier once every tcgen05.mma this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -396,21 +404,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
         __syncwarp();
     } else if (warp == kTcWarpMma) {
         // ======================= MMA issuer =======================
-        if (lane == 0) {
-            int gi = 0, li = 0;
-            for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
-                const int buf = li % p.acc_bufs;
-                if (li >= p.acc_bufs)
-                    mbar_wait(smem_addr(acc_empty + buf), (uint32_t)(li / p.acc_bufs - 1) & 1u, abort_flag);
+        // The whole warp runs the loop (so the stage addresses are warp-uniform values) and
+        // one elected thread issues the MMAs and commits.
+        int gi = 0, li = 0;
+        for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
+            const int buf = li % p.acc_bufs;
+            if (li >= p.acc_bufs)
+                mbar_wait(smem_addr(acc_empty + buf), (uint32_t)(li / p.acc_bufs - 1) & 1u, abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t d0 = tmem + (uint32_t)(buf * kTcUm * p.n_pad);
+            for (int g = 0; g < G; g += kTcSG, ++gi) {
+                const int sx = gi % XS, sa = gi % AS;
+                mbar_wait(smem_addr(x_full + sx), (uint32_t)(gi / XS) & 1u, abort_flag);
+                mbar_wait(smem_addr(a_full + sa), (uint32_t)(gi / AS) & 1u, abort_flag);
+                __syncwarp();
                 tc_fence_after();
-                const uint32_t d0 = tmem + (uint32_t)(buf * kTcUm * p.n_pad);
-                for (int g = 0; g < G; g += kTcSG, ++gi) {
-                    const int sx = gi % XS, sa = gi % AS;
-                    mbar_wait(smem_addr(x_full + sx), (uint32_t)(gi / XS) & 1u, abort_flag);
-                    mbar_wait(smem_addr(a_full + sa), (uint32_t)(gi / AS) & 1u, abort_flag);
-                    tc_fence_after();
-                    const uint32_t xs0 = smem_addr(smem + L.xr + sx * L.x_stage);
-                    const uint32_t a0 = tmem + p.a_col0 + (uint32_t)(sa * kTcUm * kTcSG * kTcACols);
+                const uint32_t xs0 = smem_addr(smem + L.xr + sx * L.x_stage);
+                const uint32_t a0 = tmem + p.a_col0 + (uint32_t)(sa * kTcUm * kTcSG * kTcACols);
+                if (elect_one()) {
 #pragma unroll
                     for (int gg = 0; gg < kTcSG; ++gg) {
                         const uint64_t bd = smem_desc(xs0 + (uint32_t)(gg * p.n_pad * 128));
@@ -425,10 +437,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     tc_commit(smem_addr(x_empty + sx));
                     tc_commit(smem_addr(a_empty + sa));
                 }
-                tc_commit(smem_addr(acc_full + buf));
+                __syncwarp();
             }
+            if (elect_one()) tc_commit(smem_addr(acc_full + buf));
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp < kTcWarpDq0) {
         // ======================= epilogue =======================
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
