@@ -65,16 +65,18 @@ constexpr int kTcWarpMma = 1;
 constexpr int kTcWarpEpi0 = 2;
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcWarpDq0 = kTcWarpEpi0 + kTcEpiWarps;
-constexpr int kTcDqWarps = 8;
+constexpr int kTcDqSplit = 1;               // dequantisation threads per weight row (column parts)
+constexpr int kTcDqCols = kTcACols / kTcDqSplit;             // TMEM columns per thread and group
+constexpr int kTcDqWarps = 4 * kTcUm * kTcDqSplit;
 constexpr int kTcWarpX = kTcWarpDq0 + kTcDqWarps;          // x-tile producer
-constexpr int kTcThreads = (kTcWarpX + 1) * 32;              // 480
+constexpr int kTcThreads = (kTcWarpX + 1) * 32;
 constexpr int kTcMaxN = 128;                // activation rows per launch (MMA N, TMEM budget)
 constexpr int kTcYCols = 16;                // activation rows per y store box (128 weight rows x 16 fp32)
 constexpr int kTcYBox = kTcM * kTcYCols * 4;   // 8 KB; two of them alternate
 constexpr int kTcEpiBarrier = 1;            // named barrier of the epilogue warps
-static_assert(kTcDqWarps * 32 == kTcUnitRows, "one dequantisation thread per unit row");
+static_assert(kTcDqWarps * 32 == kTcUnitRows * kTcDqSplit, "kTcDqSplit dequantisation threads per unit row");
+static_assert(kTcDqSplit == 1 || kTcDqSplit == 2, "16-byte code chunks (32 weights, 16 TMEM columns) per thread");
 static_assert(kTcEpiWarps * 32 == kTcM, "one epilogue thread per TMEM lane");
-static_assert(kTcDqWarps == 4 * kTcUm, "one dequantisation warp per TMEM lane quarter and tile");
 
 struct TcLayout {
     uint32_t code;        // code ring: cs stages of kTcUm tiles
@@ -102,8 +104,8 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
     L.exps = L.ybuf + 2u * kTcYBox;
     L.bars = L.exps + 2u * kTcUnitRows * 4u;
     // code_full[cs] code_empty[cs] x_full[xs] x_empty[xs] a_full[A] a_empty[A]
-    // acc_full[2] acc_empty[2] exp_full[2] exp_empty[2]
-    L.tmem_slot = L.bars + (uint32_t)(2 * cs + 2 * xs + 2 * kTcAStages + 8) * 8u;
+    // acc_full[2] acc_empty[2] exp_full[2] exp_empty[2] exp_first
+    L.tmem_slot = L.bars + (uint32_t)(2 * cs + 2 * xs + 2 * kTcAStages + 9) * 8u;
     L.abort = L.tmem_slot + 4u;
     L.total = L.abort + 4u;
     return L;
@@ -163,25 +165,37 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-// 32 TMEM lanes (this warp's quarter) x 32 columns from 32 registers per thread (asynchronous:
+// 32 TMEM lanes (this warp's quarter) x N columns from N registers per thread (asynchronous:
 // tc_wait_st orders it before the MMA that reads it).
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
+template <int N>
+__device__ __forceinline__ void tc_st(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 16 || N == 32, "x16 or x32");
+    if constexpr (N == 16) {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+            "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+            "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+            "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+            "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+            "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+            "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+            : "memory");
+    }
 }
 
-// Keeps 32 registers live up to this point (the sources of an issued tcgen05.st).
-__device__ __forceinline__ void keep32(const uint32_t (&r)[32]) {
-    asm volatile("" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-                 "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-                 "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-                 "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+// Keeps N registers live up to this point (the sources of an issued tcgen05.st).
+template <int N>
+__device__ __forceinline__ void keep_live(const uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; i += 8)
+        asm volatile("" ::"r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]),
+                     "r"(r[i + 6]), "r"(r[i + 7]));
 }
 
 // Completion of this thread's earlier tcgen05.st: once per operand stage, before the MMA warp
@@ -281,30 +295,54 @@ __device__ __forceinline__ int row_exponent(float m) {
 
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// max over the row's groups of 15|s| + |b| (bf16 values, exact in fp32)
-__device__ __forceinline__ float row_weight_bound(const uint16_t* srow, const uint16_t* brow, int G) {
+// max over 8 groups of 15|s| + |b| (bf16 values, exact in fp32)
+__device__ __forceinline__ float bound8(uint4 sv, uint4 bv) {
+    const uint32_t ss[4] = {sv.x, sv.y, sv.z, sv.w};
+    const uint32_t bb[4] = {bv.x, bv.y, bv.z, bv.w};
     float m = 0.f;
-    for (int k = 0; k < G; k += 32) {
-        uint4 sv[4], bv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool on = k + 8 * j < G;
-            sv[j] = on ? ld_nc_16(srow + k + 8 * j) : make_uint4(0, 0, 0, 0);
-            bv[j] = on ? ld_nc_16(brow + k + 8 * j) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t ss[4] = {sv[j].x, sv[j].y, sv[j].z, sv[j].w};
-            const uint32_t bb[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float s0 = fabsf(bf16_to_f32(ss[h] & 0xFFFFu)), s1 = fabsf(bf16_to_f32(ss[h] >> 16));
-                const float b0 = fabsf(bf16_to_f32(bb[h] & 0xFFFFu)), b1 = fabsf(bf16_to_f32(bb[h] >> 16));
-                m = fmaxf(m, fmaxf(fmaf(15.f, s0, b0), fmaf(15.f, s1, b1)));
-            }
-        }
+    for (int h = 0; h < 4; ++h) {
+        const float s0 = fabsf(bf16_to_f32(ss[h] & 0xFFFFu)), s1 = fabsf(bf16_to_f32(ss[h] >> 16));
+        const float b0 = fabsf(bf16_to_f32(bb[h] & 0xFFFFu)), b1 = fabsf(bf16_to_f32(bb[h] >> 16));
+        m = fmaxf(m, fmaxf(fmaf(15.f, s0, b0), fmaf(15.f, s1, b1)));
     }
     return m;
+}
+
+// Row weight bound max_g (15|s[o][g]| + |b[o][g]|) of row row0 + lane, 0 beyond out_dim. The
+// warp reads its 32 rows together, 4 rows of 64 groups (4 x 128 bytes) per load instruction
+// (one row per thread would touch 32 cache lines per instruction); 8 lanes share a row and
+// reduce with shuffles. All 32 lanes must call it.
+__device__ __forceinline__ float warp_row_bound(const uint16_t* s, const uint16_t* b, int64_t row0, int64_t out_dim,
+                                                int G, int lane) {
+    const int sub = lane >> 3, part = lane & 7;
+    float mp[8];
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) mp[pp] = 0.f;
+    for (int k0 = 0; k0 < G; k0 += 64) {
+        const int g = k0 + part * 8;
+        uint4 sv[8], bv[8];
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) {
+            const int64_t row = row0 + pp * 4 + sub;
+            const bool on = g < G && row < out_dim;
+            sv[pp] = on ? ld_nc_16(s + row * G + g) : make_uint4(0, 0, 0, 0);
+            bv[pp] = on ? ld_nc_16(b + row * G + g) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int pp = 0; pp < 8; ++pp) mp[pp] = fmaxf(mp[pp], bound8(sv[pp], bv[pp]));
+    }
+    float own = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) {
+        float m = mp[pp];
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        const float got = __shfl_sync(0xffffffffu, m, (lane & 3) << 3);   // row 4 pp + (lane & 3)
+        if ((lane >> 2) == pp) own = got;
+    }
+    return own;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_constant__ TcParams p) {
@@ -325,6 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* exp_full = acc_empty + 2;
     uint64_t* exp_empty = exp_full + 2;
+    uint64_t* exp_first = exp_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.tmem_slot);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L.abort);
     float* exps = reinterpret_cast<float*>(smem + L.exps);
@@ -355,6 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             mbar_init(smem_addr(exp_full + i), kTcEpiWarps);
             mbar_init(smem_addr(exp_empty + i), kTcDqWarps);
         }
+        mbar_init(smem_addr(exp_first), kTcDqWarps);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -437,8 +477,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     tc_commit(smem_addr(x_empty + sx));
                     tc_commit(smem_addr(a_empty + sa));
                 }
-                __syncwarp();
             }
+            __syncwarp();
             if (elect_one()) tc_commit(smem_addr(acc_full + buf));
             __syncwarp();
         }
@@ -455,10 +495,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
 #pragma unroll
             for (int u = 0; u < kTcUm; ++u) {
                 const int64_t row = (int64_t)unit * kTcUnitRows + u * kTcM + rl;
+                const float m = warp_row_bound(p.s, p.b, row - lane, p.out_dim, G, lane);
                 int e = 0;
                 float dq = 0.f;                       // rows beyond out_dim dequantise to 0
                 if (row < p.out_dim) {
-                    e = row_exponent(row_weight_bound(p.s + row * G, p.b + row * G, G));
+                    e = row_exponent(m);
                     dq = pow2f(-e);
                 }
                 esc_next[u] = pow2f(e);
@@ -467,17 +508,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(exp_full + slot));
         };
+        // Row factors: the dequantisation threads compute their first unit's themselves (one row
+        // each, into slot 0, signalled on exp_first); this warp group computes every later
+        // unit's one unit ahead, unit j (j >= 1) into slot j % 2 as that slot's write
+        // k = (j - 1) / 2.
         grid_dep_wait();   // scales, biases and y may belong to the previous kernel of the stream
-        if ((int)blockIdx.x < p.n_units) exponents(blockIdx.x, 0);
         int li = 0;
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             float esc[kTcUm];
+            if (li == 0) {
+                mbar_wait(smem_addr(exp_first), 0u, abort_flag);
 #pragma unroll
-            for (int u = 0; u < kTcUm; ++u) esc[u] = esc_next[u];
+                for (int u = 0; u < kTcUm; ++u) {
+                    const float dqv = exps[u * kTcM + rl];   // 2^-e, or 0 beyond out_dim
+                    esc[u] = dqv > 0.f ? 1.0f / dqv : 1.0f;  // exact: a power of two
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kTcUm; ++u) esc[u] = esc_next[u];
+            }
             const int nxt = unit + gridDim.x;
             if (nxt < p.n_units) {
-                const int slot = (li + 1) & 1;
-                if (li + 1 >= 2) mbar_wait(smem_addr(exp_empty + slot), (uint32_t)((li + 1) / 2 - 1) & 1u, abort_flag);
+                const int j = li + 1, slot = j & 1, k = (j - 1) >> 1;
+                if (k >= 1) mbar_wait(smem_addr(exp_empty + slot), (uint32_t)(k - 1) & 1u, abort_flag);
                 exponents(nxt, slot);
             }
             const int buf = li % p.acc_bufs;
@@ -543,38 +596,68 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
     } else if (warp < kTcWarpX) {
         // ======================= dequantisation =======================
         const int quarter = warp & 3;                     // TMEM lanes this warp may write
-        const int u = (warp - kTcWarpDq0) / 4;            // tile
+        const int dw = warp - kTcWarpDq0;
+        const int u = (dw >> 2) % kTcUm;                  // tile
+        const int hc = dw / (4 * kTcUm);                  // column part of every group
         const int rl = quarter * 32 + lane;               // row within the tile = TMEM lane
         const int r = u * kTcM + rl;                      // row within the unit
         const uint32_t rsw = (uint32_t)rl & 7u;
         const uint32_t code_base = smem_addr(smem + L.code) + (uint32_t)(u * kTcTileBytes) + (uint32_t)rl * 128u;
-        const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 + (uint32_t)(u * kTcSG * kTcACols);
+        const uint32_t a_lane = tmem + ((uint32_t)(quarter * 32) << 16) + p.a_col0 +
+                                (uint32_t)(u * kTcSG * kTcACols + hc * kTcDqCols);
+        constexpr int kChunks = kTcDqCols / 16;           // 16-byte code chunks per thread and group
         grid_dep_wait();   // scales and biases may be written by the previous kernel of the stream
         int ci = 0, gi = 0, li = 0;
+        // scale and bias words of the next chunk (across units: the next unit's first chunk is
+        // loaded during this unit's last one)
+        uint2 s_nx = make_uint2(0, 0), b_nx = make_uint2(0, 0);
+        if ((int)blockIdx.x < p.n_units) {
+            const int64_t row = (int64_t)blockIdx.x * kTcUnitRows + r;
+            if (row < p.out_dim) {
+                s_nx = ld_nc_8(p.s + row * G);
+                b_nx = ld_nc_8(p.b + row * G);
+            }
+        }
         for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++li) {
             const int slot = li & 1;
-            mbar_wait(smem_addr(exp_full + slot), (uint32_t)(li >> 1) & 1u, abort_flag);
-            const float dq = exps[slot * kTcUnitRows + r];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(exp_empty + slot));
             const int64_t row = (int64_t)unit * kTcUnitRows + r;
             const bool valid = row < p.out_dim;
             const uint16_t* srow = p.s + (valid ? row : 0) * G;
             const uint16_t* brow = p.b + (valid ? row : 0) * G;
-            uint2 s_nx = valid ? ld_nc_8(srow) : make_uint2(0, 0);
-            uint2 b_nx = valid ? ld_nc_8(brow) : make_uint2(0, 0);
+            float dq;
+            if (li == 0) {
+                // the first unit's row factor: computed here, not waited for
+                const float m = warp_row_bound(p.s, p.b, row - lane, p.out_dim, G, lane);
+                dq = valid ? pow2f(-row_exponent(m)) : 0.f;
+                exps[r] = dq;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(exp_first));
+            } else {
+                const int k = (li - 1) >> 1;
+                mbar_wait(smem_addr(exp_full + slot), (uint32_t)k & 1u, abort_flag);
+                dq = exps[slot * kTcUnitRows + r];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(exp_empty + slot));
+            }
+            const int64_t nrow = (int64_t)(unit + gridDim.x) * kTcUnitRows + r;
+            const bool nvalid = unit + (int)gridDim.x < p.n_units && nrow < p.out_dim;
             for (int c = 0; c < nchunks; ++c, ++ci) {
                 const uint2 s_cur = s_nx, b_cur = b_nx;
-                if (c + 1 < nchunks && valid) {
-                    s_nx = ld_nc_8(srow + (c + 1) * kTcChunkGroups);
-                    b_nx = ld_nc_8(brow + (c + 1) * kTcChunkGroups);
+                if (c + 1 < nchunks) {
+                    if (valid) {
+                        s_nx = ld_nc_8(srow + (c + 1) * kTcChunkGroups);
+                        b_nx = ld_nc_8(brow + (c + 1) * kTcChunkGroups);
+                    }
+                } else {
+                    s_nx = nvalid ? ld_nc_8(p.s + nrow * G) : make_uint2(0, 0);
+                    b_nx = nvalid ? ld_nc_8(p.b + nrow * G) : make_uint2(0, 0);
                 }
                 const int cs_ = ci % CS;
                 mbar_wait(smem_addr(code_full + cs_), (uint32_t)(ci / CS) & 1u, abort_flag);
                 const uint32_t cb = code_base + (uint32_t)cs_ * L.code_stage;
                 // Groups alternate between two register sets: a tcgen05.st reads its source
                 // registers after it issues, so the next group's unpack must not overwrite them.
-                uint32_t hb[2][32];
+                uint32_t hb[2][kTcDqCols];
 #pragma unroll
                 for (int k = 0; k < kTcChunkGroups; ++k) {   // G % 8 == 0: every chunk is full
                     const int sa = gi % AS;
@@ -585,12 +668,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     const float bfv = bf16_to_f32((k & 1) ? (bp >> 16) : (bp & 0xFFFFu)) * dq;
                     const __half2 sc = __floats2half2_rn(sf, sf * 0.0625f);
                     const __half2 bi = __floats2half2_rn(bfv, bfv);
-                    const uint4 q0 = lds_v4(cb + ((((uint32_t)(2 * k)) ^ rsw) << 4));
-                    const uint4 q1 = lds_v4(cb + ((((uint32_t)(2 * k + 1)) ^ rsw) << 4));
-                    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    uint32_t (&h)[32] = hb[k & 1];
+                    uint32_t words[4 * kChunks];
 #pragma unroll
-                    for (int w8 = 0; w8 < 8; ++w8) {
+                    for (int v = 0; v < kChunks; ++v) {
+                        const uint4 q = lds_v4(cb + ((((uint32_t)(2 * k + hc * kChunks + v)) ^ rsw) << 4));
+                        words[4 * v] = q.x;
+                        words[4 * v + 1] = q.y;
+                        words[4 * v + 2] = q.z;
+                        words[4 * v + 3] = q.w;
+                    }
+                    uint32_t (&h)[kTcDqCols] = hb[k & 1];
+#pragma unroll
+                    for (int w8 = 0; w8 < 4 * kChunks; ++w8) {
                         h[4 * w8 + 0] = dequant_pair<0>(words[w8], sc, bi);
                         h[4 * w8 + 1] = dequant_pair<1>(words[w8], sc, bi);
                         h[4 * w8 + 2] = dequant_pair<2>(words[w8], sc, bi);
@@ -600,8 +689,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                         if (gi >= AS) mbar_wait(smem_addr(a_empty + sa), (uint32_t)(gi / AS - 1) & 1u, abort_flag);
                         tc_fence_after();
                     }
-                    tc_st32(a_lane + (uint32_t)((sa * kTcUm * kTcSG + gg) * kTcACols), h);
-                    if (k > 0) keep32(hb[(k + 1) & 1]);
+                    tc_st<kTcDqCols>(a_lane + (uint32_t)((sa * kTcUm * kTcSG + gg) * kTcACols), h);
+                    if (k > 0) keep_live<kTcDqCols>(hb[(k + 1) & 1]);
                     if (gg == kTcSG - 1) {
                         tc_wait_st();
                         tc_fence_before();
