@@ -29,6 +29,7 @@ __all__ = [
     "gemv_rmsnorm",
     "gemv_rmsnorm_grouped", "gemv_inject_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "decode_mlp", "lowbit_pack",
     "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error", "debug_withhold_stage",
+    "gemv_kernel_choice",
     "STATUS", "MAX_SEGMENTS",
 ]
 
@@ -78,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "q4a_moe_combine": (I32, [P, P, P, P, I32, I32, I64, I64, P, P, P, P]),
         "q4a_check_device_error": (I32, [P]),
         "q4a_debug_withhold_stage": (I32, [I32]),
+        "q4a_gemv_kernel_choice": (I32, [P, P, I32, I64, I64]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -439,6 +441,13 @@ def moe_combine(y: torch.Tensor, slot: torch.Tensor, w: torch.Tensor, y_shared: 
 
 def check_device_error(stream=None) -> None:
     _check("q4a_check_device_error", _lib.q4a_check_device_error(_stream(stream)))
+
+
+def gemv_kernel_choice(s, b, nb: int, out_dim: int, in_dim: int) -> str:
+    """The kernel gemv() launches for these arguments, without launching: "tcgen05" or "gemv".
+    s and b are the scale and bias tensors (only their addresses matter) or raw addresses."""
+    ps, pb = (ctypes.c_void_p(t.data_ptr() if isinstance(t, torch.Tensor) else int(t)) for t in (s, b))
+    return "tcgen05" if _lib.q4a_gemv_kernel_choice(ps, pb, int(nb), int(out_dim), int(in_dim)) == 1 else "gemv"
 
 
 def debug_withhold_stage(stage: int) -> None:

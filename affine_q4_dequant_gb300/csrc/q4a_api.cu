@@ -72,6 +72,11 @@ const char* q4a_status_string(q4a_status status) {
 
 int q4a_last_cuda_error(void) { return t_last_cuda_error; }
 
+int q4a_gemv_kernel_choice(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim) {
+    if (!s || !b || nb < 1 || check_matrix_shape(out_dim, in_dim) != Q4A_OK) return 0;
+    return dense_tc_eligible(s, b, nb, out_dim, in_dim) ? 1 : 0;
+}
+
 q4a_status q4a_debug_withhold_stage(int stage) {
     if (stage < -1) return Q4A_ERR_SHAPE;
     t_withhold_stage = stage;

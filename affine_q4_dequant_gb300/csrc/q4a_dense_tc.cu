@@ -845,10 +845,11 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
 }  // namespace
 
 bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim) {
-    // From NB 64, or from NB 17 on matrices tall enough to give every SM a 256-row unit (the
-    // GEMV kernel's 17..32-row form splits K across a cluster and loses to the contraction there;
-    // on shorter matrices the contraction has too few units to fill the GPU).
-    const bool wide = nb >= kDenseTcMinRows || (nb > 16 && out_dim >= (int64_t)kDenseTcTallRows);
+    // From NB 64, or from NB 13 on matrices tall enough to give every SM a 256-row unit (the
+    // GEMV kernel's 13..32-row forms lose to the contraction there: on the 4096 x 151936 LM head
+    // 154 us at NB 13..16 against 114 us, while NB 12 takes 105 us; on shorter matrices the
+    // contraction has too few units to fill the GPU).
+    const bool wide = nb >= kDenseTcMinRows || (nb >= kDenseTcTallMinRows && out_dim >= (int64_t)kDenseTcTallRows);
     return wide && (in_dim / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(s) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(b) % 16 == 0;
 }

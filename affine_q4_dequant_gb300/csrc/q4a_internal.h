@@ -24,7 +24,8 @@ constexpr int kXFragBudget = 128 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path,
-constexpr int kDenseTcTallRows = 152 * 256;   // and from 17 rows on matrices this tall
+constexpr int kDenseTcTallRows = 152 * 256;   // and from kDenseTcTallMinRows rows on matrices this tall
+constexpr int kDenseTcTallMinRows = 13;
 constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
 constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation segments per row
 
@@ -209,7 +210,7 @@ q4a_status read_and_clear_device_error(cudaStream_t stream, uint32_t* word);
 
 // Dense path for wide batches (q4a_dense_tc.cu): dequantise to binary16 tiles, tcgen05.mma.
 // Eligible when in_dim % 512 == 0, s and b are 16-byte aligned, and nb >= kDenseTcMinRows (or
-// nb > 16 with out_dim >= kDenseTcTallRows).
+// nb >= kDenseTcTallMinRows with out_dim >= kDenseTcTallRows).
 bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim);
 q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
                            int nb, int64_t out_dim, int64_t in_dim, bool silu, float silu_div,

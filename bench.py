@@ -518,11 +518,13 @@ def time_dense(q4a, torch, out_dim, in_dim, nbs, bits=4, reps=60, profile=False)
                "shape": f"{in_dim}->{out_dim}", "nb": nb, "us_per_call": us, "gbs": nbytes / us / 1e3,
                "weights_per_s": out_dim * in_dim / (us * 1e-6), "frac_of_peak": nbytes / us / 1e3 / peak,
                "peak": peak, "peak_kind": kind, "launches_timed": n, "weight_copies": copies}
-        if bits == 4 and nb >= 64 and in_dim % 512 == 0:
+        path = q4a.gemv_kernel_choice(ws[0][1], ws[0][2], nb, out_dim, in_dim) if bits == 4 else "gemv"
+        rec["path"] = path
+        if path == "tcgen05":
             # the tensor-core path: a contraction, bounded by max(bytes / HBM, flops / tensor peak)
             tflops = 2.0 * out_dim * in_dim * nb / (us * 1e-6) / 1e12
             bound_us = max(nbytes / (peak * 1e3), 2.0 * out_dim * in_dim * nb / (tc_peak * 1e12) * 1e6)
-            rec.update({"path": "tcgen05", "tflops": tflops, "tc_peak": tc_peak, "tc_peak_kind": tc_kind,
+            rec.update({"tflops": tflops, "tc_peak": tc_peak, "tc_peak_kind": tc_kind,
                         "frac_of_tc_peak": tflops / tc_peak, "frac_of_bound": bound_us / us})
         out.append(rec)
     del ws

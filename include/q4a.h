@@ -101,8 +101,9 @@ Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_d
  *   Requires nb >= 1, out_dim >= 1 (any value, odd included), in_dim >= 64,
  *   in_dim % 64 == 0; w and x 16-byte aligned; s and b 2-byte aligned.
  *   Kernel choice: the tensor-core path (weights dequantised into TMEM, tcgen05.mma) takes
- *   nb >= 64, and nb >= 17 when out_dim >= 38912 (enough 256-row units for every SM), provided
- *   in_dim % 512 == 0 and s, b are 16-byte aligned; everything else runs the GEMV kernel.
+ *   nb >= 64, and nb >= 13 when out_dim >= 38912 (enough 256-row units for every SM), provided
+ *   in_dim % 512 == 0 and s, b are 16-byte aligned; everything else runs the GEMV kernel
+ *   (q4a_gemv_kernel_choice tells which, without launching).
  *   The GEMV kernel keeps a CTA's
  *   K-slice of the activations and of the row block's scales and biases in shared memory:
  *   rows longer than that budget allows, even split across 8 CTAs, return
@@ -373,6 +374,14 @@ Q4A_API q4a_status q4a_moe_combine(float* out, const float* y, const int32_t* sl
                            int n_tok, int top_k, int64_t n_slots, int64_t hidden,
                            const float* y_shared, const uint16_t* gate, const float* x,
                            q4a_stream_t stream);
+
+/*
+ * q4a_gemv_kernel_choice -- which kernel q4a_gemv (and q4a_gemv_silu) would launch for these
+ * arguments: 1 for the tensor-core path, 0 for the GEMV kernel (the rule under q4a_gemv).
+ * Host-only: it launches nothing, touches no device memory and reads only the addresses of
+ * s and b (their alignment). Invalid shapes return 0 (the call itself would reject them).
+ */
+Q4A_API int q4a_gemv_kernel_choice(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim);
 
 /*
  * q4a_debug_withhold_stage -- a hook for testing the failure path: the next launch of the

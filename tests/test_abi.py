@@ -46,6 +46,7 @@ def lib():
     lib.q4a_decode_mlp.argtypes = [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]
     lib.q4a_gemv_inject_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     lib.q4a_debug_withhold_stage.argtypes = [I32]
+    lib.q4a_gemv_kernel_choice.argtypes = [P, P, I32, I64, I64]
     lib.q4a_gemv_experts_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, P, P, P, I32, I32, I64, I64, I64, P]
     lib.q4a_check_device_error.argtypes = [P]
     lib.q4a_last_cuda_error.restype = I32
@@ -295,6 +296,12 @@ def q4a():
     return mod, torch
 
 
+def test_binding_kernel_choice(q4a):
+    mod, _ = q4a
+    assert mod.gemv_kernel_choice(0x10000, 0x10000, 16, 151936, 4096) == "tcgen05"
+    assert mod.gemv_kernel_choice(0x10000, 0x10000, 16, 12288, 4096) == "gemv"
+
+
 def _bad(fn, what):
     with pytest.raises(ValueError, match=what):
         fn()
@@ -394,6 +401,24 @@ def test_cuda_failure_is_reported(lib):
     assert lib.q4a_last_cuda_error() != 0
     assert b"CUDA" in lib.q4a_status_string(CUDA)
     assert lib.q4a_check_device_error(None) == CUDA
+
+
+def test_gemv_kernel_choice_rule(lib):
+    """q4a_gemv's routing (host logic, no launch): the tensor-core path from NB 64, and from
+    NB 13 on matrices of >= 38912 rows (152 units of 256 rows), when in_dim % 512 == 0 and the
+    scales and biases are 16-byte aligned; the GEMV kernel otherwise."""
+    A = 0x10000
+    k = lib.q4a_gemv_kernel_choice
+    assert [k(A, A, nb, 151936, 4096) for nb in (1, 8, 12, 13, 16, 17, 32, 63, 64, 128, 300)] == \
+        [0, 0, 0, 1, 1, 1, 1, 1, 1, 1, 1]
+    assert [k(A, A, nb, 38911, 4096) for nb in (13, 32, 63, 64)] == [0, 0, 0, 1]
+    assert [k(A, A, nb, 38912, 4096) for nb in (12, 13)] == [0, 1]
+    assert [k(A, A, nb, 12288, 4096) for nb in (1, 16, 32, 64)] == [0, 0, 0, 1]
+    assert k(A + 2, A, 64, 4096, 4096) == 0        # scales not 16-byte aligned
+    assert k(A, A + 8, 64, 4096, 4096) == 0        # biases not 16-byte aligned
+    assert k(A, A, 64, 4096, 4096 + 64) == 0       # 65 groups: not a multiple of 8
+    assert k(A, A, 64, 4096, 512) == 1
+    assert k(None, A, 64, 4096, 4096) == 0 and k(A, A, 0, 4096, 4096) == 0 and k(A, A, 64, 4096, 100) == 0
 
 
 def test_withhold_stage_hook_arguments(lib):

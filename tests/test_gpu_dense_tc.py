@@ -140,21 +140,21 @@ def test_wide_batch_falls_back_when_ineligible():
 
 
 def test_wide_batch_runs_on_the_tensor_core_kernel():
-    """The kernel a NB >= 64 call launches is the tcgen05 one; NB = 16 stays on the GEMV."""
-    prof = pytest.importorskip("torch.profiler")
+    """The routing a call takes (q4a_gemv_kernel_choice, the function the dispatch itself calls):
+    NB 64 on a short matrix and NB 13 on a tall one run the tcgen05 kernel, NB 16 on a short
+    matrix and NB 12 on a tall one the GEMV kernel; each result meets the oracle's bar."""
     packed, s, b, x = case(256, 512, 64, 16)
-    args = [dev(packed), dev(s), dev(b)]
-    x64, x16 = dev(x), dev(x[:16])
-    torch.cuda.synchronize()
-    with prof.profile(activities=[prof.ProfilerActivity.CUDA]) as p:
-        q4a.gemv(*args, x64)
-        torch.cuda.synchronize()
-    names = [e.name for e in p.events()]
-    if not names:
-        pytest.skip("the profiler recorded no kernels")
-    assert any("dense_tc_kernel" in n for n in names), names
-    with prof.profile(activities=[prof.ProfilerActivity.CUDA]) as p:
-        q4a.gemv(*args, x16)
-        torch.cuda.synchronize()
-    names = [e.name for e in p.events()]
-    assert any("gemv_kernel" in n for n in names) and not any("dense_tc_kernel" in n for n in names), names
+    sd, bd = dev(s), dev(b)
+    assert q4a.gemv_kernel_choice(sd, bd, 64, 256, 512) == "tcgen05"
+    assert q4a.gemv_kernel_choice(sd, bd, 16, 256, 512) == "gemv"
+    y_ref, bound = oracle.gemv(packed, s, b, x)
+    check(gemv(packed, s, b, x, 256, s_dev=sd, b_dev=bd), y_ref, bound, "NB 64 (tcgen05)")
+    check(gemv(packed, s, b, x[:16], 256, s_dev=sd, b_dev=bd), y_ref[:16], bound[:16], "NB 16 (GEMV)")
+    out_dim = 152 * 256
+    packed, s, b, x = case(out_dim, 512, 13, 17)
+    sd, bd = dev(s), dev(b)
+    assert q4a.gemv_kernel_choice(sd, bd, 13, out_dim, 512) == "tcgen05"
+    assert q4a.gemv_kernel_choice(sd, bd, 12, out_dim, 512) == "gemv"
+    y_ref, bound = oracle.gemv(packed, s, b, x)
+    check(gemv(packed, s, b, x, out_dim, s_dev=sd, b_dev=bd), y_ref, bound, "tall NB 13 (tcgen05)")
+    check(gemv(packed, s, b, x[:12], out_dim, s_dev=sd, b_dev=bd), y_ref[:12], bound[:12], "tall NB 12 (GEMV)")
