@@ -183,19 +183,19 @@ __device__ __forceinline__ float inject_weight(const P& p, int64_t slot, int g) 
 // field j is read in place (value 4^j * code), so step j's activations are scaled by 4^-j.
 // XF: the activations are fp32 (prefill); staging rounds them to binary16, the operand type of
 // the mma, as the pages' prefill contraction does (it rounds its fp32 rows to half).
-template <int NT, bool RMS, int CB, bool XF, class P>
+template <int NT, bool RMS, int CB, bool XF, bool INJ, class P>
 __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                           float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     static_assert(CB == 4 || !RMS, "the RMSNorm prologue is built for 4-bit codes only");
     static_assert(!(RMS && XF), "the RMSNorm prologue reads fp32 rows itself");
     constexpr int NTOK = NT * 8;
     constexpr int BATCH = RMS ? 2 : 4;
-    constexpr int NLD = RMS ? 10 : (XF ? 4 : 2);   // RMSNorm: x (4), norm weight (2), injected output (4)
+    constexpr int NLD = RMS ? (INJ ? 10 : 6) : (XF ? 4 : 2);   // RMSNorm: x (4), norm weight (2), injected output (4)
     constexpr int NTH = kConsumerWarps * 32;
     const int items = sg.ntok * gsz * 4;
     const int ntm = p.ntok_max;
     const uint32_t scale_odd = 0x2C002C00u;   // half2(1/16, 1/16)
-    const bool inj = RMS && p.inj_out != nullptr;
+    constexpr bool inj = RMS && INJ;   // injection code only in the kernels built for it
     for (int base = 0; base < items; base += BATCH * NTH) {
         // phase 1: loads
         uint4 ld[BATCH][NLD];
@@ -231,7 +231,7 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
                     ld[k][3] = ld_nc_16(xr + 36);
                     ld[k][4] = ld_nc_16(p.norm_w + col);
                     ld[k][5] = ld_nc_16(p.norm_w + col + 32);
-                    if (inj) {
+                    if constexpr (inj) {
                         // the item's 16 inputs lie in one 64-group, hence in one stream
                         const int64_t seg = col / p.norm_width;
                         const float* orow = p.inj_out + src * p.norm_width + (col - seg * p.norm_width);
@@ -274,16 +274,17 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
                 const float inv = live ? inv_s[tok * p.norm_groups + seg] : 0.f;
                 const int64_t slot = sg.tok0 + tok;
                 const float wgt = inj && live ? inject_weight(p, slot, seg) : 0.f;
-                float* xn_row = write_xnew && live ? p.x_new + slot * p.in_dim + (int64_t)(kg0 + gl) * kGroup + 8 * t
+                float* xn_row = inj && write_xnew && live ? p.x_new + slot * p.in_dim + (int64_t)(kg0 + gl) * kGroup + 8 * t
                                                    : nullptr;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint4 f0 = ld[k][2 * half], f1 = ld[k][2 * half + 1], wv = ld[k][4 + half];
-                    const uint4 o0 = ld[k][6 + 2 * half], o1 = ld[k][7 + 2 * half];
+
                     float xs[8] = {__uint_as_float(f0.x), __uint_as_float(f0.y), __uint_as_float(f0.z),
                                    __uint_as_float(f0.w), __uint_as_float(f1.x), __uint_as_float(f1.y),
                                    __uint_as_float(f1.z), __uint_as_float(f1.w)};
-                    if (inj) {
+                    if constexpr (inj) {
+                        const uint4 o0 = ld[k][6 + 2 * half], o1 = ld[k][7 + 2 * half];
                         const uint32_t os[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
                         for (int e = 0; e < 8; ++e) xs[e] = fmaf(__uint_as_float(os[e]), wgt, xs[e]);
@@ -355,16 +356,16 @@ __device__ void stage_x_t(const P& p, const Segment& sg, int kg0, int gsz, uint8
 
 // Staging of one op's activations: the RMSNorm form when the op asks for it (kernels built
 // with RMS), the plain fp16 form otherwise.
-template <int NT, bool RMS, int CB, bool XF, class P>
+template <int NT, bool RMS, int CB, bool XF, bool INJ, class P>
 __device__ __forceinline__ void stage_x(const P& p, bool rms, const Segment& sg, int kg0, int gsz, uint8_t* xfrag,
                                         float* xsum_s, const float* inv_s, int ctid, bool write_xnew) {
     if constexpr (RMS) {
         if (rms) {
-            stage_x_t<NT, true, CB, false>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, write_xnew);
+            stage_x_t<NT, true, CB, false, INJ>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, write_xnew);
             return;
         }
     }
-    stage_x_t<NT, false, CB, XF>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, false);
+    stage_x_t<NT, false, CB, XF, false>(p, sg, kg0, gsz, xfrag, xsum_s, inv_s, ctid, false);
 }
 
 // B fragments of the bias term sum_g b[o][g] * xsum[r][g], an m16n8k16 contraction over
@@ -412,13 +413,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // Work units are (row, segment, part): with fewer rows than consumer warps every row is split
 // into parts so that all warps load at once (one memory round trip at NB 1); each lane keeps
 // 16 independent 16-byte loads in flight. The parts' sums meet in `red` in a fixed order.
-template <int NT, class P>
+template <int NT, bool INJ, class P>
 __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, float* ssq_s, float* red, int warp,
                             int lane, int ctid) {
     constexpr int NTOK = NT * 8;
     constexpr int U = 16;
     const int G = p.norm_groups;
-    const bool inj = p.inj_out != nullptr;
+    constexpr bool inj = INJ;
     const int ntok = sg.ntok;
     const int parts = ntok >= kConsumerWarps ? 1 : kConsumerWarps / ntok;
     const int units = ntok * G * parts;
@@ -447,7 +448,7 @@ __device__ void rms_partial(const P& p, const Segment& sg, int kg0, int gsz, flo
                     const int c = c0 + k * 32 + lane;
                     f[k] = c < c_hi ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                if (inj) {
+                if constexpr (inj) {
 #pragma unroll
                     for (int k = 0; k < U; ++k) {
                         const int c = c0 + k * 32 + lane;
@@ -612,7 +613,7 @@ __device__ __noinline__ void raw_rearrange(const GemvOp& p, const uint16_t* rs_,
 // MTT: tiles per row block (0: the default for NT). Rows that a short row block lacks still
 // cost their mma work (the tile loop is unrolled for a fixed tile count), so launches whose
 // clusters get only a few tiles use a kernel built for that many.
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> pp) {
     constexpr int NTOK = NT * 8;
@@ -815,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rms) {
             // Sum of squares of this CTA's K-slice per activation row, exchanged across the
             // cluster so every CTA normalises with the full-row statistics.
-            rms_partial<NT>(p, pp.seg[0], kg0, gsz, ssq_s, wpart, warp, lane, ctid);
+            rms_partial<NT, INJ>(p, pp.seg[0], kg0, gsz, ssq_s, wpart, warp, lane, ctid);
             if (C > 1) {
                 cluster_arrive();
                 cluster_wait();
@@ -858,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (next_job(p, t, t_end, j)) {
             const Segment& sg = pp.seg[j.seg];
             if (j.seg != staged_seg) {
-                stage_x<NT, RMS, CB, XF>(p, rms, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
+                stage_x<NT, RMS, CB, XF, INJ>(p, rms, sg, kg0, gsz, xfrag, xsum_s, ssq_s + NTOK * kMaxNormGroups, ctid,
                                      rms && cid == 0 && p.x_new != nullptr);
                 consumer_sync();
                 stage_xbias(xsum_s, sg.ntok, p.ntok_max, NTOK, gsz, xbias, ctid);
@@ -1252,9 +1253,9 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1331,9 +1332,9 @@ int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_
                    : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1347,7 +1348,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT, XF>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.op.n_tiles ? max_clusters : prm.op.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
@@ -1465,6 +1466,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     const int cb = L.code_bits;
     if (cb != 4 && (L.rmsnorm || (cb != 2 && cb != 3))) return Q4A_ERR_UNSUPPORTED;
     if (L.x_f32 && (!L.experts || cb == 4 || L.rmsnorm)) return Q4A_ERR_UNSUPPORTED;
+    if (L.inj_out && (!L.rmsnorm || L.fused_gate_up || cb != 4 || MAXSEG != kDenseMaxSeg)) return Q4A_ERR_UNSUPPORTED;
     const bool fg = L.fused_gate_up;
     if (fg && (L.experts || cb != 4 || L.silu || L.out_dim % 16 != 0 || !L.h)) return Q4A_ERR_UNSUPPORTED;
     // schedule units per row block: tiles, or (fused) gate|up tile pairs
@@ -1571,6 +1573,11 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
             if (nt == 1) return launch_variant<1, false, MAXSEG, 3>(prm, smem_bytes, stream);
             if (nt == 2) return launch_variant<2, false, MAXSEG, 3>(prm, smem_bytes, stream);
             return launch_variant<4, false, MAXSEG, 3>(prm, smem_bytes, stream);
+        }
+        if (L.rmsnorm && L.inj_out) {   // the injection prologue: its own kernels
+            if (nt == 1) return launch_variant<1, true, MAXSEG, 4, false, 0, false, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, true, MAXSEG, 4, false, 0, false, true>(prm, smem_bytes, stream);
+            return launch_variant<4, true, MAXSEG, 4, false, 0, false, true>(prm, smem_bytes, stream);
         }
         if (L.rmsnorm) {
             if (nt == 1) return launch_variant<1, true, MAXSEG>(prm, smem_bytes, stream);
