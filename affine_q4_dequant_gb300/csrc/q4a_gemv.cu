@@ -619,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NTOK = NT * 8;
     constexpr int MT = MTT ? MTT : tiles_per_block(NT);  // tiles per row block
     constexpr int TPW = MT;                  // tiles per consumer warp: all of the row block
+    static_assert(MT >= 1 && MT <= kNumMaps, "row blocks of at most kNumMaps tiles: one tensor map per height");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1010,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rows through ldmatrix, B is the hi/lo split group sums.
             {
                 const int nblk = (gsz + 15) / 16;
-                for (int gb = wg; gb < nblk; gb += kGroupSlots) {
+                for (int gb = kGroupSlots - 1 - wg; gb < nblk; gb += kGroupSlots) {   // last warps first
                     uint32_t bx[NT][4];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
