@@ -26,6 +26,7 @@ from . import _build
 
 __all__ = [
     "Q4AError", "lib_path", "pack", "xsum", "gemv", "gemv_silu", "gemv_experts", "gemv_experts_lowbit",
+    "gemv_experts_gate_up_silu",
     "gemv_rmsnorm",
     "gemv_rmsnorm_grouped", "gemv_inject_rmsnorm_grouped", "gemv_gate_up_silu", "gemv_rmsnorm_gate_up_silu", "decode_mlp", "lowbit_pack",
     "gemv_lowbit", "quantize", "gemv_f32x", "silu_mul_xsum", "moe_combine", "check_device_error", "debug_withhold_stage",
@@ -71,6 +72,7 @@ def _load() -> ctypes.CDLL:
         "q4a_decode_mlp": (I32, [P, P, P, P, P, P, P, F, F, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_lowbit": (I32, [P, I32, P, P, P, P, P, I32, I64, I64, P]),
         "q4a_gemv_experts": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
+        "q4a_gemv_experts_gate_up_silu": (I32, [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_experts_lowbit": (I32, [P, I32, P, P, P, P, P, I32, P, P, P, I32, I32, I64, I64, I64, P]),
         "q4a_gemv_rmsnorm": (I32, [P, P, P, P, P, P, F, F, I32, I64, I64, P]),
         "q4a_gemv_rmsnorm_grouped": (I32, [P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]),
@@ -374,6 +376,31 @@ def gemv_experts(w_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n
     _check("q4a_gemv_experts", _lib.q4a_gemv_experts(
         py, pw, ps, pb, px, pr, ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
         int(expert_ids.shape[0]), int(n_experts), n_rows, int(out_dim), int(in_dim), _stream(stream)))
+    return out
+
+
+def gemv_experts_gate_up_silu(w_bank, s_bank, b_bank, x, x_rows, expert_ids, token_offsets, n_experts: int,
+                              inter: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h = fp16(silu(gate) * up) [n_rows][inter] over a bank of fused gate|up experts (expert e:
+    gate rows e*2*inter .., then its up rows). expert_ids / token_offsets are HOST int32 arrays;
+    x_rows is a CUDA int32 tensor or None."""
+    expert_ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    token_offsets = np.ascontiguousarray(token_offsets, dtype=np.int32)
+    if token_offsets.ndim != 1 or expert_ids.ndim != 1 or token_offsets.shape[0] != expert_ids.shape[0] + 1:
+        raise ValueError("token_offsets must have one entry more than expert_ids")
+    n_rows = int(token_offsets[-1])
+    x_n, in_dim = _dims(x, "x")
+    out = _empty((max(n_rows, 0), inter), torch.float16, x) if out is None else out
+    if x_rows is None and x_n < n_rows:
+        raise ValueError(f"x has {x_n} rows; without x_rows it needs token_offsets[-1] = {n_rows}")
+    xr = None if x_rows is None else (x_rows, "x_rows", _I32, (n_rows,))
+    ph, pw, ps, pb, px, pr = _ptrs(
+        (out, "h", _F16, (n_rows, inter)),
+        *_mat(w_bank, s_bank, b_bank, int(n_experts) * 2 * int(inter), in_dim, "w_bank", "s_bank", "b_bank"),
+        (x, "x", _F16, None), xr)
+    _check("q4a_gemv_experts_gate_up_silu", _lib.q4a_gemv_experts_gate_up_silu(
+        ph, pw, ps, pb, px, pr, ctypes.c_void_p(expert_ids.ctypes.data), ctypes.c_void_p(token_offsets.ctypes.data),
+        int(expert_ids.shape[0]), int(n_experts), n_rows, int(inter), int(in_dim), _stream(stream)))
     return out
 
 

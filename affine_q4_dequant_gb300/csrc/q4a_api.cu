@@ -430,20 +430,27 @@ namespace {
 
 // The routed-expert schedule shared by the 4-bit and the low-bit entry points: host checks of
 // the segment table, NaN rows for out-of-range expert ids, one launch over every segment.
-q4a_status experts_common(float* y, const uint8_t* w_bank, const uint8_t* w_lo_bank, int code_bits,
+// y (fp32 [n_rows][out_dim]) or, with h set, the fused gate|up form: experts of 2 * out_dim rows
+// (gate, then up) and h = fp16(silu(gate) * up) [n_rows][out_dim].
+q4a_status experts_common(float* y, uint16_t* h, const uint8_t* w_bank, const uint8_t* w_lo_bank, int code_bits,
                           const uint16_t* s_bank, const uint16_t* b_bank, const void* x, bool x_f32,
                           const int32_t* x_rows, const int32_t* expert_ids, const int32_t* token_offsets,
                           int n_active, int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
                           cudaStream_t stream) {
+    const bool fg = h != nullptr;
+    const int64_t rows_per_expert = fg ? 2 * out_dim : out_dim;
     if (n_active < 1 || n_active > Q4A_MAX_SEGMENTS || n_experts < 1 || n_rows < 1) return Q4A_ERR_SHAPE;
-    q4a_status st = check_matrix_shape(out_dim, in_dim);
+    if (fg && (out_dim < 16 || out_dim % 16 != 0)) return Q4A_ERR_SHAPE;
+    q4a_status st = check_matrix_shape(rows_per_expert, in_dim);
     if (st != Q4A_OK) return st;
     if (code_bits == 3 && in_dim % 128 != 0) return Q4A_ERR_SHAPE;   // lowest-bit rows: 16-byte multiples
-    if ((int64_t)n_experts * out_dim > ((int64_t)1 << 31) - 16) return Q4A_ERR_UNSUPPORTED;
+    if ((int64_t)n_experts * rows_per_expert > ((int64_t)1 << 31) - 16) return Q4A_ERR_UNSUPPORTED;
     if (n_rows > ((int64_t)1 << 31) - 1) return Q4A_ERR_UNSUPPORTED;
     if (!aligned(w_bank, 16) || (w_lo_bank && !aligned(w_lo_bank, 16)) || !aligned(x, 16) || !aligned(s_bank, 2) ||
-        !aligned(b_bank, 2) || !aligned(y, 4) || (x_rows && !aligned(x_rows, 4)))
+        !aligned(b_bank, 2) || (y && !aligned(y, 4)) || (fg && !aligned(h, 16)) || (x_rows && !aligned(x_rows, 4)))
         return Q4A_ERR_ALIGN;
+    // the fused row blocks fetch the gate and up rows' scales with 2D TMA boxes only
+    if (fg && (in_dim % 512 != 0 || !aligned(s_bank, 16) || !aligned(b_bank, 16))) return Q4A_ERR_UNSUPPORTED;
     if (token_offsets[0] != 0 || token_offsets[n_active] != n_rows) return Q4A_ERR_SHAPE;
     for (int a = 0; a < n_active; ++a)
         if (token_offsets[a + 1] < token_offsets[a]) return Q4A_ERR_SHAPE;
@@ -458,7 +465,7 @@ q4a_status experts_common(float* y, const uint8_t* w_bank, const uint8_t* w_lo_b
             bad.push_back(a);
             continue;
         }
-        push_segments(segs, (int32_t)((int64_t)e * out_dim), token_offsets[a], n);
+        push_segments(segs, (int32_t)((int64_t)e * rows_per_expert), token_offsets[a], n);
     }
     if ((int)segs.size() > Q4A_MAX_SEGMENTS) return Q4A_ERR_UNSUPPORTED;
     int max_ntok = 0;
@@ -467,13 +474,15 @@ q4a_status experts_common(float* y, const uint8_t* w_bank, const uint8_t* w_lo_b
     L.w = w_bank;
     L.w_lo = code_bits == 3 ? w_lo_bank : nullptr;
     L.code_bits = code_bits;
-    L.tensor_rows = (int64_t)n_experts * out_dim;
+    L.tensor_rows = (int64_t)n_experts * rows_per_expert;
     L.s = s_bank;
     L.b = b_bank;
     L.x = x;
     L.x_f32 = x_f32;
     L.x_rows = x_rows;
     L.y = y;
+    L.h = h;
+    L.fused_gate_up = fg;
     L.out_dim = out_dim;
     L.in_dim = in_dim;
     L.experts = true;
@@ -487,7 +496,8 @@ q4a_status experts_common(float* y, const uint8_t* w_bank, const uint8_t* w_lo_b
         L.plan_only = false;
     }
     for (int a : bad) {
-        st = launch_fill_nan(y, token_offsets[a], token_offsets[a + 1] - token_offsets[a], out_dim, stream);
+        const int64_t r0 = token_offsets[a], nr = token_offsets[a + 1] - token_offsets[a];
+        st = fg ? launch_fill_nan_h(h, r0, nr, out_dim, stream) : launch_fill_nan(y, r0, nr, out_dim, stream);
         if (st != Q4A_OK) return st;
     }
     if (segs.empty()) return Q4A_OK;
@@ -505,8 +515,18 @@ q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint16_t* s_b
                             int n_experts, int64_t n_rows, int64_t out_dim, int64_t in_dim,
                             q4a_stream_t stream) {
     if (!y || !w_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets) return Q4A_ERR_NULL;
-    return experts_common(y, w_bank, nullptr, 4, s_bank, b_bank, x, false, x_rows, expert_ids, token_offsets,
+    return experts_common(y, nullptr, w_bank, nullptr, 4, s_bank, b_bank, x, false, x_rows, expert_ids, token_offsets,
                           n_active, n_experts, n_rows, out_dim, in_dim, (cudaStream_t)stream);
+}
+
+q4a_status q4a_gemv_experts_gate_up_silu(uint16_t* h, const uint8_t* w_bank, const uint16_t* s_bank,
+                                         const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
+                                         const int32_t* expert_ids, const int32_t* token_offsets, int n_active,
+                                         int n_experts, int64_t n_rows, int64_t inter, int64_t in_dim,
+                                         q4a_stream_t stream) {
+    if (!h || !w_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets) return Q4A_ERR_NULL;
+    return experts_common(nullptr, h, w_bank, nullptr, 4, s_bank, b_bank, x, false, x_rows, expert_ids, token_offsets,
+                          n_active, n_experts, n_rows, inter, in_dim, (cudaStream_t)stream);
 }
 
 q4a_status q4a_gemv_experts_lowbit(float* y, int bits, const uint8_t* w_up_bank, const uint8_t* w_lo_bank,
@@ -517,7 +537,7 @@ q4a_status q4a_gemv_experts_lowbit(float* y, int bits, const uint8_t* w_up_bank,
     if (bits != 2 && bits != 3) return Q4A_ERR_UNSUPPORTED;
     if (!y || !w_up_bank || !s_bank || !b_bank || !x || !expert_ids || !token_offsets || (bits == 3 && !w_lo_bank))
         return Q4A_ERR_NULL;
-    return experts_common(y, w_up_bank, bits == 3 ? w_lo_bank : nullptr, bits, s_bank, b_bank, x, x_is_f32 != 0,
+    return experts_common(y, nullptr, w_up_bank, bits == 3 ? w_lo_bank : nullptr, bits, s_bank, b_bank, x, x_is_f32 != 0,
                           x_rows, expert_ids, token_offsets, n_active, n_experts, n_rows, out_dim, in_dim,
                           (cudaStream_t)stream);
 }

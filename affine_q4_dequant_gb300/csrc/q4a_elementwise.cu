@@ -277,11 +277,11 @@ __global__ void silu_mul_kernel(uint16_t* __restrict__ h, float* __restrict__ hs
     }
 }
 
-__global__ void fill_nan_kernel(float* __restrict__ y, int64_t n) {
+__global__ void fill_nan_kernel(uint32_t* __restrict__ y, int64_t n, uint32_t pattern) {
     grid_dep_wait();
     grid_dep_launch();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = __int_as_float(0x7fc00000);
+        y[i] = pattern;
 }
 
 // Routed-expert combine ("BATCH_MSL" page, experts.metal fn_moe_combine_b and
@@ -437,7 +437,14 @@ q4a_status launch_moe_combine(float* out, const float* y, const int32_t* slot, c
 
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim, cudaStream_t stream) {
     const int64_t n = nrows * out_dim;
-    return launch_pdl(fill_nan_kernel, grid_for(n, 256), 256, stream, y + row0 * out_dim, n);
+    return launch_pdl(fill_nan_kernel, grid_for(n, 256), 256, stream, reinterpret_cast<uint32_t*>(y + row0 * out_dim), n,
+                      0x7fc00000u);
+}
+
+q4a_status launch_fill_nan_h(uint16_t* h, int64_t row0, int64_t nrows, int64_t inter, cudaStream_t stream) {
+    const int64_t n = nrows * inter / 2;   // inter is even: pairs of binary16 NaNs
+    return launch_pdl(fill_nan_kernel, grid_for(n, 256), 256, stream, reinterpret_cast<uint32_t*>(h + row0 * inter), n,
+                      0x7e007e00u);
 }
 
 }  // namespace q4a

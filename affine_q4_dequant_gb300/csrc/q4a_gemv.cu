@@ -1469,7 +1469,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     if (L.x_f32 && (!L.experts || cb == 4 || L.rmsnorm)) return Q4A_ERR_UNSUPPORTED;
     if (L.inj_out && (!L.rmsnorm || L.fused_gate_up || cb != 4 || MAXSEG != kDenseMaxSeg)) return Q4A_ERR_UNSUPPORTED;
     const bool fg = L.fused_gate_up;
-    if (fg && (L.experts || cb != 4 || L.silu || L.out_dim % 16 != 0 || !L.h)) return Q4A_ERR_UNSUPPORTED;
+    if (fg && (cb != 4 || L.silu || L.x_f32 || L.out_dim % 16 != 0 || !L.h || (L.experts && L.rmsnorm)))
+        return Q4A_ERR_UNSUPPORTED;
     // schedule units per row block: tiles, or (fused) gate|up tile pairs
     int mt_units = fg ? mt / 2 : mt;
     const int G = (int)(L.in_dim / kGroup);
@@ -1587,6 +1588,11 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         }
     }
     if constexpr (MAXSEG != kDenseMaxSeg) {
+        if (fg) {   // routed experts' fused gate|up with the activation in the epilogue
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
+        }
         // routed low-bit experts, binary16 or fp32 activations
         if (cb == 2 && !L.x_f32) {
             if (nt == 1) return launch_variant<1, false, MAXSEG, 2>(prm, smem_bytes, stream);

@@ -203,6 +203,7 @@ q4a_status launch_silu_mul_xsum(uint16_t* h, float* hsum, const float* gate_up, 
                                 int64_t inter, cudaStream_t stream);
 q4a_status launch_fill_nan(float* y, int64_t row0, int64_t nrows, int64_t out_dim,
                            cudaStream_t stream);
+q4a_status launch_fill_nan_h(uint16_t* h, int64_t row0, int64_t nrows, int64_t inter, cudaStream_t stream);
 q4a_status launch_moe_combine(float* out, const float* y, const int32_t* slot, const float* w, int n_tok,
                               int top_k, int64_t n_slots, int64_t hidden, const float* y_shared,
                               const uint16_t* gate, const float* x, cudaStream_t stream);

@@ -267,6 +267,27 @@ Q4A_API q4a_status q4a_gemv_experts(float* y, const uint8_t* w_bank, const uint1
                             int64_t in_dim, q4a_stream_t stream);
 
 /*
+ * q4a_gemv_experts_gate_up_silu -- q4a_gemv_experts over a bank of fused gate|up experts with
+ * the activation in the epilogue ("BATCH_MSL", experts.metal fn_moe_gate_up_b followed by
+ * fn_moe_act_b): expert e holds its gate rows at e*2*inter .. e*2*inter+inter-1 and its up
+ * rows right after them, and for row r of segment a (expert e = expert_ids[a])
+ *     h[r][i] = fp16( silu(g) * u ),  g = (W_e,gate . x_r)[i],  u = (W_e,up . x_r)[i]
+ * with x_r = x[x_rows ? x_rows[r] : r]; no fp32 gate|up output exists.
+ *   h              out   fp16 [n_rows][inter]
+ *   w_bank         in    uint8 [n_experts*2*inter][in_dim/2]
+ *   s_bank, b_bank in    bf16 [n_experts*2*inter][in_dim/64], 16-byte aligned
+ *   x, x_rows, expert_ids, token_offsets, n_active, n_rows as q4a_gemv_experts.
+ *   Requires inter % 16 == 0 and in_dim % 512 == 0 (the fused row blocks fetch the gate and
+ *   up scales with 2D TMA boxes); other layouts return Q4A_ERR_UNSUPPORTED. A segment whose
+ *   expert id lies outside [0, n_experts) produces NaN rows of h.
+ */
+Q4A_API q4a_status q4a_gemv_experts_gate_up_silu(uint16_t* h, const uint8_t* w_bank, const uint16_t* s_bank,
+                                                 const uint16_t* b_bank, const uint16_t* x, const int32_t* x_rows,
+                                                 const int32_t* expert_ids, const int32_t* token_offsets,
+                                                 int n_active, int n_experts, int64_t n_rows, int64_t inter,
+                                                 int64_t in_dim, q4a_stream_t stream);
+
+/*
  * q4a_gemv_experts_lowbit -- q4a_gemv_experts over derived low-bit codes, on binary16 or fp32
  * activations: the routed form of the 2/3-bit products ("BATCH_MSL", quantized_rows.metal
  * fn_q2_rows_h / fn_q3_rows_h for decode rows; expert_gemm.metal fn_expert_qmm, the low-bit

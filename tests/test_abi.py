@@ -47,6 +47,7 @@ def lib():
     lib.q4a_gemv_inject_rmsnorm_grouped.argtypes = [P, P, P, P, P, P, P, P, P, F, F, I32, I32, I64, I64, P]
     lib.q4a_debug_withhold_stage.argtypes = [I32]
     lib.q4a_gemv_kernel_choice.argtypes = [P, P, I32, I64, I64]
+    lib.q4a_gemv_experts_gate_up_silu.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I64, I64, I64, P]
     lib.q4a_gemv_experts_lowbit.argtypes = [P, I32, P, P, P, P, P, I32, P, P, P, I32, I32, I64, I64, I64, P]
     lib.q4a_check_device_error.argtypes = [P]
     lib.q4a_last_cuda_error.restype = I32
@@ -425,6 +426,28 @@ def test_withhold_stage_hook_arguments(lib):
     assert lib.q4a_debug_withhold_stage(-2) == SHAPE
     assert lib.q4a_debug_withhold_stage(3) == OK
     assert lib.q4a_debug_withhold_stage(-1) == OK     # clears the request
+
+
+def test_experts_gate_up_silu_rejections(lib):
+    A = 0x1000
+    f = lib.q4a_gemv_experts_gate_up_silu
+    ids = np.array([0, 1], np.int32)
+    offs = np.array([0, 2, 3], np.int32)
+    pi, po = ctypes.c_void_p(ids.ctypes.data), ctypes.c_void_p(offs.ctypes.data)
+    ok = dict(h=A, w=A, s=A, b=A, x=A, xr=None, ids=pi, offs=po, na=2, ne=4, nr=3, inter=640, ind=2048)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["h"], a["w"], a["s"], a["b"], a["x"], a["xr"], a["ids"], a["offs"], a["na"], a["ne"], a["nr"],
+                 a["inter"], a["ind"], None)
+
+    assert call(h=None) == NULL and call(ids=None) == NULL
+    assert call(inter=8) == SHAPE                  # inter % 16
+    assert call(inter=648) == SHAPE
+    assert call(nr=4) == SHAPE                     # token_offsets[-1] != n_rows
+    assert call(h=A + 8) == ALIGN                  # h 16-byte aligned
+    assert call(ind=2048 + 64) == UNSUP            # in_dim % 512
+    assert call(s=A + 2) == UNSUP                  # scales must be 16-byte aligned for the fused form
 
 
 def test_experts_lowbit_rejections(lib):
