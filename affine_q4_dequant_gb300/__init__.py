@@ -127,14 +127,15 @@ def _ptrs(*specs):
     """Device pointers for specs (tensor, name, dtypes, shape); a spec may be None (a NULL
     pointer). Every shape is checked first, then dtypes, CUDA residency, contiguity and the
     device: a mis-shaped buffer would be read or written past its end by the kernels, so it is
-    refused here, before anything launches."""
+    refused here, before anything launches. (Plain comparisons and C-level tensor queries: this
+    runs on every call.)"""
     for sp in specs:
         if sp is None:
             continue
         t, name, _, shape = sp
         if not isinstance(t, torch.Tensor):
             raise TypeError(f"{name} must be a CUDA tensor")
-        if shape is not None and tuple(t.shape) != tuple(int(v) for v in shape):
+        if shape is not None and t.shape != shape:
             raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(int(v) for v in shape)}")
     dev = None
     out = []
@@ -145,17 +146,17 @@ def _ptrs(*specs):
         t, name, dtypes, _ = sp
         if dtypes is not None and t.dtype not in dtypes:
             raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
-        if not t.is_cuda:
+        d = t.get_device()
+        if d < 0:
             raise TypeError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
         if dev is None:
             dev = torch.cuda.current_device()
-        if t.device.index != dev:
+        if d != dev:
             raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
         out.append(t.data_ptr())
     return out
-
 
 def _dims(t: torch.Tensor, name: str, ndim: int = 2):
     if not isinstance(t, torch.Tensor):

@@ -1368,8 +1368,32 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
 
 // One op of a launch from its description: the tensor maps of its codes (and 3-bit lowest
 // bits), of its scales and biases in the chosen fetch mode, and its shape and schedule.
-q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_mode, int sb_tiles, uint32_t sb_pitch) {
-    if (!encode_fn()) return Q4A_ERR_UNSUPPORTED;
+struct OpMapKey {
+    const void* w;
+    const void* w_lo;
+    const void* s;
+    const void* b;
+    int64_t rows, in_dim;
+    int32_t cb, sb_mode;
+    bool operator==(const OpMapKey& k) const { return memcmp(this, &k, sizeof(*this)) == 0; }
+};
+struct OpMapKeyHash {
+    size_t operator()(const OpMapKey& k) const {
+        const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+        uint64_t h = 1469598103934665603ull;   // FNV-1a over the key's bytes
+        for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ p[i]) * 1099511628211ull;
+        return (size_t)h;
+    }
+};
+struct OpMaps {
+    CUtensorMap w[kNumMaps], lo[kNumMaps], s[kNumMaps], b[kNumMaps], s1, b1;
+};
+std::mutex g_opmap_mu;
+std::unordered_map<OpMapKey, OpMaps, OpMapKeyHash> g_opmaps;
+
+// Every tensor map an op may use: codes (and the 3-bit lowest bits) for each row-block height,
+// and the scales and biases in the chosen fetch mode.
+q4a_status encode_op_maps(GemvOp& o, const GemvLaunch& L, int sb_mode) {
     auto enc = encode_tiled_cached;
     const int cb = L.code_bits;
     const int G = (int)(L.in_dim / kGroup);
@@ -1395,6 +1419,79 @@ q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_
             if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
         }
     }
+    if (sb_mode == kSbTma) {
+        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
+        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
+        for (int i = 0; i < kNumMaps; ++i) {
+            const cuuint32_t box[2] = {64u, (cuuint32_t)(16 * (i + 1))};
+            for (int k = 0; k < 2; ++k) {
+                CUresult r = enc(k ? &o.tmap_b[i] : &o.tmap_s[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t*>(k ? L.b : L.s), sdims, sstrides, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+            }
+        }
+    }
+    if (sb_mode == kSbRaw) {
+        const cuuint64_t rdims[1] = {(cuuint64_t)(L.tensor_rows * G)};
+        const cuuint64_t rstrides[1] = {0};
+        const cuuint32_t rbox[1] = {(cuuint32_t)kRawBox};
+        for (int k = 0; k < 2; ++k) {
+            CUresult r = enc(k ? &o.tmap_b1 : &o.tmap_s1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1,
+                             const_cast<uint16_t*>(k ? L.b : L.s), rdims, rstrides, rbox, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+        }
+    }
+    return Q4A_OK;
+}
+
+q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_mode, int sb_tiles, uint32_t sb_pitch) {
+    if (!encode_fn()) return Q4A_ERR_UNSUPPORTED;
+    // The tensor maps of this matrix and fetch mode, encoded once and reused: a call's host
+    // time is otherwise dominated by looking up ~18 maps one at a time.
+    OpMapKey key;
+    memset(&key, 0, sizeof(key));
+    key.w = L.w;
+    key.w_lo = L.w_lo;
+    key.s = L.s;
+    key.b = L.b;
+    key.rows = L.tensor_rows;
+    key.in_dim = L.in_dim;
+    key.cb = L.code_bits;
+    key.sb_mode = sb_mode;
+    bool cached = false;
+    {
+        std::lock_guard<std::mutex> lock(g_opmap_mu);
+        auto it = g_opmaps.find(key);
+        if (it != g_opmaps.end()) {
+            const OpMaps& m = it->second;
+            memcpy(o.tmap_w, m.w, sizeof(m.w));
+            memcpy(o.tmap_lo, m.lo, sizeof(m.lo));
+            memcpy(o.tmap_s, m.s, sizeof(m.s));
+            memcpy(o.tmap_b, m.b, sizeof(m.b));
+            o.tmap_s1 = m.s1;
+            o.tmap_b1 = m.b1;
+            cached = true;
+        }
+    }
+    if (!cached) {
+        const q4a_status st = encode_op_maps(o, L, sb_mode);
+        if (st != Q4A_OK) return st;
+        OpMaps m;
+        memcpy(m.w, o.tmap_w, sizeof(m.w));
+        memcpy(m.lo, o.tmap_lo, sizeof(m.lo));
+        memcpy(m.s, o.tmap_s, sizeof(m.s));
+        memcpy(m.b, o.tmap_b, sizeof(m.b));
+        m.s1 = o.tmap_s1;
+        m.b1 = o.tmap_b1;
+        std::lock_guard<std::mutex> lock(g_opmap_mu);
+        if (g_opmaps.size() >= 4096) g_opmaps.clear();   // a bound for callers that churn buffers
+        g_opmaps.emplace(key, m);
+    }
+    const int G = (int)(L.in_dim / kGroup);
     o.s = L.s;
     o.b = L.b;
     o.x = L.x;
@@ -1425,32 +1522,6 @@ q4a_status fill_op(GemvOp& o, const GemvLaunch& L, int gs, int mt_units, int sb_
     o.rms = L.rmsnorm ? 1 : 0;
     o.fg = L.fused_gate_up ? 1 : 0;
     o.withhold_stage = L.withhold_stage;
-    if (sb_mode == kSbTma) {
-        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)L.tensor_rows};
-        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
-        for (int i = 0; i < kNumMaps; ++i) {
-            const cuuint32_t box[2] = {64u, (cuuint32_t)(16 * (i + 1))};
-            for (int k = 0; k < 2; ++k) {
-                CUresult r = enc(k ? &o.tmap_b[i] : &o.tmap_s[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 const_cast<uint16_t*>(k ? L.b : L.s), sdims, sstrides, box, estr,
-                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-            }
-        }
-    }
-    if (sb_mode == kSbRaw) {
-        const cuuint64_t rdims[1] = {(cuuint64_t)(L.tensor_rows * G)};
-        const cuuint64_t rstrides[1] = {0};
-        const cuuint32_t rbox[1] = {(cuuint32_t)kRawBox};
-        for (int k = 0; k < 2; ++k) {
-            CUresult r = enc(k ? &o.tmap_b1 : &o.tmap_s1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 1,
-                             const_cast<uint16_t*>(k ? L.b : L.s), rdims, rstrides, rbox, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-        }
-    }
     return Q4A_OK;
 }
 
