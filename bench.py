@@ -779,33 +779,48 @@ def per_config(q4a, torch, reps=40):
 
 
 def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
-    """Public API, host buffers: every step copies each NB's activations in from pinned
-    memory, runs one decode-layer MLP per NB through the binding (eager launches, no
-    graph), and copies the down projection's output back."""
-    host_in, host_out = {}, {}
+    """Public API, host buffers: every step copies all NBs' activations in from pinned memory
+    (one copy of one packed buffer), runs one decode-layer MLP per NB through the binding
+    (eager launches, no graph; outputs into preallocated device buffers), and copies the down
+    projections' outputs back (one copy)."""
+    parts_in, parts_out = [], []
     for nb in nbs:
         a = wl.normal_f32(wl.DENSE_GATE_UP, wl.T_A, (nb, HIDDEN))
         ga = wl.normal_f32(wl.DENSE_DOWN, wl.T_A, (nb, DOWN_IN))
         gb = wl.normal_f32(wl.DENSE_DOWN, wl.T_B, (nb, DOWN_IN))
-        host_in[nb] = (torch.from_numpy(a).pin_memory(),
-                       torch.from_numpy(np.concatenate([ga, gb], axis=1)).pin_memory())
-        host_out[nb] = torch.empty((nb, DOWN_OUT), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * 4 for nb in nbs for t in host_in[nb])
-    d2h = sum(host_out[nb].numel() * 4 for nb in nbs)
+        parts_in.append((nb, a, np.concatenate([ga, gb], axis=1)))
+        parts_out.append((nb, nb * DOWN_OUT))
+    flat_in = np.concatenate([np.concatenate([a.ravel(), g.ravel()]) for _, a, g in parts_in]).astype(np.float32)
+    host_in = torch.from_numpy(flat_in).pin_memory()
+    host_out = torch.empty(sum(n for _, n in parts_out), dtype=torch.float32).pin_memory()
+    dev_in = torch.empty(host_in.numel(), dtype=torch.float32, device=dev)
+    dev_out = torch.empty(host_out.numel(), dtype=torch.float32, device=dev)
+    views, off, ooff = [], 0, 0
+    for (nb, a, g), (_, n_out) in zip(parts_in, parts_out):
+        va = dev_in[off:off + a.size].view(nb, HIDDEN)
+        off += a.size
+        vg = dev_in[off:off + g.size].view(nb, 2 * DOWN_IN)
+        off += g.size
+        vo = dev_out[ooff:ooff + n_out].view(nb, DOWN_OUT)
+        ooff += n_out
+        h = torch.empty((nb, INTER2 // 2), dtype=torch.float16, device=dev)
+        x_dn = torch.empty((nb, DOWN_IN), dtype=torch.float16, device=dev)
+        views.append((va, vg, vo, h, x_dn))
+    h2d = host_in.numel() * 4
+    d2h = host_out.numel() * 4
     L = len(layers)
 
     def one(k):
         ly = layers[k % L]
         with torch.cuda.stream(stream):
-            for nb in nbs:
-                a = host_in[nb][0].to(dev, non_blocking=True)
-                gu_dn = host_in[nb][1].to(dev, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            for va, vg, vo, h, x_dn in views:
                 w, s, b = ly["gu"]
-                q4a.gemv_rmsnorm_gate_up_silu(w, s, b, a, ly["norm_w"], eps=1e-6, stream=stream)
-                x_dn, _ = q4a.silu_mul_xsum(gu_dn, want_hsum=False, stream=stream)
+                q4a.gemv_rmsnorm_gate_up_silu(w, s, b, va, ly["norm_w"], eps=1e-6, out=h, stream=stream)
+                q4a.silu_mul_xsum(vg, h=x_dn, want_hsum=False, stream=stream)
                 w, s, b = ly["dn"]
-                y_dn = q4a.gemv(w, s, b, x_dn, stream=stream)
-                host_out[nb].copy_(y_dn, non_blocking=True)
+                q4a.gemv(w, s, b, x_dn, out=vo, stream=stream)
+            host_out.copy_(dev_out, non_blocking=True)
         stream.synchronize()
 
     for k in range(2):
