@@ -187,17 +187,30 @@ def oracle_sample(seconds_target: float = 12.0):
 
 
 def host_info():
-    """The host's logical core count and CPU model (the oracle uses one of the cores)."""
-    model = None
+    """The host's logical core count and CPU model (the oracle uses one of the cores). Arm hosts
+    list no model name in /proc/cpuinfo, only the implementer and part numbers; those are
+    reported, with the core's name for the parts known here."""
+    model, impl, part = None, None, None
+    arm_parts = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+                 ("0x41", "0xd0c"): "Arm Neoverse-N1", ("0x41", "0xd49"): "Arm Neoverse-N2"}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware") and ":" in line:
-                    model = line.split(":", 1)[1].strip()
-                    break
+                if ":" not in line:
+                    continue
+                key, val = (t.strip() for t in line.split(":", 1))
+                key = key.lower()
+                if key in ("model name", "cpu model", "hardware") and not model:
+                    model = val
+                elif key == "cpu implementer" and impl is None:
+                    impl = val.lower()
+                elif key == "cpu part" and part is None:
+                    part = val.lower()
     except Exception:
         pass
+    if not model and impl and part:
+        name = arm_parts.get((impl, part))
+        model = f"{name + ' ' if name else ''}(CPU implementer {impl}, part {part})"
     if not model:
         import platform
 
