@@ -551,9 +551,10 @@ __device__ __noinline__ void sb_plain_copy(const GemvOp& p, uint8_t* sdst, int64
 // Before the CTA exits, lane 0 waits for every copy it issued and no consumer waited for
 // (after an abort): the last `S` ring stages (bit k of st_bits: stage it - 1 - k), the last
 // `nsb` scale/bias fetches and the raw buffers' latest fills.
+template <int kRawBufs>
 __device__ __noinline__ void drain_copies(const uint64_t* full_b, int S, int it, uint32_t st_bits, const uint64_t* sbfull_b,
-                                         int nsb, int blk, uint32_t sb_bits, const uint64_t* rawfull_b, int raw_rb0,
-                                         int raw_rb1) {
+                                         int nsb, int blk, uint32_t sb_bits, const uint64_t* rawfull_b,
+                                         int raw_rb0, int raw_rb1, int raw_rb2) {
     int slot = (it - 1) % S, round = (it - 1) / S;
 #pragma unroll 1
     for (int k = 0; k < S && k < it; ++k) {
@@ -569,8 +570,9 @@ __device__ __noinline__ void drain_copies(const uint64_t* full_b, int S, int it,
             const int q = blk - 1 - k;
             mbar_drain(smem_addr(sbfull_b + q % nsb), (uint32_t)(q / nsb) & 1u);
         }
-    if (raw_rb0 >= 0) mbar_drain(smem_addr(rawfull_b), (uint32_t)(raw_rb0 >> 1) & 1u);
-    if (raw_rb1 >= 0) mbar_drain(smem_addr(rawfull_b + 1), (uint32_t)(raw_rb1 >> 1) & 1u);
+    if (raw_rb0 >= 0) mbar_drain(smem_addr(rawfull_b), ((uint32_t)raw_rb0 / (uint32_t)kRawBufs) & 1u);
+    if (raw_rb1 >= 0) mbar_drain(smem_addr(rawfull_b + 1), ((uint32_t)raw_rb1 / (uint32_t)kRawBufs) & 1u);
+    if (kRawBufs > 2 && raw_rb2 >= 0) mbar_drain(smem_addr(rawfull_b + 2), ((uint32_t)raw_rb2 / (uint32_t)kRawBufs) & 1u);
 }
 
 // Raw mode, consumer side: rearrange a row block's raw [rows][groups] scales and biases into
@@ -613,13 +615,20 @@ __device__ __noinline__ void raw_rearrange(const GemvOp& p, const uint16_t* rs_,
 // MTT: tiles per row block (0: the default for NT). Rows that a short row block lacks still
 // cost their mma work (the tile loop is unrolled for a fixed tile count), so launches whose
 // clusters get only a few tiles use a kernel built for that many.
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
+// RAWD (raw scale mode, 4-bit routed experts): the consumers read each row block's scales and
+// biases straight from the raw staging buffer ([rows][groups] bf16, as TMA copied it) instead of
+// first rearranging them into the swizzled layout; a buffer is handed back after the row
+// block's bias term.
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false,
+          bool RAWD = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams<MAXSEG> pp) {
     constexpr int NTOK = NT * 8;
     constexpr int MT = MTT ? MTT : tiles_per_block(NT);  // tiles per row block
     constexpr int TPW = MT;                  // tiles per consumer warp: all of the row block
     static_assert(MT >= 1 && MT <= kNumMaps, "row blocks of at most kNumMaps tiles: one tensor map per height");
+    static_assert(!RAWD || (CB == 4 && !FG && !RMS), "direct raw reads: plain 4-bit products");
+    constexpr int kRawBufs = raw_bufs(RAWD);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -637,9 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty_b = bars + S;         // [S]  every consumer warp is done with a stage
     uint64_t* sbfull_b = bars + 2 * S;    // [2]  a row block's scales/biases landed
     uint64_t* sbempty_b = bars + 2 * S + 2;  // [2] every consumer warp is done with them
-    uint64_t* rawfull_b = bars + 2 * S + 4;  // [2] raw mode: a row block's raw scales/biases landed
-    uint64_t* rawempty_b = bars + 2 * S + 6; // [2] raw mode: the consumers rearranged them
-    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * S + 8);
+    uint64_t* rawfull_b = bars + 2 * S + 4;  // [kRawBufs] raw mode: a row block's raw scales/biases landed
+    uint64_t* rawempty_b = rawfull_b + kRawBufs;   // [kRawBufs] raw mode: the consumers are done with them
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(rawempty_b + kRawBufs);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -665,8 +674,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 2; ++q) {
             mbar_init(smem_addr(sbfull_b + q), 1);
             mbar_init(smem_addr(sbempty_b + q), kConsumerWarps);
+        }
+        for (int q = 0; q < kRawBufs; ++q) {
             mbar_init(smem_addr(rawfull_b + q), 1);
-            mbar_init(smem_addr(rawempty_b + q), 1);
+            mbar_init(smem_addr(rawempty_b + q), RAWD ? kConsumerWarps : 1);
         }
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -687,8 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exits: after an abort the consumers no longer wait for them. Once the abort flag is
         // set no new copy is issued; the control flow (and every cluster barrier) stays as is.
         uint32_t st_bits = 0, sb_bits = 0;
-        int raw_rb[2] = {-1, -1};   // raw mode: the row block whose scales each buffer received
-        uint8_t* raw = smem + L.raw;   // raw mode: [2 buffers][scales | biases][raw_elems] bf16
+        static_assert(kRawBufs <= 3, "one register per raw buffer below");
+        int raw_rb0 = -1, raw_rb1 = -1, raw_rb2 = -1;   // raw mode: the row block each buffer received
+        uint8_t* raw = smem + L.raw;   // raw mode: [kRawBufs buffers][scales | biases][raw_elems] bf16
         const GemvOp& p = pp.op;
         const bool fg = FG && p.fg;
         const OpRange R0 = op_range(p, crank, cid, pp.n_clusters);
@@ -699,7 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         auto raw_issue_to = [&](const Job& jb, int buf, int rb) {
             if (lane != 0 || *abort_flag) return;
-            if (buf) raw_rb[1] = rb; else raw_rb[0] = rb;
+            if constexpr (kRawBufs == 2) {
+                if (buf) raw_rb1 = rb; else raw_rb0 = rb;
+            } else {
+                if (buf == 0) raw_rb0 = rb;
+                else if (buf == 1) raw_rb1 = rb;
+                else raw_rb2 = rb;
+            }
             raw_issue(p, pp.seg[jb.seg], jb.tile, jb.ntile, raw + (size_t)buf * 2u * L.raw_elems * 2u, L.raw_elems,
                       smem_addr(rawfull_b + buf));
         };
@@ -733,14 +751,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else if (p.sb_mode == kSbRaw) {
                     // the next row block's raw scales/biases, into the buffer the consumers
-                    // finished rearranging a row block ago (they rearrange this one)
+                    // released kRawBufs - 1 row blocks ago
                     int t2 = t;
                     Job jn;
                     if (next_job(p, t2, t_end, jn)) {
-                        const int nbuf = (blk + 1) & 1;
-                        if (blk + 1 >= 2)
-                            mbar_wait(smem_addr(rawempty_b + nbuf), (uint32_t)((blk + 1) / 2 - 1) & 1u, abort_flag);
-                        raw_issue_to(jn, nbuf, blk + 1);
+                        if constexpr (kRawBufs == 2) {
+                            const int nbuf = (blk + 1) & 1;
+                            if (blk + 1 >= 2)
+                                mbar_wait(smem_addr(rawempty_b + nbuf), (uint32_t)((blk + 1) / 2 - 1) & 1u, abort_flag);
+                            raw_issue_to(jn, nbuf, blk + 1);
+                        } else {
+                            const uint32_t nb1 = (uint32_t)blk + 1u;
+                            const int nbuf = (int)(nb1 % (uint32_t)kRawBufs);
+                            if (nb1 >= (uint32_t)kRawBufs)
+                                mbar_wait(smem_addr(rawempty_b + nbuf), (nb1 / (uint32_t)kRawBufs - 1u) & 1u, abort_flag);
+                            raw_issue_to(jn, nbuf, blk + 1);
+                        }
                     }
                 } else {
                     sb_plain_copy(p, sdst, trow0, rows_valid, kg0, gsz, lane);
@@ -793,7 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++blk;
         }
         if (lane == 0)
-            drain_copies(full_b, S, it, st_bits, sbfull_b, (int)L.n_sb, blk, sb_bits, rawfull_b, raw_rb[0], raw_rb[1]);
+            drain_copies<kRawBufs>(full_b, S, it, st_bits, sbfull_b, (int)L.n_sb, blk, sb_bits, rawfull_b, raw_rb0,
+                                   raw_rb1, raw_rb2);
         __syncwarp();
         if (pending) cluster_wait();
     } else {
@@ -876,16 +903,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) acc[mi][nt][k] = 0.f;
 
             const int q = blk % (int)L.n_sb;
+            const int rbuf = kRawBufs == 2 ? (blk & 1) : (int)((uint32_t)blk % (uint32_t)kRawBufs);
+            // RAWD: this lane's scale of (row g, group wg) of the row block's first tile in the raw
+            // buffer, and the buffer's biases
+            uint32_t raw_sl = 0, raw_b = 0;
+            int raw_off = 0;
             if (p.sb_mode == kSbRaw) {
-                // Rearrange the row block's raw scales and biases (every warp of the previous
-                // row block has passed its epilogue barrier, so the buffer is free).
-                mbar_wait(smem_addr(rawfull_b + (blk & 1)), (uint32_t)(blk >> 1) & 1u, abort_flag);
-                const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(smem + L.raw + (size_t)(blk & 1) * 2u * L.raw_elems * 2u);
+                mbar_wait(smem_addr(rawfull_b + rbuf),
+                          (kRawBufs == 2 ? (uint32_t)(blk >> 1) : (uint32_t)blk / (uint32_t)kRawBufs) & 1u, abort_flag);
+                const uint16_t* rs_ = reinterpret_cast<const uint16_t*>(smem + L.raw + (size_t)rbuf * 2u * L.raw_elems * 2u);
                 const int64_t e0 = ((int64_t)sg.row0 + (int64_t)j.tile * 16) * p.groups;
-                const int rv = (int)llmin((int64_t)j.ntile * 16, p.out_dim - (int64_t)j.tile * 16);
-                raw_rearrange(p, rs_, L.raw_elems, sbuf + (size_t)q * L.sb_buf, e0, gsz, rv, ctid);
-                consumer_sync();
-                if (ctid == 0) mbar_arrive(smem_addr(rawempty_b + (blk & 1)));
+                raw_off = (int)(e0 - (e0 & ~(int64_t)7));
+                if constexpr (RAWD) {
+                    raw_b = smem_addr(rs_) + L.raw_elems * 2u;
+                    raw_sl = smem_addr(rs_) + 2u * (uint32_t)(raw_off + g * gsz + wg);
+                } else {
+                    // Rearrange the row block's raw scales and biases (every warp of the previous
+                    // row block has passed its epilogue barrier, so the buffer is free).
+                    const int rv = (int)llmin((int64_t)j.ntile * 16, p.out_dim - (int64_t)j.tile * 16);
+                    raw_rearrange(p, rs_, L.raw_elems, sbuf + (size_t)q * L.sb_buf, e0, gsz, rv, ctid);
+                    consumer_sync();
+                    if (ctid == 0) mbar_arrive(smem_addr(rawempty_b + rbuf));
+                }
             } else {
                 mbar_wait(smem_addr(sbfull_b + q), (uint32_t)(blk / (int)L.n_sb) & 1u, abort_flag);
             }
@@ -935,16 +974,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bf[nt][4] = q1.x; bf[nt][5] = q1.y; bf[nt][6] = q1.z; bf[nt][7] = q1.w;
                     }
                     // group gl = 8ks + wg: chunk ks/8, granule (ks & 7) ^ g, element wg
-                    const uint32_t sa = s_blk + (uint32_t)((ks >> 3) * p.sb_tiles * kTileBytes) +
-                                        ((uint32_t)((ks & 7) ^ g) << 4);
+                    // (RAWD: row-major [rows][gsz] from the row block's first element)
+                    const uint32_t sa = RAWD ? raw_sl + (uint32_t)(16 * ks)
+                                             : s_blk + (uint32_t)((ks >> 3) * p.sb_tiles * kTileBytes) +
+                                                   ((uint32_t)((ks & 7) ^ g) << 4);
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
                         // The mma partial sums are sum(q x) * 2^-24; s multiplies them as is and
                         // the result is multiplied by 2^24 once at the end (no scale overflows).
                         // Low-bit codes: the steps compute sum(q x) / (4 or 2); the scale restores it.
                         constexpr float kq = CB == 4 ? 1.0f : (CB == 2 ? 4.0f : 2.0f);
-                        const float s0 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes)));
-                        const float s1 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes + 1024)));
+                        float s0, s1;
+                        if constexpr (RAWD) {   // next tile: 16 rows on; row + 8: 8 rows on
+                            s0 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * 32 * gsz)));
+                            s1 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * 32 * gsz + 16 * gsz)));
+                        } else {
+                            s0 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes)));
+                            s1 = kq * bf16_to_f32(lds_u16(sa + (uint32_t)(mi * kTileBytes + 1024)));
+                        }
                         // h[a][jj]: mma step jj's A register a (a0/a2: row g, a1/a3: row g+8)
                         uint32_t h[4][4];
                         if constexpr (CB == 4) {
@@ -1027,7 +1074,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int mi = 0; mi < TPW; ++mi) {
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4(boff + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
+                        if constexpr (RAWD) {
+                            // A fragment of m16n8k16: rows g, g + 8 x groups 16gb + 2tq (+1), + 8 (+9)
+                            auto bpair = [&](int row, int gl) -> uint32_t {
+                                const uint32_t e = raw_b + 2u * (uint32_t)(raw_off + (mi * 16 + row) * gsz + gl);
+                                const uint32_t lo = gl < gsz ? lds_u16(e) : 0u;
+                                const uint32_t hi = gl + 1 < gsz ? lds_u16(e + 2u) : 0u;
+                                return lo | (hi << 16);
+                            };
+                            const int gl0 = gb * 16 + 2 * tq;
+                            a0 = bpair(g, gl0);
+                            a1 = bpair(g + 8, gl0);
+                            a2 = bpair(g, gl0 + 8);
+                            a3 = bpair(g + 8, gl0 + 8);
+                        } else {
+                            ldsm_x4(boff + (uint32_t)(mi * kTileBytes), a0, a1, a2, a3);
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             mma_bf16(acc[mi][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
@@ -1051,6 +1113,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(sbempty_b + q));
+            if constexpr (RAWD) {
+                if (lane == 0) mbar_arrive(smem_addr(rawempty_b + rbuf));   // the raw buffer is free
+            }
 
             // ---- end of the row block: reduce over group slots, then over the cluster ----
             const int R = j.ntile * 16;
@@ -1254,9 +1319,10 @@ std::mutex g_cache_mu;
 std::map<OccKey, int> g_occ_cache;
 std::map<std::pair<const void*, int>, uint32_t> g_smem_set;
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false,
+          bool RAWD = false>
 int occupancy_clusters(int cluster, uint32_t smem_bytes) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ, RAWD>;
     const void* fn = reinterpret_cast<const void*>(kern);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1333,9 +1399,10 @@ int cluster_capacity(int nt, bool rms, bool experts, int cluster, uint32_t smem_
                    : cluster_capacity_t<kDenseMaxSeg>(nt, rms, cluster, smem_bytes, cb);
 }
 
-template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false>
+template <int NT, bool RMS, int MAXSEG, int CB = 4, bool FG = false, int MTT = 0, bool XF = false, bool INJ = false,
+          bool RAWD = false>
 q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStream_t stream) {
-    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>;
+    auto kern = gemv_kernel<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ, RAWD>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1349,7 +1416,7 @@ q4a_status launch_variant(GemvParams<MAXSEG>& prm, uint32_t smem_bytes, cudaStre
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ>(prm.cluster, smem_bytes);
+    int max_clusters = occupancy_clusters<NT, RMS, MAXSEG, CB, FG, MTT, XF, INJ, RAWD>(prm.cluster, smem_bytes);
     if (max_clusters <= 0) return Q4A_ERR_CUDA;
     prm.n_clusters = max_clusters < prm.op.n_tiles ? max_clusters : prm.op.n_tiles;
     cfg.gridDim = dim3((unsigned)(prm.n_clusters * prm.cluster), 1, 1);
@@ -1545,6 +1612,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     // schedule units per row block: tiles, or (fused) gate|up tile pairs
     int mt_units = fg ? mt / 2 : mt;
     const int G = (int)(L.in_dim / kGroup);
+    // 4-bit routed experts in raw scale mode read the raw buffers directly (no rearrangement)
+    const bool rawd = MAXSEG != kDenseMaxSeg && cb == 4 && !fg && !L.rmsnorm && !L.x_f32;
 
     // Cluster size (K split). Candidates are powers of two whose K-slice leaves room for a
     // ring of at least 3 stages (a deeper ring matters less than avoiding the split: each
@@ -1578,14 +1647,16 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         if (c > 1 && sbm_full != kSbTma) return false;
         if (c > 1 && (int64_t)g * (c - 1) >= G) return false;
         if (xfrag_bytes(g, ntm) > (uint32_t)kXFragBudget) return false;
-        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c), cb).total + 1024) <= di.max_smem_optin;
+        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c), cb, 0, rawd).total + 1024) <=
+               di.max_smem_optin;
     };
     int C = 0;
     for (int c = 1; c <= 8; c *= 2) {
         if (!fits(c, 3)) continue;
         if (C == 0) C = c;                       // smallest that fits at all
         const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
-                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb).total + 1024, cb, fg);
+                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb, 0, rawd).total + 1024,
+                                       cb, fg);
         if (q <= 0) continue;
         if (tile_work >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
             C = c;
@@ -1610,7 +1681,7 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     int stages = 8;
     while (stages > 2 && !fits(C, stages)) --stages;
     if (!fits(C, stages)) return Q4A_ERR_UNSUPPORTED;
-    const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C), cb);
+    const SmemLayout lay = smem_layout(nt, mt, stages, gs, ntm, sbmode(C), sbufs(C), cb, 0, rawd);
     if (L.plan_only) return Q4A_OK;
 
     static thread_local GemvParams<MAXSEG> prm;   // large: keep it off the stack
@@ -1659,6 +1730,11 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         }
     }
     if constexpr (MAXSEG != kDenseMaxSeg) {
+        if (rawd && sbmode(C) == kSbRaw) {   // short rows: scales and biases read in place
+            if (nt == 1) return launch_variant<1, false, MAXSEG, 4, false, 0, false, false, true>(prm, smem_bytes, stream);
+            if (nt == 2) return launch_variant<2, false, MAXSEG, 4, false, 0, false, false, true>(prm, smem_bytes, stream);
+            return launch_variant<4, false, MAXSEG, 4, false, 0, false, false, true>(prm, smem_bytes, stream);
+        }
         if (fg) {   // routed experts' fused gate|up with the activation in the epilogue
             if (nt == 1) return launch_variant<1, false, MAXSEG, 4, true>(prm, smem_bytes, stream);
             if (nt == 2) return launch_variant<2, false, MAXSEG, 4, true>(prm, smem_bytes, stream);

@@ -28,6 +28,9 @@ constexpr int kDenseTcTallRows = 152 * 256;   // and from kDenseTcTallMinRows ro
 constexpr int kDenseTcTallMinRows = 13;
 constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
 constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation segments per row
+// raw scale mode: row blocks of raw scales/biases in flight (3 where the consumers read them in
+// place for a whole row block, 2 where they rearrange them first)
+__host__ __device__ constexpr int raw_bufs(bool raw_direct) { return raw_direct ? 3 : 2; }
 
 // How the producer fetches a row block's scales and biases into shared memory. Both modes
 // write the same layout: [64-group chunk][row][128 bytes], 16-byte granule u of row r
@@ -83,7 +86,7 @@ constexpr uint32_t kLoTileBytes = 16u * 64u;
 
 __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, int gs, int ntok_max,
                                                   int sb_mode, int sb_bufs, int code_bits = 4,
-                                                  uint32_t sb_pitch_bytes = 0) {
+                                                  uint32_t sb_pitch_bytes = 0, bool raw_direct = false) {
     SmemLayout L;
     const uint32_t ntok = 8u * nt, rows = 16u * mt;
     L.stage_bytes = (uint32_t)mt * (code_bits == 4 ? 2u : 1u) * kTileBytes +   // [box column][rows][128 B]
@@ -92,7 +95,9 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     L.xfrag = L.ring + (uint32_t)stages * L.stage_bytes;
     L.xsum = L.xfrag + align_up(xfrag_bytes(gs, ntok_max), 16);
     L.sb_pitch = sb_pitch_bytes ? sb_pitch_bytes : sb_bytes(sb_mode, gs, rows);   // scales, then biases
-    L.sb_buf = 2u * L.sb_pitch;
+    // raw_direct (raw mode only): the consumers read the raw buffers, no swizzled scale/bias buffers
+    raw_direct = raw_direct && sb_mode == kSbRaw;
+    L.sb_buf = raw_direct ? 0u : 2u * L.sb_pitch;
     L.xbias = align_up(L.xsum + (uint32_t)gs * ntok * 4u, 16);   // bf16 hi/lo group sums
     L.sb = align_up(L.xbias + (uint32_t)((gs + 15) / 16) * ntok_max * 64u, 1024);
     L.n_sb = (uint32_t)sb_bufs;                             // 2 when a CTA has several row blocks
@@ -102,9 +107,10 @@ __host__ __device__ inline SmemLayout smem_layout(int nt, int mt, int stages, in
     L.raw = align_up(L.ssq + 2u * ntok * (uint32_t)kMaxNormGroups * 4u, 128);   // sums, then factors
     // a row block's elements plus up to 7 in front (the box start is rounded down to 16 bytes)
     L.raw_elems = sb_mode == kSbRaw ? align_up(rows * (uint32_t)gs + 7u, (uint32_t)kRawBox) : 0u;
-    L.bars = align_up(L.raw + 2u * 2u * L.raw_elems * 2u, 8);
-    // full[stages] empty[stages] sbfull[2] sbempty[2] rawfull[2] rawempty[2], then the abort flag
-    L.total = L.bars + (2u * (uint32_t)stages + 8u) * 8u + 16u;
+    const uint32_t nrb = (uint32_t)raw_bufs(raw_direct);
+    L.bars = align_up(L.raw + nrb * 2u * L.raw_elems * 2u, 8);
+    // full[stages] empty[stages] sbfull[2] sbempty[2] rawfull[nrb] rawempty[nrb], then the abort flag
+    L.total = L.bars + (2u * (uint32_t)stages + 4u + 2u * nrb) * 8u + 16u;
     return L;
 }
 

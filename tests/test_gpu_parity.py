@@ -303,6 +303,26 @@ def test_experts_many_tokens_per_expert():
     assert_within_bound(y, y_ref, bound, "experts 40 rows")
 
 
+@pytest.mark.parametrize("in_dim,tokens", [(640, 1), (320, 12), (704, 20)])
+def test_experts_short_rows_scales_read_in_place(in_dim, tokens):
+    """Rows whose group count is not a multiple of 8 (10, 5 and 11 groups) take the raw scale
+    mode: each row block's scales and biases arrive as one contiguous [rows][groups] copy and
+    the consumers read them where they landed (odd group counts: 16-bit reads only). 48 experts
+    of 600 rows (a ragged last tile each) and 1 / 12 / 20 tokens per expert (one, two and four
+    8-row activation tiles) give every CTA several row blocks, so the three raw buffers cycle."""
+    n_exp, out_dim = 48, 600
+    packed, s, b = bank_case(n_exp, out_dim, in_dim, 24 + tokens)
+    n_x = 7
+    x = wl.normal_f16(94, 0, (n_x, in_dim))
+    rng = np.random.default_rng(95 + tokens)
+    ids = rng.permutation(n_exp).astype(np.int32)
+    offs = np.arange(n_exp + 1, dtype=np.int32) * tokens
+    x_rows = rng.integers(0, n_x, size=n_exp * tokens).astype(np.int32)
+    y = run_experts(packed, s, b, x, x_rows, ids, offs, n_exp, out_dim)
+    y_ref, bound = oracle.gemv_experts(packed, s, b, x, x_rows, ids, offs, n_exp, out_dim)
+    assert_within_bound(y, y_ref, bound, f"experts, {in_dim // 64} groups per row")
+
+
 def test_pack_then_gemv_back_to_back():
     """The GEMV streams weights without waiting for the previous kernel of the stream;
     q4a_pack must still be fully visible to a GEMV launched right after it. The same
