@@ -154,24 +154,25 @@ class ClockSampler:
 
 # ---- CPU baseline (the oracle as it stands) --------------------------------------------
 
-def oracle_sample(seconds_target: float = 12.0):
-    """Time the CPU oracle on a bounded sample of the same workload: the decode-layer
-    MLP at NB = 1 and 2 on a row sample of both projections (512 gate|up rows, 256
-    down rows), repeated until ~seconds_target. Returns (GB/s, description, cores)."""
+def oracle_sample(seconds_target: float = 12.0, nbs=(1, 2, 4, 8, 16)):
+    """Time the CPU oracle on a bounded sample of the same workload: the decode-layer MLP at
+    every NB of the step on a row sample of both projections (128 gate|up rows -- 64 gate, 64
+    up -- and 64 down rows), repeated until ~seconds_target. Returns (GB/s, description,
+    cores)."""
     import oracle
 
-    rows_gu, rows_dn = 512, 256
+    rows_gu, rows_dn = 128, 64
     qm_gu = wl.quant_matrix(wl.DENSE_GATE_UP, rows_gu, HIDDEN)
     qm_dn = wl.quant_matrix(wl.DENSE_DOWN, rows_dn, DOWN_IN)
     p_gu, p_dn = oracle.pack(qm_gu.codes), oracle.pack(qm_dn.codes)
     nw = wl.norm_weight(wl.DENSE_GATE_UP, wl.T_NORM_W, HIDDEN)
     total_bytes, t0, reps = 0.0, time.perf_counter(), 0
     while True:
-        for nb in (1, 2):
+        for nb in nbs:
             a = wl.normal_f32(wl.DENSE_GATE_UP, wl.T_A, (nb, HIDDEN))
             xn, _ = oracle.rmsnorm_f16(a, nw, eps=1e-6)
             y, _ = oracle.gemv(p_gu, qm_gu.scale, qm_gu.bias, xn)
-            h = oracle.silu_mul_f16(y.astype(np.float32))    # 256 gate rows, then 256 up rows
+            h = oracle.silu_mul_f16(y.astype(np.float32))    # 64 gate rows, then 64 up rows
             xd = wl.normal_f16(wl.DENSE_DOWN, wl.T_X, (nb, DOWN_IN))
             oracle.gemv(p_dn, qm_dn.scale, qm_dn.bias, xd)
             # the same accounting as layer_bytes, for the sampled rows
@@ -182,7 +183,8 @@ def oracle_sample(seconds_target: float = 12.0):
             break
     dt = time.perf_counter() - t0
     desc = (f"oracle decode-layer MLP on a row sample ({rows_gu} of {INTER2} gate|up rows, {rows_dn} of "
-            f"{DOWN_OUT} down rows) at NB=1,2, {reps} repetitions, {dt:.1f} s, single-threaded fp64")
+            f"{DOWN_OUT} down rows) at NB={','.join(str(v) for v in nbs)}, {reps} repetitions, {dt:.1f} s, "
+            f"single-threaded fp64")
     return total_bytes / dt / 1e9, desc, 1
 
 
@@ -225,7 +227,7 @@ def run_reference(args, rank, world):
     import oracle  # noqa: F401
     for i in range(args.warmup + args.steps):
         per = max(2.0, 60.0 / max(1, args.warmup + args.steps))
-        gbs, desc, cores = oracle_sample(seconds_target=per)
+        gbs, desc, cores = oracle_sample(seconds_target=per, nbs=tuple(int(v) for v in args.nbs.split(",")))
         if i >= args.warmup:
             times.append(gbs)
     value = statistics.mean(times)
@@ -435,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        gbs, desc, cores = oracle_sample(seconds_target=args.cpu_seconds)
+        gbs, desc, cores = oracle_sample(seconds_target=args.cpu_seconds, nbs=tuple(int(v) for v in args.nbs.split(",")))
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
                                 **host_info()}
     print(json.dumps(line), flush=True)
