@@ -816,9 +816,10 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
     for _, _, x in parts:
         hv[off:off + x.size * 2] = np.ascontiguousarray(x, np.uint16).view(np.uint8).ravel()
         off += x.size * 2
-    host_out = torch.empty(sum(nb * DOWN_OUT for nb in nbs), dtype=torch.float32).pin_memory()
+    # two pinned output buffers: step k + 1 is enqueued before the host reads step k's output
+    host_out = [torch.empty(sum(nb * DOWN_OUT for nb in nbs), dtype=torch.float32).pin_memory() for _ in range(2)]
     dev_in = torch.empty(host_in.numel(), dtype=torch.uint8, device=dev)
-    dev_out = torch.empty(host_out.numel(), dtype=torch.float32, device=dev)
+    dev_out = torch.empty(host_out[0].numel(), dtype=torch.float32, device=dev)
     views, fo, ho, oo = [], 0, n_f32 * 4, 0
     for nb, a, x in parts:
         va = dev_in[fo:fo + a.size * 4].view(torch.float32).view(nb, HIDDEN)
@@ -830,10 +831,14 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
         h = torch.empty((nb, INTER2 // 2), dtype=torch.float16, device=dev)
         views.append((va, vx, vo, h))
     h2d = host_in.numel()
-    d2h = host_out.numel() * 4
+    d2h = host_out[0].numel() * 4
     L = len(layers)
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    seen = []
 
-    def one(k):
+    def enqueue(k):
+        # step k: its inputs in, its kernels, its outputs out (stream order keeps the copies of
+        # consecutive steps apart from each other's kernels)
         ly = layers[k % L]
         with torch.cuda.stream(stream):
             dev_in.copy_(host_in, non_blocking=True)
@@ -842,15 +847,25 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
                 q4a.gemv_rmsnorm_gate_up_silu(w, s, b, va, ly["norm_w"], eps=1e-6, out=h, stream=stream)
                 w, s, b = ly["dn"]
                 q4a.gemv(w, s, b, vx, out=vo, stream=stream)
-            host_out.copy_(dev_out, non_blocking=True)
-        stream.synchronize()
+            host_out[k % 2].copy_(dev_out, non_blocking=True)
+            done[k % 2].record(stream)
+
+    def read(k):
+        # the host waits for step k and reads its outputs
+        done[k % 2].synchronize()
+        seen.append(float(host_out[k % 2][-1]))
 
     for k in range(2):
-        one(k)
+        enqueue(k)
+        read(k)
     t0 = time.perf_counter()
-    for k in range(steps):
-        one(k)
+    enqueue(0)
+    for k in range(1, steps):
+        enqueue(k)
+        read(k - 1)
+    read(steps - 1)
     dt = (time.perf_counter() - t0) / steps
+    assert all(v == v for v in seen), "non-finite output in the end-to-end steps"
     step_bytes = sum(sum(layer_bytes(nb)) for nb in nbs)
     # host cost of one call through the binding (argument checks, marshalling, the C ABI's
     # validation, planning and launch): back-to-back calls on a small product, no sync between
@@ -871,8 +886,10 @@ def e2e_measure(q4a, torch, layers, nbs, dev, stream, steps):
     return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "host_us_per_call": host_us,
             "note": "per NB per step the step's two kernels (fused RMSNorm + gate|up + silu*up, then the "
-                    "down projection), eager launches through the Python binding; host_us_per_call: wall "
-                    "time of one q4a.gemv call on the host (launch included)"}
+                    "down projection), eager launches through the Python binding; every step copies its "
+                    "inputs in and its outputs out, and the host reads each step's outputs while the next "
+                    "step runs (two steps in flight); host_us_per_call: wall time of one q4a.gemv call on "
+                    "the host (launch included)"}
 
 
 def main():
