@@ -226,7 +226,9 @@ def run_reference(args, rank, world):
     steps_bytes, times = [], []
     import oracle  # noqa: F401
     for i in range(args.warmup + args.steps):
-        per = max(2.0, 60.0 / max(1, args.warmup + args.steps))
+        # about a minute in all, whatever --steps and --warmup are (a repetition over every NB
+        # takes ~40-60 ms)
+        per = max(0.1, 60.0 / max(1, args.warmup + args.steps))
         gbs, desc, cores = oracle_sample(seconds_target=per, nbs=tuple(int(v) for v in args.nbs.split(",")))
         if i >= args.warmup:
             times.append(gbs)
