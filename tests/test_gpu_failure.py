@@ -58,3 +58,32 @@ def test_withheld_stage_times_out_and_the_next_call_is_clean(out_dim, in_dim, nb
     ref, bound = oracle.gemv(packed, s, b, x)
     worst = float((np.abs(y.cpu().numpy().astype(np.float64) - ref) / bound).max())
     assert worst <= 1.0, f"after the timeout: worst err/bound {worst:.3g}"
+
+
+def test_withheld_stage_routed_short_rows():
+    """The routed down projection's form: 640-wide rows whose scales and biases the consumers
+    read from the raw staging buffers (three in flight). 16 experts of 2048 rows give every CTA
+    three row blocks; every CTA misses its second weight stage (the 2-group second stage of its
+    first row block). The launch gives up its wait, drains its copies, reports Q4A_ERR_TIMEOUT,
+    and the next call on the stream matches the oracle."""
+    n_exp, out_dim, in_dim, per = 16, 2048, 640, 2
+    packed, s, b, x = case(n_exp * out_dim, in_dim, n_exp * per, 77)
+    w_d, s_d, b_d, x_d = dev(packed), dev(s), dev(b), dev(x)
+    ids = np.arange(n_exp, dtype=np.int32)[::-1].copy()
+    offs = np.arange(n_exp + 1, dtype=np.int32) * per
+    n_rows = int(offs[-1])
+    q4a.check_device_error()
+    q4a.debug_withhold_stage(1)
+    t0 = time.perf_counter()
+    q4a.gemv_experts(w_d, s_d, b_d, x_d, None, ids, offs, n_exp, out_dim)
+    with pytest.raises(q4a.Q4AError) as err:
+        q4a.check_device_error()
+    waited = time.perf_counter() - t0
+    assert err.value.status_name == "ERR_TIMEOUT"
+    assert waited < 30.0
+    y = torch.full((n_rows, out_dim), float("nan"), device=DEV)
+    q4a.gemv_experts(w_d, s_d, b_d, x_d, None, ids, offs, n_exp, out_dim, out=y)
+    q4a.check_device_error()
+    ref, bound = oracle.gemv_experts(packed, s, b, x, None, ids, offs, n_exp, out_dim)
+    worst = float((np.abs(y.cpu().numpy().astype(np.float64) - ref) / bound).max())
+    assert worst <= 1.0, f"after the timeout: worst err/bound {worst:.3g}"
