@@ -71,8 +71,10 @@ constexpr int kTcDqWarps = 4 * kTcUm * kTcDqSplit;
 constexpr int kTcWarpX = kTcWarpDq0 + kTcDqWarps;          // x-tile producer
 constexpr int kTcThreads = (kTcWarpX + 1) * 32;
 constexpr int kTcMaxN = 128;                // activation rows per launch (MMA N, TMEM budget)
-constexpr int kTcYCols = 16;                // activation rows per y store box (128 weight rows x 16 fp32)
-constexpr int kTcYBox = kTcM * kTcYCols * 4;   // 8 KB; two of them alternate
+constexpr int kTcYCols = 16;                // accumulator columns per TMEM load (tcgen05.ld 32x32b.x16)
+// y store boxes: 128 weight rows x YC activation rows fp32, two alternating; YC = 16, or 32 with one
+// accumulator set (N > 64), where the MMA waits for the epilogue to drain: half the box handoffs
+__host__ __device__ constexpr uint32_t tc_ybox_bytes(int yc) { return (uint32_t)kTcM * (uint32_t)yc * 4u; }
 constexpr int kTcEpiBarrier = 1;            // named barrier of the epilogue warps
 static_assert(kTcDqWarps * 32 == kTcUnitRows * kTcDqSplit, "kTcDqSplit dequantisation threads per unit row");
 static_assert(kTcDqSplit == 1 || kTcDqSplit == 2, "16-byte code chunks (32 weights, 16 TMEM columns) per thread");
@@ -83,7 +85,7 @@ struct TcLayout {
     uint32_t code_stage;
     uint32_t xr;          // x ring: xs stages of [kTcSG groups][n_pad rows][128 bytes]
     uint32_t x_stage;
-    uint32_t ybuf;        // 2 y store boxes [kTcYCols][kTcM] fp32
+    uint32_t ybuf;        // 2 y store boxes [yc][kTcM] fp32
     uint32_t exps;        // [2][kTcUnitRows] fp32 2^-e of the rows of the next two units
     uint32_t bars;
     uint32_t tmem_slot;
@@ -92,7 +94,7 @@ struct TcLayout {
     int32_t cs, xs;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
+__host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs, int yc) {
     TcLayout L;
     L.cs = cs;
     L.xs = xs;
@@ -101,7 +103,7 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
     L.xr = L.code + (uint32_t)cs * L.code_stage;
     L.x_stage = (uint32_t)kTcSG * n_pad * 128u;             // n_pad % 16 == 0: 2 KB multiples
     L.ybuf = L.xr + (uint32_t)xs * L.x_stage;
-    L.exps = L.ybuf + 2u * kTcYBox;
+    L.exps = L.ybuf + 2u * tc_ybox_bytes(yc);
     L.bars = L.exps + 2u * kTcUnitRows * 4u;
     // code_full[cs] code_empty[cs] x_full[xs] x_empty[xs] a_full[A] a_empty[A]
     // acc_full[2] acc_empty[2] exp_full[2] exp_empty[2] exp_first
@@ -114,7 +116,7 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int cs, int xs) {
 struct TcParams {
     CUtensorMap tmap_w;   // uint8 [out_dim][in_dim/2], box 128 bytes x 128 rows, 128B swizzle
     CUtensorMap tmap_x;   // fp16 [nb][in_dim], box 64 x n_pad, 128B swizzle
-    CUtensorMap tmap_y;   // fp32 [nb][out_dim], box kTcM x kTcYCols, no swizzle (when y_tma)
+    CUtensorMap tmap_y;   // fp32 [nb][out_dim], box kTcM x YC, no swizzle (when y_tma)
     const uint16_t* s;    // bf16 [out_dim][groups]
     const uint16_t* b;
     float* y;             // fp32 [nb][out_dim]
@@ -345,7 +347,10 @@ __device__ __forceinline__ float warp_row_bound(const uint16_t* s, const uint16_
     return own;
 }
 
+template <int YC>
 __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_constant__ TcParams p) {
+    static_assert(YC % kTcYCols == 0, "y boxes of whole TMEM loads");
+    constexpr int NL = YC / kTcYCols;   // TMEM loads per y box
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -536,34 +541,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
             const int buf = li % p.acc_bufs;
             mbar_wait(smem_addr(acc_full + buf), (uint32_t)(li / p.acc_bufs) & 1u, abort_flag);
             tc_fence_after();
-            // The accumulators leave 16 columns at a time in a rolled loop: the epilogue runs once
+            // The accumulators leave YC columns at a time in a rolled loop: the epilogue runs once
             // per unit, so its code is cold each time, and a short loop body fetches far fewer
-            // instruction lines than an unrolled sweep. The next 16 columns' TMEM load is in
-            // flight while the current ones are stored. With y_tma, each 16 columns go to one of
-            // two shared-memory boxes [16][128] and leave with one tensor store (the box's rows
+            // instruction lines than an unrolled sweep. The next YC columns' TMEM loads are in
+            // flight while the current ones are stored. With y_tma, each YC columns go to one of
+            // two shared-memory boxes [YC][128] and leave with one tensor store (the box's rows
             // beyond out_dim and columns beyond nb are clipped by the tensor map): a store
             // instruction per value and activation row costs far more issue time than its bytes.
-            const int nh = p.n_pad / kTcYCols;
+            const int nh = p.n_pad / YC;
 #pragma unroll 1
             for (int u = 0; u < kTcUm; ++u) {
                 const int64_t row0 = (int64_t)unit * kTcUnitRows + u * kTcM;
                 const int64_t row = row0 + rl;
                 const float eu = u == 0 ? esc[0] : esc[1];
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((buf * kTcUm + u) * p.n_pad);
-                uint32_t r[kTcYCols];
-                tc_ld16_issue(taddr, r);
-                tc_ld16_wait(r);
+                uint32_t r[NL][kTcYCols];
+#pragma unroll
+                for (int l = 0; l < NL; ++l) tc_ld16_issue(taddr + (uint32_t)(l * kTcYCols), r[l]);
+#pragma unroll
+                for (int l = 0; l < NL; ++l) tc_ld16_wait(r[l]);
 #pragma unroll 1
                 for (int h = 0; h < nh; ++h) {
-                    uint32_t rn[kTcYCols];   // the next 16 columns (the last ones again at the end)
-                    tc_ld16_issue(taddr + (uint32_t)(min(h + 1, nh - 1) * kTcYCols), rn);
-                    const int c0 = h * kTcYCols;
-                    float o[kTcYCols];
+                    uint32_t rn[NL][kTcYCols];   // the next box's columns (the last ones again at the end)
+                    const uint32_t tn = taddr + (uint32_t)(min(h + 1, nh - 1) * YC);
 #pragma unroll
-                    for (int j = 0; j < kTcYCols; ++j) o[j] = __uint_as_float(r[j]) * eu;
+                    for (int l = 0; l < NL; ++l) tc_ld16_issue(tn + (uint32_t)(l * kTcYCols), rn[l]);
+                    const int c0 = h * YC;
+                    float o[YC];
+#pragma unroll
+                    for (int l = 0; l < NL; ++l)
+#pragma unroll
+                        for (int j = 0; j < kTcYCols; ++j) o[l * kTcYCols + j] = __uint_as_float(r[l][j]) * eu;
                     if (p.silu) {
 #pragma unroll
-                        for (int j = 0; j < kTcYCols; ++j) {
+                        for (int j = 0; j < YC; ++j) {
                             const float t = o[j] / p.silu_div;
                             o[j] = t / (1.0f + expf(-t));
                         }
@@ -571,21 +582,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     if (p.y_tma) {
                         if (elected) bulk_wait_read_1();   // the store that last read this box is done with it
                         epi_sync();
-                        const uint32_t yb = ybuf + (uint32_t)(ych & 1) * (uint32_t)kTcYBox;
+                        const uint32_t yb = ybuf + (uint32_t)(ych & 1) * tc_ybox_bytes(YC);
 #pragma unroll
-                        for (int j = 0; j < kTcYCols; ++j) sts_f32(yb + (uint32_t)(j * kTcM + rl) * 4u, o[j]);
+                        for (int j = 0; j < YC; ++j) sts_f32(yb + (uint32_t)(j * kTcM + rl) * 4u, o[j]);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         epi_sync();
                         if (elected && row0 < p.out_dim) tma_store_2d(&p.tmap_y, yb, (int)row0, c0);
                         ++ych;
                     } else if (row < p.out_dim) {
 #pragma unroll
-                        for (int j = 0; j < kTcYCols; ++j)
+                        for (int j = 0; j < YC; ++j)
                             if (c0 + j < p.nb) p.y[(int64_t)(c0 + j) * p.out_dim + row] = o[j];
                     }
-                    tc_ld16_wait(rn);
 #pragma unroll
-                    for (int j = 0; j < kTcYCols; ++j) r[j] = rn[j];
+                    for (int l = 0; l < NL; ++l) tc_ld16_wait(rn[l]);
+#pragma unroll
+                    for (int l = 0; l < NL; ++l)
+#pragma unroll
+                        for (int j = 0; j < kTcYCols; ++j) r[l][j] = rn[l][j];
                 }
             }
             tc_fence_before();
@@ -743,10 +757,10 @@ std::map<int, TcDevice> g_tc_dev;
 // Layout choice: the deepest code ring that fits (its depth is the HBM prefetch distance),
 // then the x ring. The smem request never drops below half an SM, so two CTAs never share
 // one SM's TMEM (the allocation can then never wait).
-bool tc_pick_layout(int n_pad, int max_smem, TcLayout& out, uint32_t& smem_bytes) {
+bool tc_pick_layout(int n_pad, int yc, int max_smem, TcLayout& out, uint32_t& smem_bytes) {
     static const int order[6][2] = {{4, 8}, {4, 6}, {4, 4}, {3, 4}, {3, 3}, {2, 3}};
     for (int i = 0; i < 6; ++i) {
-        const TcLayout L = tc_layout(n_pad, order[i][0], order[i][1]);
+        const TcLayout L = tc_layout(n_pad, order[i][0], order[i][1], yc);
         const uint32_t need = L.total + 1024u;
         if ((int)need <= max_smem) {
             out = L;
@@ -784,20 +798,27 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
     }
+    // TMEM (512 columns): accumulators [acc_bufs][kTcUm][n_pad], then the A stages
+    // [kTcAStages][kTcUm][kTcSG][32]
+    const int a_cols = kTcAStages * kTcUm * kTcSG * kTcACols;
+    prm.acc_bufs = 2 * kTcUm * n_pad + a_cols <= 512 ? 2 : 1;
+    if (prm.acc_bufs * kTcUm * n_pad + a_cols > 512) return Q4A_ERR_UNSUPPORTED;
+    // y box width: 32 columns where one accumulator set makes the MMA wait for each unit's drain
+    const int yc = prm.acc_bufs == 1 && n_pad % 32 == 0 ? 32 : 16;
     // y through tensor stores: rows 16-byte aligned (out_dim % 4 == 0, y 16-byte aligned), and at
     // least one full box of rows so the box never exceeds the tensor.
     prm.y_tma = (out_dim % 4 == 0 && out_dim >= kTcM && reinterpret_cast<uintptr_t>(y) % 16 == 0) ? 1 : 0;
     if (prm.y_tma) {
         const cuuint64_t dims[2] = {(cuuint64_t)out_dim, (cuuint64_t)nb};
         const cuuint64_t strides[1] = {(cuuint64_t)out_dim * 4};
-        const cuuint32_t box[2] = {(cuuint32_t)kTcM, (cuuint32_t)kTcYCols};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcM, (cuuint32_t)yc};
         CUresult r = encode_tiled_cached(&prm.tmap_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
                                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
     }
     uint32_t smem_bytes = 0;
-    if (!tc_pick_layout(n_pad, dev.max_smem, prm.lay, smem_bytes)) return Q4A_ERR_UNSUPPORTED;
+    if (!tc_pick_layout(n_pad, yc, dev.max_smem, prm.lay, smem_bytes)) return Q4A_ERR_UNSUPPORTED;
     prm.s = s;
     prm.b = b;
     prm.y = y;
@@ -808,11 +829,6 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     prm.silu = silu ? 1 : 0;
     prm.silu_div = silu ? silu_div : 1.0f;
     prm.n_units = (int32_t)((out_dim + kTcUnitRows - 1) / kTcUnitRows);
-    // TMEM (512 columns): accumulators [acc_bufs][kTcUm][n_pad], then the A stages
-    // [kTcAStages][kTcUm][kTcSG][32]
-    const int a_cols = kTcAStages * kTcUm * kTcSG * kTcACols;
-    prm.acc_bufs = 2 * kTcUm * n_pad + a_cols <= 512 ? 2 : 1;
-    if (prm.acc_bufs * kTcUm * n_pad + a_cols > 512) return Q4A_ERR_UNSUPPORTED;
     prm.a_col0 = (uint32_t)(prm.acc_bufs * kTcUm * n_pad);
     uint32_t cols = 32;
     while (cols < prm.a_col0 + (uint32_t)a_cols) cols *= 2;
@@ -835,9 +851,10 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
     static const bool debug = getenv("Q4A_DEBUG") != nullptr;
     if (debug)
         fprintf(stderr, "q4a dense_tc: out=%lld in=%lld nb=%d n_pad=%d units=%d grid=%u cs=%d xs=%d acc_bufs=%d "
-                "tmem_cols=%u smem=%u\n", (long long)out_dim, (long long)in_dim, nb, n_pad, prm.n_units,
-                cfg.gridDim.x, prm.lay.cs, prm.lay.xs, prm.acc_bufs, prm.tmem_cols, smem_bytes);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, dense_tc_kernel, prm);
+                "tmem_cols=%u smem=%u y_box=%d\n", (long long)out_dim, (long long)in_dim, nb, n_pad, prm.n_units,
+                cfg.gridDim.x, prm.lay.cs, prm.lay.xs, prm.acc_bufs, prm.tmem_cols, smem_bytes, yc);
+    const cudaError_t e = yc == 32 ? cudaLaunchKernelEx(&cfg, dense_tc_kernel<32>, prm)
+                                   : cudaLaunchKernelEx(&cfg, dense_tc_kernel<16>, prm);
     if (e != cudaSuccess) return cuda_fail(e);
     return Q4A_OK;
 }
@@ -867,7 +884,9 @@ q4a_status launch_dense_tc(const uint8_t* w, const uint16_t* s, const uint16_t* 
         if (!c.attr_set) {
             cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev);
             cudaDeviceGetAttribute(&c.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-            e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
+            e = cudaFuncSetAttribute(dense_tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(dense_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, c.max_smem);
             if (e != cudaSuccess) return cuda_fail(e);
             c.attr_set = c.sm_count > 0;
         }

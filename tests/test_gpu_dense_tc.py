@@ -69,7 +69,7 @@ TC_CASES = [
     (70, 512, 300),      # three launches: 128, 128, then 44 rows
     (40000, 512, 64),    # 157 units: CTAs take a second unit
     (1100, 512, 64),     # last unit's second tile starts beyond out_dim (its y box is not stored)
-    (384, 2048, 96),     # y boxes of 16 columns: 96 = 3 x 32
+    (384, 2048, 96),     # one accumulator set: y boxes of 32 columns, 96 = 3 x 32
 ]
 
 
