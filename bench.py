@@ -226,9 +226,9 @@ def run_reference(args, rank, world):
     steps_bytes, times = [], []
     import oracle  # noqa: F401
     for i in range(args.warmup + args.steps):
-        # about a minute in all, whatever --steps and --warmup are (a repetition over every NB
-        # takes ~40-60 ms)
-        per = max(0.1, 60.0 / max(1, args.warmup + args.steps))
+        # --ref-seconds in all (a minute by default), whatever --steps and --warmup are (one
+        # repetition over every NB takes ~40-60 ms)
+        per = max(0.05, args.ref_seconds / max(1, args.warmup + args.steps))
         gbs, desc, cores = oracle_sample(seconds_target=per, nbs=tuple(int(v) for v in args.nbs.split(",")))
         if i >= args.warmup:
             times.append(gbs)
@@ -903,6 +903,8 @@ def main():
     ap.add_argument("--nbs", default="1,2,4,8,16")
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: total seconds of oracle work over all warm-up and timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload launch timings")
     ap.add_argument("--kernel", choices=sorted(KERNEL_SHAPES) + ["fused_gate_up", "moe", "prefill"], default=None,
