@@ -9,11 +9,13 @@
 // fp32 accumulators in TMEM.
 //
 // Precision: every row o gets a power-of-two factor 2^-e_o that puts its largest possible
-// weight, max_g (15|s| + |b|), in [2^13, 2^14). The operand holds w' = fp16(w * 2^-e_o),
-// computed from exact binary16 operands with one fused multiply-add (the codes become
-// exact binary16 integers), so |w' 2^e_o - w| <= 2^-11 |w| for every weight that is not
-// 2^27 below its row's largest; the accumulation is fp32 and the epilogue multiplies by
-// 2^e_o (exact).
+// weight, max_g (15|s| + |b|), in [2^-6, 2^-5). The operand holds w' = fp16(w * 2^-e_o),
+// computed from exact binary16 operands with one fused multiply-add: the masked code bits are
+// the binary16 subnormal q * 2^-24 (16 q * 2^-24 for a high nibble) and the scale operand is
+// s' * 2^24 (s' * 2^20), below 2^16 for this range. So |w' 2^e_o - w| <= 2^-11 |w| for every
+// weight that is not 2^9 below its row's largest, and at most 2^-20 of the largest otherwise
+// (binary16 subnormal spacing); the accumulation is fp32 and the epilogue multiplies by 2^e_o
+// (exact).
 //
 // Why A lives in TMEM: a 128 x N x 16 MMA costs the tensor core about 55 cycles for N <= 64
 // and 64 cycles at N = 128, while staging A through shared memory (written by the
@@ -273,26 +275,26 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cas
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // Byte k of a packed word holds elements 2k (low nibble) and 2k+1 (high nibble). Returns
-// (w[2k], w[2k+1]) as binary16: the byte is copied into both halves, masked to the low
-// nibble (half 0) and the high nibble (half 1, at 16x), turned into 1024 + code with the
-// binary16 exponent of 1024 (exact: codes are integers below 1024), 1024 is taken off
-// (exact), and one fused multiply-add applies (s', s'/16) and (b', b').
+// (w[2k], w[2k+1]) as binary16: the byte is copied into both halves and masked to the low
+// nibble (half 0) and the high nibble (half 1); as bit patterns the halves are the binary16
+// subnormals q * 2^-24 and 16 q * 2^-24 (exact), and one fused multiply-add (subnormal
+// operands are not flushed) applies (s' 2^24, s' 2^20) and (b', b').
 template <int K>
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t word, __half2 sc, __half2 bi) {
     uint32_t t;
     asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(word), "n"(0x4040 | (K << 8) | K));
-    t = (t & 0x00F0000Fu) | 0x64006400u;
-    const __half2 q = __hsub2(bits_h2(t), bits_h2(0x64006400u));
-    return h2_bits(__hfma2(q, sc, bi));
+    t &= 0x00F0000Fu;
+    return h2_bits(__hfma2(bits_h2(t), sc, bi));
 }
 
-// 2^-e for a row whose largest weight magnitude is at most m: e = floor(log2 m) - 13, so
-// m * 2^-e lies in [2^13, 2^14); e is clamped to [-120, 120] (2^-e and 2^e stay normal fp32).
+// 2^-e for a row whose largest weight magnitude is at most m: e = floor(log2 m) + 6, so
+// m * 2^-e lies in [2^-6, 2^-5); e is clamped to [-126, 126] (2^-e and 2^e stay normal fp32;
+// rows whose weights reach 2^121 are out of range and come out non-finite).
 __device__ __forceinline__ int row_exponent(float m) {
     if (!(m > 0.f) || !(m <= 3.0e38f)) return 0;
     const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
-    int e = E - 13;
-    return e < -120 ? -120 : (e > 120 ? 120 : e);
+    int e = E + 6;
+    return e < -126 ? -126 : (e > 126 ? 126 : e);
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
@@ -680,7 +682,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
                     const uint32_t bp = k < 2 ? b_cur.x : b_cur.y;
                     const float sf = bf16_to_f32((k & 1) ? (sp >> 16) : (sp & 0xFFFFu)) * dq;
                     const float bfv = bf16_to_f32((k & 1) ? (bp >> 16) : (bp & 0xFFFFu)) * dq;
-                    const __half2 sc = __floats2half2_rn(sf, sf * 0.0625f);
+                    const __half2 sc = __floats2half2_rn(sf * 16777216.0f, sf * 1048576.0f);   // 2^24, 2^20
                     const __half2 bi = __floats2half2_rn(bfv, bfv);
                     uint32_t words[4 * kChunks];
 #pragma unroll
