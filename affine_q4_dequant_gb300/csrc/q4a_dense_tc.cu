@@ -864,11 +864,14 @@ q4a_status launch_chunk(const TcDevice& dev, const uint8_t* w, const uint16_t* s
 }  // namespace
 
 bool dense_tc_eligible(const uint16_t* s, const uint16_t* b, int nb, int64_t out_dim, int64_t in_dim) {
-    // From NB 64, or from NB 13 on matrices tall enough to give every SM a 256-row unit (the
-    // GEMV kernel's 13..32-row forms lose to the contraction there: on the 4096 x 151936 LM head
-    // 154 us at NB 13..16 against 114 us, while NB 12 takes 105 us; on shorter matrices the
-    // contraction has too few units to fill the GPU).
-    const bool wide = nb >= kDenseTcMinRows || (nb >= kDenseTcTallMinRows && out_dim >= (int64_t)kDenseTcTallRows);
+    // From NB 64; from NB 9 on matrices tall enough to give every SM a 256-row unit (4096 x
+    // 151936 LM head: 87 us at NB 9..16 against 97..106 us on the GEMV kernel at NB 9..12, which
+    // keeps NB 8 at 78 us); from NB 17 on matrices of 48 units or more (4096 -> 12288: 24 us at
+    // NB 24..32 against 33..38 us, while NB 16 takes 19 us on the GEMV kernel and 23 us here).
+    // Shorter matrices have too few units to fill the GPU (12288 -> 4096, 16 units: 66..79 us
+    // at NB 16..63 against 18..76 us).
+    const bool wide = nb >= kDenseTcMinRows || (nb >= kDenseTcTallMinRows && out_dim >= (int64_t)kDenseTcTallRows) ||
+                      (nb >= kDenseTcMidMinRows && out_dim >= (int64_t)kDenseTcMidRows);
     return wide && (in_dim / kGroup) % 8 == 0 && reinterpret_cast<uintptr_t>(s) % 16 == 0 &&
            reinterpret_cast<uintptr_t>(b) % 16 == 0;
 }

@@ -24,8 +24,10 @@ constexpr int kXFragBudget = 128 * 1024; // staged activation fragments per CTA
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
 constexpr uint32_t kSuspendHintNs = 20000;        // per try_wait sleep bound
 constexpr int kDenseTcMinRows = 64;   // q4a_gemv batches this wide take the tensor-core path,
-constexpr int kDenseTcTallRows = 152 * 256;   // and from kDenseTcTallMinRows rows on matrices this tall
-constexpr int kDenseTcTallMinRows = 13;
+constexpr int kDenseTcTallRows = 152 * 256;   // from kDenseTcTallMinRows rows on matrices this tall
+constexpr int kDenseTcTallMinRows = 9;        // (a 256-row unit for every SM),
+constexpr int kDenseTcMidRows = 48 * 256;     // and from kDenseTcMidMinRows rows on matrices this tall
+constexpr int kDenseTcMidMinRows = 17;        // (where the GEMV kernel needs 4 activation tiles)
 constexpr int kCombineMaxK = 64;      // q4a_moe_combine: experts per token
 constexpr int kMaxNormGroups = 8;     // q4a_gemv_rmsnorm_grouped: normalisation segments per row
 // raw scale mode: row blocks of raw scales/biases in flight (3 where the consumers read them in

@@ -101,7 +101,8 @@ Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_d
  *   Requires nb >= 1, out_dim >= 1 (any value, odd included), in_dim >= 64,
  *   in_dim % 64 == 0; w and x 16-byte aligned; s and b 2-byte aligned.
  *   Kernel choice: the tensor-core path (weights dequantised into TMEM, tcgen05.mma) takes
- *   nb >= 64, and nb >= 13 when out_dim >= 38912 (enough 256-row units for every SM), provided
+ *   nb >= 64, nb >= 9 when out_dim >= 38912 (a 256-row unit for every SM) and nb >= 17 when
+ *   out_dim >= 12288 (48 units), provided
  *   in_dim % 512 == 0 and s, b are 16-byte aligned; everything else runs the GEMV kernel
  *   (q4a_gemv_kernel_choice tells which, without launching).
  *   The GEMV kernel keeps a CTA's

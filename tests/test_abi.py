@@ -405,16 +405,19 @@ def test_cuda_failure_is_reported(lib):
 
 
 def test_gemv_kernel_choice_rule(lib):
-    """q4a_gemv's routing (host logic, no launch): the tensor-core path from NB 64, and from
-    NB 13 on matrices of >= 38912 rows (152 units of 256 rows), when in_dim % 512 == 0 and the
-    scales and biases are 16-byte aligned; the GEMV kernel otherwise."""
+    """q4a_gemv's routing (host logic, no launch): the tensor-core path from NB 64, from NB 9
+    on matrices of >= 38912 rows (152 units of 256 rows) and from NB 17 on matrices of >= 12288
+    rows (48 units), when in_dim % 512 == 0 and the scales and biases are 16-byte aligned; the
+    GEMV kernel otherwise."""
     A = 0x10000
     k = lib.q4a_gemv_kernel_choice
-    assert [k(A, A, nb, 151936, 4096) for nb in (1, 8, 12, 13, 16, 17, 32, 63, 64, 128, 300)] == \
-        [0, 0, 0, 1, 1, 1, 1, 1, 1, 1, 1]
-    assert [k(A, A, nb, 38911, 4096) for nb in (13, 32, 63, 64)] == [0, 0, 0, 1]
-    assert [k(A, A, nb, 38912, 4096) for nb in (12, 13)] == [0, 1]
-    assert [k(A, A, nb, 12288, 4096) for nb in (1, 16, 32, 64)] == [0, 0, 0, 1]
+    assert [k(A, A, nb, 151936, 4096) for nb in (1, 8, 9, 12, 13, 16, 17, 32, 63, 64, 128, 300)] == \
+        [0, 0, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1]
+    assert [k(A, A, nb, 38911, 4096) for nb in (9, 16, 17, 32, 63, 64)] == [0, 0, 1, 1, 1, 1]
+    assert [k(A, A, nb, 38912, 4096) for nb in (8, 9)] == [0, 1]
+    assert [k(A, A, nb, 12288, 4096) for nb in (1, 9, 16, 17, 32, 64)] == [0, 0, 0, 1, 1, 1]
+    assert [k(A, A, nb, 12287, 4096) for nb in (17, 63, 64)] == [0, 0, 1]
+    assert [k(A, A, nb, 4096, 12288) for nb in (16, 32, 63, 64)] == [0, 0, 0, 1]
     assert k(A + 2, A, 64, 4096, 4096) == 0        # scales not 16-byte aligned
     assert k(A, A + 8, 64, 4096, 4096) == 0        # biases not 16-byte aligned
     assert k(A, A, 64, 4096, 4096 + 64) == 0       # 65 groups: not a multiple of 8

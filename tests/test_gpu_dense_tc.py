@@ -141,8 +141,8 @@ def test_wide_batch_falls_back_when_ineligible():
 
 def test_wide_batch_runs_on_the_tensor_core_kernel():
     """The routing a call takes (q4a_gemv_kernel_choice, the function the dispatch itself calls):
-    NB 64 on a short matrix and NB 13 on a tall one run the tcgen05 kernel, NB 16 on a short
-    matrix and NB 12 on a tall one the GEMV kernel; each result meets the oracle's bar."""
+    NB 64 on a short matrix and NB 9 on a tall one run the tcgen05 kernel, NB 16 on a short
+    matrix and NB 8 on a tall one the GEMV kernel; each result meets the oracle's bar."""
     packed, s, b, x = case(256, 512, 64, 16)
     sd, bd = dev(s), dev(b)
     assert q4a.gemv_kernel_choice(sd, bd, 64, 256, 512) == "tcgen05"
@@ -151,10 +151,19 @@ def test_wide_batch_runs_on_the_tensor_core_kernel():
     check(gemv(packed, s, b, x, 256, s_dev=sd, b_dev=bd), y_ref, bound, "NB 64 (tcgen05)")
     check(gemv(packed, s, b, x[:16], 256, s_dev=sd, b_dev=bd), y_ref[:16], bound[:16], "NB 16 (GEMV)")
     out_dim = 152 * 256
-    packed, s, b, x = case(out_dim, 512, 13, 17)
+    packed, s, b, x = case(out_dim, 512, 9, 17)
     sd, bd = dev(s), dev(b)
-    assert q4a.gemv_kernel_choice(sd, bd, 13, out_dim, 512) == "tcgen05"
-    assert q4a.gemv_kernel_choice(sd, bd, 12, out_dim, 512) == "gemv"
+    assert q4a.gemv_kernel_choice(sd, bd, 9, out_dim, 512) == "tcgen05"
+    assert q4a.gemv_kernel_choice(sd, bd, 8, out_dim, 512) == "gemv"
     y_ref, bound = oracle.gemv(packed, s, b, x)
-    check(gemv(packed, s, b, x, out_dim, s_dev=sd, b_dev=bd), y_ref, bound, "tall NB 13 (tcgen05)")
-    check(gemv(packed, s, b, x[:12], out_dim, s_dev=sd, b_dev=bd), y_ref[:12], bound[:12], "tall NB 12 (GEMV)")
+    check(gemv(packed, s, b, x, out_dim, s_dev=sd, b_dev=bd), y_ref, bound, "tall NB 9 (tcgen05)")
+    check(gemv(packed, s, b, x[:8], out_dim, s_dev=sd, b_dev=bd), y_ref[:8], bound[:8], "tall NB 8 (GEMV)")
+    # 48 units: from NB 17
+    out_dim = 48 * 256
+    packed, s, b, x = case(out_dim, 512, 17, 18)
+    sd, bd = dev(s), dev(b)
+    assert q4a.gemv_kernel_choice(sd, bd, 17, out_dim, 512) == "tcgen05"
+    assert q4a.gemv_kernel_choice(sd, bd, 16, out_dim, 512) == "gemv"
+    y_ref, bound = oracle.gemv(packed, s, b, x)
+    check(gemv(packed, s, b, x, out_dim, s_dev=sd, b_dev=bd), y_ref, bound, "NB 17 on 48 units (tcgen05)")
+    check(gemv(packed, s, b, x[:16], out_dim, s_dev=sd, b_dev=bd), y_ref[:16], bound[:16], "NB 16 on 48 units (GEMV)")
