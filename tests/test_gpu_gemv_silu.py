@@ -30,7 +30,9 @@ def dev(a: np.ndarray) -> torch.Tensor:
 
 @pytest.mark.parametrize("out_dim,in_dim,nb,div", [(256, 512, 1, 1.0), (300, 1024, 9, -0.5), (129, 4096, 33, 3.7),
                                                    (513, 1024, 64, 0.25), (200, 512, 100, -2.0),
-                                                   (40, 12288, 4, 1.5)])
+                                                   (40, 12288, 4, 1.5),
+                                                   (300, 512, 128, 0.5),      # tensor cores, 32-column y boxes
+                                                   (152 * 256, 512, 9, 2.0)])  # tall: tensor cores from NB 9
 def test_gemv_silu_matches_oracle(out_dim, in_dim, nb, div):
     rng = np.random.default_rng(out_dim + nb)
     codes = rng.integers(0, 16, size=(out_dim, in_dim), dtype=np.uint8)
