@@ -1638,16 +1638,29 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
              (uint64_t)(16 * mt) * (uint64_t)G + 7u <= kRawBudget)
         sbm_full = kSbRaw;
     auto sbmode = [&](int c) { return c == 1 ? sbm_full : kSbTma; };
+    // Row-block height with c-CTA clusters: plain dense products whose clusters get at most 2 or
+    // 4 tiles run the kernel built for row blocks of that height (the default height would spend
+    // mma work on absent rows). Decided per candidate c, so that the shared-memory fit of c is
+    // judged with the row blocks c would run.
+    const bool short_ok = MAXSEG == kDenseMaxSeg && !fg && !L.rmsnorm && cb == 4 && nt <= 2;
+    const int mt_default = mt;
+    auto mt_for = [&](int c) {
+        if (!short_ok) return mt_default;
+        const int64_t clusters = di.sm_count / c;
+        const int64_t per = (n_tiles + clusters - 1) / clusters;
+        return per <= 2 ? 2 : (per <= 4 ? 4 : mt_default);
+    };
     auto sbufs = [&](int c) {
         const int64_t clusters = di.sm_count / c;
-        return (n_tiles + clusters - 1) / clusters <= mt_units && L.nseg == 1 ? 1 : 2;
+        const int units = fg ? mt_for(c) / 2 : mt_for(c);
+        return (n_tiles + clusters - 1) / clusters <= units && L.nseg == 1 ? 1 : 2;
     };
     auto fits = [&](int c, int stages) {
         const int g = slice(c);
         if (c > 1 && sbm_full != kSbTma) return false;
         if (c > 1 && (int64_t)g * (c - 1) >= G) return false;
         if (xfrag_bytes(g, ntm) > (uint32_t)kXFragBudget) return false;
-        return (int)(smem_layout(nt, mt, stages, g, ntm, sbmode(c), sbufs(c), cb, 0, rawd).total + 1024) <=
+        return (int)(smem_layout(nt, mt_for(c), stages, g, ntm, sbmode(c), sbufs(c), cb, 0, rawd).total + 1024) <=
                di.max_smem_optin;
     };
     int C = 0;
@@ -1655,7 +1668,8 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
         if (!fits(c, 3)) continue;
         if (C == 0) C = c;                       // smallest that fits at all
         const int q = cluster_capacity(nt, L.rmsnorm, L.experts, c,
-                                       smem_layout(nt, mt, 3, slice(c), ntm, sbmode(c), sbufs(c), cb, 0, rawd).total + 1024,
+                                       smem_layout(nt, mt_for(c), 3, slice(c), ntm, sbmode(c), sbufs(c), cb, 0, rawd).total +
+                                           1024,
                                        cb, fg);
         if (q <= 0) continue;
         if (tile_work >= 3 * (int64_t)q && 10 * (int64_t)q * c >= 9 * (int64_t)di.sm_count) {
@@ -1666,17 +1680,9 @@ q4a_status launch_gemv_t(const GemvLaunch& L, cudaStream_t stream) {
     }
     if (C == 0) return Q4A_ERR_UNSUPPORTED;
     const int gs = slice(C);
-    // Plain dense products whose clusters get at most 2 or 4 tiles run the kernel built for
-    // row blocks of that height (the default height would spend mma work on absent rows).
-    if (MAXSEG == kDenseMaxSeg && !fg && !L.rmsnorm && cb == 4 && nt <= 2) {
-        const int q = cluster_capacity(nt, false, false, C, smem_layout(nt, mt, 3, gs, ntm, sbmode(C), sbufs(C), cb).total + 1024,
-                                       cb, false);
-        const int64_t per = q > 0 ? (n_tiles + q - 1) / q : mt;
-        const int short_mt = per <= 2 ? 2 : (per <= 4 ? 4 : mt);
-        if (short_mt < mt) {
-            mt = short_mt;
-            mt_units = short_mt;
-        }
+    if (mt_for(C) < mt) {
+        mt = mt_for(C);
+        mt_units = mt;
     }
     int stages = 8;
     while (stages > 2 && !fits(C, stages)) --stages;

@@ -110,7 +110,8 @@ Q4A_API q4a_status q4a_xsum(float* xsum, const uint16_t* x, int nb, int64_t in_d
  *   rows longer than that budget allows, even split across 8 CTAs, return
  *   Q4A_ERR_UNSUPPORTED before any launch. Every in_dim up to 98304 runs at NB 1, up to
  *   65536 at NB <= 4, up to 16384 at NB <= 16 and up to 4096 at any NB (8192, 12288 and
- *   16384 run at any NB too).
+ *   16384 run at any NB too); matrices of a few tiles reach further (short row blocks leave
+ *   more room: 131072 inputs at NB 1 on 16 rows).
  *   ("BATCH_MSL", hyperconnection.metal fn_qmv_silu_b over quantized_rows.metal
  *   fn_q4_rows_h; experts.metal fn_moe_down_b for the two-rows-per-pass form.)
  */

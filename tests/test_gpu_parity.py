@@ -99,7 +99,8 @@ GEMV_CASES = [
     (24, 12288, 2),     # long rows, cluster of 4
     (17, 12288, 16),    # long rows, cluster of 8
     (2000, 256, 4),     # many tiles per cluster
-    (40, 98304, 1),     # 1536 groups, the longest row at NB <= 8: an 8-CTA K split
+    (40, 98304, 1),     # 1536 groups, the longest row at NB <= 8 on any matrix: an 8-CTA K split
+    (16, 131072, 1),    # 2048 groups on one tile: an 8-CTA K split of 2-tile row blocks
     (20, 576, 63),      # the widest batch below the tensor-core path (two segments)
     (10, 576, 256),     # 9 groups keep NB 256 on the GEMV kernel: eight 32-row segments
 ]
@@ -107,9 +108,10 @@ GEMV_CASES = [
 
 def test_gemv_row_longer_than_the_budget_is_unsupported():
     """The GEMV kernel keeps a CTA's K-slice of activations and of the row block's scales and
-    biases in shared memory: 2048 groups at NB 1 exceed it even split 8 ways, and the call
-    reports Q4A_ERR_UNSUPPORTED before launching anything."""
-    codes, s, b, x = ragged_case(16, 131072, 1, 5)
+    biases in shared memory: 16384 groups at NB 1 exceed it even split 8 ways (2048 groups of
+    activation fragments per CTA), and the call reports Q4A_ERR_UNSUPPORTED before launching
+    anything."""
+    codes, s, b, x = ragged_case(16, 1048576, 1, 5)
     with pytest.raises(q4a.Q4AError) as e:
         run_gemv(oracle.pack(codes), s, b, x, 16)
     assert e.value.status == 4
