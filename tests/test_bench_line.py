@@ -26,3 +26,23 @@ def test_reference_line_has_the_contract_keys():
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] == 1 and cb["sample"]
     assert cb["host_cores"] >= 1 and cb["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_host_info_names_an_arm_cpu_from_its_part_number(monkeypatch):
+    """Arm hosts list implementer and part numbers instead of a model name in /proc/cpuinfo."""
+    import builtins
+    import io
+
+    import bench
+
+    text = ("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\n"
+            "CPU variant\t: 0x0\nCPU part\t: 0xd4f\nCPU revision\t: 0\n")
+    real_open = builtins.open
+
+    def fake_open(path, *a, **k):
+        return io.StringIO(text) if path == "/proc/cpuinfo" else real_open(path, *a, **k)
+
+    monkeypatch.setattr(builtins, "open", fake_open)
+    info = bench.host_info()
+    assert info["cpu_model"] == "Arm Neoverse-V2 (CPU implementer 0x41, part 0xd4f)"
+    assert info["host_cores"] >= 1
