@@ -783,9 +783,9 @@ def per_config(q4a, torch, reps=40):
 
     out = {
         "gemv_256x512": brief(time_dense(q4a, torch, 256, 512, [1], reps=reps)),
-        "gate_up_4096x12288": brief(time_dense(q4a, torch, INTER2, HIDDEN, [1, 2, 4, 8, 16], reps=reps)),
+        "gate_up_4096x12288": brief(time_dense(q4a, torch, INTER2, HIDDEN, [1, 2, 4, 8, 16, 32, 64], reps=reps)),
         "fused_rmsnorm_gate_up_silu_4096x2x6144": brief(time_fused_gate_up(q4a, torch, [1, 2, 4, 8, 16], reps=reps)),
-        "down_12288x4096": brief(time_dense(q4a, torch, DOWN_OUT, DOWN_IN, [1, 4, 16], reps=reps)),
+        "down_12288x4096": brief(time_dense(q4a, torch, DOWN_OUT, DOWN_IN, [1, 4, 8, 16, 32, 64], reps=reps)),
         "lm_head_4096x151936": brief(time_dense(q4a, torch, 151936, HIDDEN, [1, 8, 32, 64, 128], reps=reps)),
     }
     moe = time_moe(q4a, torch, reps=reps)
